@@ -1,0 +1,249 @@
+"""CPU oracle for MTraining's dynamic Vertical-Slash sparse attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / ``--impl reference`` legs may import this
+package.  The product path (the CUDA library and its binding) never does.
+
+Plain, slow and fp64: the arithmetic lives in ``vs_oracle.c`` (loaded with
+ctypes) plus a few numpy helpers here that follow the pages' definitions
+directly:
+
+* ``estimate`` / ``topk`` / ``select`` -- Algorithm 1 of *MTraining:
+  Distributed Dynamic Sparse Attention for Efficient Ultra-Long Context
+  Training*: the last-``last_q`` observation window, ``sum_v`` / ``sum_s`` and
+  ``argtopk`` (fixed budgets; ties go to the lower index).
+* ``rows`` / ``keys`` / ``attention`` -- masked softmax attention on the VS
+  mask and its gradients by Eq. 1 (dS) and Eq. 2 (dV, dQ, dK).
+* ``merge`` -- ``merge_out_and_lse`` of Algorithm 2.
+* ``stripe_positions`` / ``striped_permute`` -- 64-token block-level
+  striping (section 4.2 (ii)).
+
+Inputs are converted to float64 (bf16 values widen exactly); all arithmetic is fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.ora_topk.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+        L.ora_estimate.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                                          ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p]
+        L.ora_rows.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p]
+        L.ora_keys.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.ora_mask_count.argtypes = [ctypes.c_void_p]
+        L.ora_mask_count.restype = ctypes.c_int64
+        L.ora_mask_dense.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        L.ora_stripe_positions.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_void_p]
+        L.ora_merge.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p, ctypes.c_double,
+                                ctypes.c_void_p, ctypes.c_void_p]
+        L.ora_num_threads.restype = ctypes.c_int
+        L.ora_row_stats.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p]
+        _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().ora_num_threads())
+
+
+def _p(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+# ------------------------------------------------------------------ selection
+def estimate(q: np.ndarray, k: np.ndarray, last_q: int, scale: float):
+    """sum_v and sum_s of the last-``last_q`` causal softmax (Algorithm 1).
+
+    q: [B, N, Hq, d], k: [B, N, Hkv, d].
+    Returns (v, s), each float64 [B, Hq, N]: v[m] = sum_i A_hat[i, m],
+    s[o] = sum_i A_hat[i, n_i - o] with n_i = N - last_q + i.
+    """
+    q, k = _f64(q), _f64(k)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    v = np.zeros((B, Hq, N), np.float64)
+    s = np.zeros((B, Hq, N), np.float64)
+    lib().ora_estimate(B, N, Hq, Hkv, d, _p(q), _p(k), int(last_q), float(scale), _p(v), _p(s))
+    return v, s
+
+
+def topk(score: np.ndarray, k: int) -> np.ndarray:
+    """argtopk under the total order (score descending, index ascending),
+    returned sorted ascending.  Float32 scores widen to fp64 exactly, so the
+    same routine replays a selection made on float32 scores."""
+    score = np.ascontiguousarray(score, dtype=np.float64)
+    out = np.zeros(int(k), np.int32)
+    lib().ora_topk(int(score.shape[0]), _p(score), int(k), _p(out))
+    return out
+
+
+def select(v: np.ndarray, s: np.ndarray, kv: int, ks: int):
+    """Per (b, h): iv = argtopk(v, kv), is = argtopk(s, ks)."""
+    B, H, N = v.shape
+    iv = np.zeros((B, H, kv), np.int32)
+    is_ = np.zeros((B, H, ks), np.int32)
+    for b in range(B):
+        for h in range(H):
+            iv[b, h] = topk(v[b, h], kv)
+            is_[b, h] = topk(s[b, h], ks)
+    return iv, is_
+
+
+# ------------------------------------------------------------------ attention
+class _Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Nq", ctypes.c_int), ("Nk", ctypes.c_int), ("Hq", ctypes.c_int),
+                ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("n_global", ctypes.c_int64),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dout", ctypes.c_void_p),
+                ("qpos", ctypes.c_void_p), ("kpos", ctypes.c_void_p), ("iv", ctypes.c_void_p),
+                ("is_", ctypes.c_void_p), ("kv", ctypes.c_int), ("ks", ctypes.c_int), ("scale", ctypes.c_double)]
+
+
+class Problem:
+    """One VS attention problem.
+
+    q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d], dout [B, Nq, Hq, d] or None;
+    iv [B, Hq, kv] and is_ [B, Hq, ks] index the global sequence of length
+    ``n_global``; qpos / kpos give each local row's / key's global position
+    (identity when None).
+    """
+
+    def __init__(self, q, k, v, iv, is_, scale, dout=None, qpos=None, kpos=None, n_global=None):
+        self.q, self.k, self.v = _f64(q), _f64(k), _f64(v)
+        self.dout = None if dout is None else _f64(dout)
+        B, Nq, Hq, d = self.q.shape
+        Nk, Hkv = self.k.shape[1], self.k.shape[2]
+        self.iv = np.ascontiguousarray(iv, dtype=np.int32)
+        self.is_ = np.ascontiguousarray(is_, dtype=np.int32)
+        self.qpos = np.arange(Nq, dtype=np.int64) if qpos is None else np.ascontiguousarray(qpos, np.int64)
+        self.kpos = np.arange(Nk, dtype=np.int64) if kpos is None else np.ascontiguousarray(kpos, np.int64)
+        self.n_global = int(n_global if n_global is not None else max(Nq, Nk))
+        assert self.iv.shape[:2] == (B, Hq) and self.is_.shape[:2] == (B, Hq)
+        assert Hq % Hkv == 0
+        self.shape = (B, Nq, Nk, Hq, Hkv, d)
+        self.scale = float(scale)
+        self._c = _Problem(B, Nq, Nk, Hq, Hkv, d, self.n_global, self.q.ctypes.data, self.k.ctypes.data,
+                           self.v.ctypes.data, None if self.dout is None else self.dout.ctypes.data,
+                           self.qpos.ctypes.data, self.kpos.ctypes.data, self.iv.ctypes.data, self.is_.ctypes.data,
+                           self.iv.shape[2], self.is_.shape[2], self.scale)
+
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
+def rows(p: Problem, rows_bhn: np.ndarray):
+    """Forward (O, LSE) and, when dout is set, dQ for the given (b, h, n) rows."""
+    rows_bhn = np.ascontiguousarray(rows_bhn, dtype=np.int32).reshape(-1, 3)
+    R, d = rows_bhn.shape[0], p.shape[5]
+    o = np.zeros((R, d), np.float64)
+    lse = np.zeros(R, np.float64)
+    dq = np.zeros((R, d), np.float64) if p.dout is not None else None
+    lib().ora_rows(p.ref(), R, _p(rows_bhn), _p(o), _p(lse), None if dq is None else _p(dq))
+    return o, lse, dq
+
+
+def row_stats(p: Problem, rows_bhn: np.ndarray):
+    """LSE_n and D_n = sum_m dA_nm A_nm (Eq. 1's row sum) for (b, h, n) rows."""
+    rows_bhn = np.ascontiguousarray(rows_bhn, dtype=np.int32).reshape(-1, 3)
+    R = rows_bhn.shape[0]
+    lse = np.zeros(R, np.float64)
+    D = np.zeros(R, np.float64)
+    lib().ora_row_stats(p.ref(), R, _p(rows_bhn), _p(lse), _p(D))
+    return lse, D
+
+
+def keys(p: Problem, keys_bkm: np.ndarray):
+    """dK, dV (summed over the query heads of the KV group) for (b, hk, m) keys."""
+    assert p.dout is not None
+    keys_bkm = np.ascontiguousarray(keys_bkm, dtype=np.int32).reshape(-1, 3)
+    R, d = keys_bkm.shape[0], p.shape[5]
+    dk = np.zeros((R, d), np.float64)
+    dv = np.zeros((R, d), np.float64)
+    lib().ora_keys(p.ref(), R, _p(keys_bkm), _p(dk), _p(dv))
+    return dk, dv
+
+
+def attention(p: Problem):
+    """Every output of the problem: O [B,Nq,Hq,d], LSE [B,Hq,Nq] and, with
+    dout, dQ [B,Nq,Hq,d], dK / dV [B,Nk,Hkv,d].  Small cases only."""
+    B, Nq, Nk, Hq, Hkv, d = p.shape
+    bb, hh, nn = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(Nq), indexing="ij")
+    r = np.stack([bb.ravel(), hh.ravel(), nn.ravel()], 1)
+    o, lse, dq = rows(p, r)
+    O = o.reshape(B, Hq, Nq, d).transpose(0, 2, 1, 3).copy()
+    LSE = lse.reshape(B, Hq, Nq)
+    out = {"o": O, "lse": LSE}
+    if p.dout is not None:
+        out["dq"] = dq.reshape(B, Hq, Nq, d).transpose(0, 2, 1, 3).copy()
+        bb, hh, mm = np.meshgrid(np.arange(B), np.arange(Hkv), np.arange(Nk), indexing="ij")
+        kk = np.stack([bb.ravel(), hh.ravel(), mm.ravel()], 1)
+        dk, dv = keys(p, kk)
+        out["dk"] = dk.reshape(B, Hkv, Nk, d).transpose(0, 2, 1, 3).copy()
+        out["dv"] = dv.reshape(B, Hkv, Nk, d).transpose(0, 2, 1, 3).copy()
+    return out
+
+
+def mask_dense(p: Problem, b: int, h: int) -> np.ndarray:
+    """The VS mask of one head as a dense bool [Nq, Nk] (small cases only)."""
+    B, Nq, Nk = p.shape[:3]
+    out = np.zeros((Nq, Nk), np.uint8)
+    lib().ora_mask_dense(p.ref(), int(b), int(h), _p(out))
+    return out.astype(bool)
+
+
+def mask_count(p: Problem) -> int:
+    """|M| summed over (b, h, n): the effective mask area."""
+    return int(lib().ora_mask_count(p.ref()))
+
+
+# ------------------------------------------------------- striping and merging
+def stripe_positions(N: int, W: int, stripe: int, r: int) -> np.ndarray:
+    """Global positions of worker r's tokens under block-level striping."""
+    pos = np.zeros(N // W, np.int64)
+    lib().ora_stripe_positions(int(N), int(W), int(stripe), int(r), _p(pos))
+    return pos
+
+
+def striped_permute(x: np.ndarray, W: int, stripe: int, inverse: bool = False) -> np.ndarray:
+    """x [B, N, H, d] -> [W, B, N/W, H, d] shards (or back with inverse=True):
+    global block j goes to shard j mod W, local block j // W."""
+    if not inverse:
+        B, N = x.shape[:2]
+        out = np.empty((W, B, N // W) + x.shape[2:], x.dtype)
+        for j in range(N // stripe):
+            out[j % W, :, (j // W) * stripe:(j // W + 1) * stripe] = x[:, j * stripe:(j + 1) * stripe]
+        return out
+    W_, B, Nl = x.shape[:3]
+    N = Nl * W_
+    out = np.empty((B, N) + x.shape[3:], x.dtype)
+    for j in range(N // stripe):
+        out[:, j * stripe:(j + 1) * stripe] = x[j % W_, :, (j // W_) * stripe:(j // W_ + 1) * stripe]
+    return out
+
+
+def merge(o1, l1, o2, l2):
+    """merge_out_and_lse of Algorithm 2 for one row (fp64)."""
+    o1 = np.ascontiguousarray(o1, np.float64)
+    o2 = np.ascontiguousarray(o2, np.float64)
+    o = np.zeros_like(o1)
+    l = ctypes.c_double(0.0)
+    lib().ora_merge(int(o1.shape[0]), _p(o1), float(l1), _p(o2), float(l2), _p(o), ctypes.byref(l))
+    return o, l.value

@@ -1,0 +1,192 @@
+"""Seeded synthetic inputs for Vertical-Slash sparse attention.
+
+This module is shared by the tests, the benchmark, the CPU oracle side and
+the CUDA side.  It holds none of the method's arithmetic: it only draws
+Gaussian tensors, applies rotary position embeddings and plants vertical and
+slash structure, then rounds to bf16.
+
+Recipe for one sequence (seeded numpy PCG64, float32 until the final
+round-to-nearest-even bf16):
+
+1. Q, K, V, dO ~ i.i.d. N(0, 1) with shape [N, H, d].
+2. Rotate-half RoPE on Q and K, theta_i = 10000^(-2i/d) for i < d/2, pairing
+   channel i with i + d/2, positions 0..N-1 (the convention whose dot product
+   is the expansion in the proof of Theorem 3.1 of the MTraining paper).
+3. Vertical plant: per KV head, ``n_out`` key rows chosen without
+   replacement are multiplied by 4 (outlier tokens with large key norm,
+   section 3.2).
+4. Slash plant: for each planted offset o and every n >= o, in post-RoPE
+   space q[n, h] += c * k[n - o, h // g] with c = gamma / sqrt(#planted
+   offsets).  Each planted diagonal gains about gamma * sqrt(d / #planted)
+   logits; the other logits gain noise of standard deviation about gamma.
+   Planted offsets are either ``n_slash`` random offsets in [1, N/8) or the
+   contiguous band [1, w].
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+ROPE_THETA = 10000.0
+OUTLIER_SCALE = 4.0
+SLASH_GAMMA = 1.0
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest, ties to even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    rounding = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    out = ((u + rounding) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def bf16_to_f32(u: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact float32 values."""
+    return (np.ascontiguousarray(u, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def rope_tables(N: int, d: int, theta: float = ROPE_THETA, positions: Optional[np.ndarray] = None):
+    half = d // 2
+    inv = theta ** (-2.0 * np.arange(half, dtype=np.float64) / d)
+    pos = np.arange(N, dtype=np.float64) if positions is None else np.asarray(positions, np.float64)
+    ang = pos[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def apply_rope(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """Rotate-half RoPE on x [N, H, d] (float32), in place and returned."""
+    half = x.shape[-1] // 2
+    c = cos[:, None, :]
+    s = sin[:, None, :]
+    lo = x[..., :half].copy()
+    hi = x[..., half:].copy()
+    x[..., :half] = lo * c - hi * s
+    x[..., half:] = hi * c + lo * s
+    return x
+
+
+@dataclasses.dataclass
+class SeqSpec:
+    """Planting recipe of one sequence."""
+    seed: int
+    n_out: int = 0                 # outlier key columns per KV head
+    n_slash: int = 0               # random planted diagonals in [1, N/8)
+    band: int = 0                  # or a contiguous planted band [1, band]
+    gamma: float = SLASH_GAMMA
+
+
+@dataclasses.dataclass
+class Workload:
+    """A VS attention workload: shapes, budgets and per-sequence recipes."""
+    name: str
+    N: int
+    Hq: int
+    Hkv: int
+    d: int
+    kv: int
+    ks: int
+    seqs: List[SeqSpec]
+    last_q: int = 64
+    world: int = 1                 # striped-shard mode: number of workers
+    stripe: int = 64
+
+    @property
+    def B(self) -> int:
+        return len(self.seqs)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+def workloads() -> dict:
+    """The named workloads (Qwen2.5-3B attention shapes: 16 query heads,
+    2 KV heads, head_dim 128, except the tiny case)."""
+    W = {}
+    W["tiny-1k"] = Workload("tiny-1k", N=1024, Hq=2, Hkv=1, d=64, kv=32, ks=32,
+                            seqs=[SeqSpec(seed=1, n_out=8)])
+    W["qwen3b-32k"] = Workload("qwen3b-32k", N=32768, Hq=16, Hkv=2, d=128, kv=1024, ks=2048,
+                               seqs=[SeqSpec(seed=2, n_out=64, n_slash=16)])
+    W["qwen3b-128k"] = Workload("qwen3b-128k", N=131072, Hq=16, Hkv=2, d=128, kv=1024, ks=2048,
+                                seqs=[SeqSpec(seed=3, n_out=256, n_slash=32)])
+    W["qwen3b-512k-striped8"] = Workload("qwen3b-512k-striped8", N=524288, Hq=16, Hkv=2, d=128, kv=1024,
+                                         ks=2048, seqs=[SeqSpec(seed=4, n_out=256, n_slash=32)], world=8)
+    W["batch4-64k"] = Workload("batch4-64k", N=65536, Hq=16, Hkv=2, d=128, kv=1024, ks=2048,
+                               seqs=[SeqSpec(seed=10, n_out=0, band=16), SeqSpec(seed=11, n_out=16, band=64),
+                                     SeqSpec(seed=12, n_out=128, band=256), SeqSpec(seed=13, n_out=512, band=1024)])
+    W["dense-64k"] = Workload("dense-64k", N=65536, Hq=16, Hkv=2, d=128, kv=1024, ks=65536,
+                              seqs=[SeqSpec(seed=14, n_out=0)])
+    return W
+
+
+def make_sequence(N: int, Hq: int, Hkv: int, d: int, spec: SeqSpec, with_dout: bool = True):
+    """One sequence: dict of bf16 bit arrays q, k, v, dout ([N, H, d] uint16)
+    plus the planted columns / offsets for reference."""
+    rng = np.random.Generator(np.random.PCG64(spec.seed))
+    q = rng.standard_normal((N, Hq, d), dtype=np.float32)
+    k = rng.standard_normal((N, Hkv, d), dtype=np.float32)
+    v = rng.standard_normal((N, Hkv, d), dtype=np.float32)
+    dout = rng.standard_normal((N, Hq, d), dtype=np.float32) if with_dout else None
+    cos, sin = rope_tables(N, d)
+    apply_rope(q, cos, sin)
+    apply_rope(k, cos, sin)
+    cols = np.zeros((Hkv, spec.n_out), np.int64)
+    for hk in range(Hkv):
+        if spec.n_out:
+            cols[hk] = np.sort(rng.choice(N, size=spec.n_out, replace=False))
+            k[cols[hk], hk, :] *= OUTLIER_SCALE
+    if spec.band:
+        offs = np.arange(1, min(spec.band, N - 1) + 1, dtype=np.int64)
+    elif spec.n_slash:
+        hi = max(2, N // 8)
+        offs = np.sort(rng.choice(np.arange(1, hi), size=min(spec.n_slash, hi - 1), replace=False))
+    else:
+        offs = np.zeros(0, np.int64)
+    if offs.size:
+        g = Hq // Hkv
+        c = np.float32(spec.gamma / math.sqrt(offs.size))
+        if spec.band:
+            # contiguous band [1, w]: add[n] = sum_{m = n-w}^{n-1} k[m], via
+            # an fp64 exclusive prefix sum over positions
+            pre = np.zeros((N + 1, Hkv, d), np.float64)
+            np.cumsum(k, axis=0, dtype=np.float64, out=pre[1:])
+            n = np.arange(N)
+            lo = np.maximum(n - offs.size, 0)
+            add = (pre[n] - pre[lo]).astype(np.float32)
+            del pre
+        else:
+            add = np.zeros((N, Hkv, d), np.float32)
+            for o in offs:
+                add[o:] += k[: N - o]
+        add *= c
+        q += np.repeat(add, g, axis=1)
+    out = {"q": bf16_round(q), "k": bf16_round(k), "v": bf16_round(v),
+           "planted_cols": cols, "planted_offsets": offs}
+    if with_dout:
+        out["dout"] = bf16_round(dout)
+    return out
+
+
+def make_batch(w: Workload, with_dout: bool = True, seqs: Optional[Sequence[int]] = None):
+    """All sequences of a workload stacked to [B, N, H, d] bf16 bit arrays."""
+    idx = list(range(w.B)) if seqs is None else list(seqs)
+    parts = [make_sequence(w.N, w.Hq, w.Hkv, w.d, w.seqs[i], with_dout) for i in idx]
+    out = {key: np.stack([p[key] for p in parts]) for key in ("q", "k", "v") + (("dout",) if with_dout else ())}
+    out["planted_cols"] = [p["planted_cols"] for p in parts]
+    out["planted_offsets"] = [p["planted_offsets"] for p in parts]
+    return out
+
+
+def small_workload(N: int, Hq: int, Hkv: int, d: int, kv: int, ks: int, seed: int, n_out: int = 0,
+                   n_slash: int = 0, band: int = 0, B: int = 1, last_q: int = 64, world: int = 1) -> Workload:
+    """An ad-hoc workload for tests."""
+    return Workload(f"N{N}-H{Hq}x{Hkv}-d{d}", N=N, Hq=Hq, Hkv=Hkv, d=d, kv=kv, ks=ks,
+                    seqs=[SeqSpec(seed=seed + i, n_out=n_out, n_slash=n_slash, band=band) for i in range(B)],
+                    last_q=last_q, world=world)
