@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) Vertical-Slash sparse attention: the hot path of MTraining's
+dynamic sparse attention as a C-ABI CUDA library (``libvs.so``) with a thin
+Python binding of the same names.
+
+    vs_estimate           online vertical / slash selection (Algorithm 1)
+    vs_build_block_index  sparse index arena (sparseformat / convert_index)
+    vs_attn_fwd           sparse attention forward (O, LSE; merge mode)
+    vs_attn_bwd           sparse attention backward (dQ, dK, dV)
+    striped_permute       64-token block-level striping
+    vs_check_status       device status word of a workspace or arena
+"""
+from ._binding import (VSError, make_shape, make_stripe, striped_permute, vs_attn_bwd, vs_attn_fwd,
+                       vs_build_block_index, vs_check_status, vs_estimate, vs_index_counts, lib, launch_count,
+                       status_string)
+from .pipeline import VSAttention, flop_counts
+
+__all__ = ["VSError", "make_shape", "make_stripe", "striped_permute", "vs_attn_bwd", "vs_attn_fwd",
+           "vs_build_block_index", "vs_check_status", "vs_estimate", "vs_index_counts", "lib", "launch_count",
+           "status_string", "VSAttention", "flop_counts"]

@@ -1,0 +1,225 @@
+"""ctypes binding of libvs.so (the C ABI in include/vs.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Torch tensors provide device memory and the current stream; outputs
+and workspaces not passed in are allocated with torch.  A missing library is
+an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+from . import _build
+
+VS_OK, VS_ERR_ARG, VS_ERR_SHAPE, VS_ERR_WORKSPACE, VS_ERR_INDEX, VS_ERR_TIMEOUT, VS_ERR_CUDA = range(7)
+
+
+class VSError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s" % (where, status_string(code)))
+
+
+class vs_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Nq", ctypes.c_int), ("Nk", ctypes.c_int), ("Hq", ctypes.c_int),
+                ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("sq", ctypes.c_int64 * 3), ("sk", ctypes.c_int64 * 3),
+                ("sv", ctypes.c_int64 * 3), ("so", ctypes.c_int64 * 3)]
+
+
+class vs_stripe(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("stripe", ctypes.c_int), ("q_rank", ctypes.c_int),
+                ("kv_rank", ctypes.c_int), ("N_global", ctypes.c_int64)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_S = ctypes.POINTER(vs_shape)
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True):
+    """The loaded libvs.so.  Raises if it is missing and cannot be built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libvs.so is not built (%s); run __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    L.vs_estimate_workspace.argtypes = [_S, ctypes.c_int]
+    L.vs_estimate_workspace.restype = ctypes.c_size_t
+    L.vs_estimate.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, _P, _P, _P,
+                              _P, ctypes.c_size_t, _P]
+    L.vs_block_index_bytes.argtypes = [_S, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vs_stripe)]
+    L.vs_block_index_bytes.restype = ctypes.c_size_t
+    L.vs_build_block_index.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vs_stripe), _P,
+                                       ctypes.c_size_t, _P]
+    L.vs_index_counts.argtypes = [_P, _P, _P]
+    L.vs_attn_fwd_workspace.argtypes = [_S]
+    L.vs_attn_fwd_workspace.restype = ctypes.c_size_t
+    L.vs_attn_fwd.argtypes = [_S, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.vs_attn_bwd_workspace.argtypes = [_S, ctypes.c_int]
+    L.vs_attn_bwd_workspace.restype = ctypes.c_size_t
+    L.vs_attn_bwd.argtypes = [_S, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.striped_permute.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    L.vs_check_status.argtypes = [_P, _P]
+    L.vs_status_string.argtypes = [ctypes.c_int]
+    L.vs_status_string.restype = ctypes.c_char_p
+    L.vs_launch_count.restype = ctypes.c_int64
+    for name in ("vs_estimate", "vs_build_block_index", "vs_index_counts", "vs_attn_fwd", "vs_attn_bwd",
+                 "striped_permute", "vs_check_status"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().vs_status_string(int(code)).decode()
+
+
+def launch_count() -> int:
+    return int(lib().vs_launch_count())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != VS_OK:
+        raise VSError(code, where)
+
+
+def make_shape(q: torch.Tensor, k: torch.Tensor, v: Optional[torch.Tensor] = None,
+               o: Optional[torch.Tensor] = None) -> vs_shape:
+    """vs_shape from BSHD tensors q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d], o like q."""
+    v = k if v is None else v
+    o = q if o is None else o
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    sh = vs_shape(B, Nq, Nk, Hq, Hkv, d)
+    for name, t in (("sq", q), ("sk", k), ("sv", v), ("so", o)):
+        if t.stride(3) != 1:
+            raise ValueError("channel dimension of %s must be contiguous" % name)
+        getattr(sh, name)[:] = [t.stride(0), t.stride(1), t.stride(2)]
+    return sh
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ entry points
+def vs_estimate(q, k, kv: int, ks: int, scale: Optional[float] = None, last_q: int = 64, v_idx=None, s_idx=None,
+                v_score=None, s_score=None, ws=None, stream=None):
+    """Vertical and slash selection (Algorithm 1).  Returns (v_idx, s_idx) int32
+    [B, Hq, kv] / [B, Hq, ks], sorted ascending."""
+    sh = make_shape(q, k)
+    B, N, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    v_idx = torch.empty(B, Hq, kv, dtype=torch.int32, device=q.device) if v_idx is None else v_idx
+    s_idx = torch.empty(B, Hq, ks, dtype=torch.int32, device=q.device) if s_idx is None else s_idx
+    need = lib().vs_estimate_workspace(ctypes.byref(sh), last_q)
+    ws = _ws(need, q.device) if ws is None else ws
+    _check(lib().vs_estimate(ctypes.byref(sh), _ptr(q), _ptr(k), last_q, kv, ks, scale, _ptr(v_idx), _ptr(s_idx),
+                             _ptr(v_score), _ptr(s_score), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream)), "vs_estimate")
+    return v_idx, s_idx
+
+
+def make_stripe(world: int, q_rank: int, kv_rank: int, N_global: int, stripe: int = 64) -> vs_stripe:
+    return vs_stripe(world, stripe, q_rank, kv_rank, N_global)
+
+
+def vs_build_block_index(q, k, v_idx, s_idx, stripe: Optional[vs_stripe] = None, arena=None, stream=None):
+    """Sparse index arena (uint8 device tensor) for the shape of q / k."""
+    sh = make_shape(q, k)
+    kv, ks = v_idx.shape[-1], s_idx.shape[-1]
+    sp = ctypes.byref(stripe) if stripe is not None else None
+    need = lib().vs_block_index_bytes(ctypes.byref(sh), kv, ks, sp)
+    if need == 0:
+        raise VSError(VS_ERR_SHAPE, "vs_block_index_bytes")
+    arena = torch.empty(need, dtype=torch.uint8, device=q.device) if arena is None else arena
+    _check(lib().vs_build_block_index(ctypes.byref(sh), _ptr(v_idx), _ptr(s_idx), kv, ks, sp, _ptr(arena),
+                                      arena.numel(), _stream(stream)), "vs_build_block_index")
+    return arena
+
+
+def vs_index_counts(arena, stream=None) -> np.ndarray:
+    """Work units per (b, h): [B, Hq, 4] int64 (see include/vs.h)."""
+    hdr = arena[:64].cpu().numpy().view(np.int32)
+    B, Hq = int(hdr[2]), int(hdr[3])
+    out = np.zeros((B, Hq, 4), np.int64)
+    _check(lib().vs_index_counts(_ptr(arena), ctypes.c_void_p(out.ctypes.data), _stream(stream)), "vs_index_counts")
+    return out
+
+
+def vs_attn_fwd(q, k, v, arena, scale: Optional[float] = None, o=None, lse=None, o_acc=None, ws=None, stream=None):
+    """Sparse forward.  Returns (o bf16 [B,Nq,Hq,d], lse fp32 [B,Hq,Nq])."""
+    B, Nq, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device) if lse is None else lse
+    sh = make_shape(q, k, v, o)
+    ws = _ws(lib().vs_attn_fwd_workspace(ctypes.byref(sh)), q.device) if ws is None else ws
+    _check(lib().vs_attn_fwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(arena), scale, _ptr(o), _ptr(lse),
+                             _ptr(o_acc), _ptr(ws), ws.numel(), _stream(stream)), "vs_attn_fwd")
+    return o, lse
+
+
+def vs_attn_bwd(q, k, v, o, lse, dO, arena, kv: int, scale: Optional[float] = None, dq=None, dk=None, dv=None,
+                dq_acc=None, ws=None, stream=None):
+    """Sparse backward.  Returns (dq, dk, dv) bf16."""
+    d = q.shape[-1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dO.stride() != o.stride():
+        raise ValueError("dO must have the layout of o")
+    sh = make_shape(q, k, v, o)
+    ws = _ws(lib().vs_attn_bwd_workspace(ctypes.byref(sh), kv), q.device) if ws is None else ws
+    _check(lib().vs_attn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(arena),
+                             scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dq_acc), _ptr(ws), ws.numel(),
+                             _stream(stream)), "vs_attn_bwd")
+    return dq, dk, dv
+
+
+def striped_permute(x, world: int, stripe: int = 64, inverse: bool = False, only_rank: int = -1, y=None,
+                    stream=None):
+    """Block-level striping of x [B, N, H, d] into [world, B, N/world, H, d]
+    (or one shard with only_rank >= 0), or back with inverse=True."""
+    if not inverse:
+        B, N, H, d = x.shape
+        shape = (B, N // world, H, d) if only_rank >= 0 else (world, B, N // world, H, d)
+    else:
+        W_, B, Nl, H, d = x.shape
+        N = Nl * W_
+        shape = (B, N, H, d)
+    y = torch.empty(shape, dtype=x.dtype, device=x.device) if y is None else y
+    _check(lib().striped_permute(_ptr(x), _ptr(y), B, N, H, d, world, stripe, int(inverse), only_rank,
+                                 _stream(stream)), "striped_permute")
+    return y
+
+
+def vs_check_status(buf, stream=None) -> int:
+    """Device status word of a workspace or arena (reset to VS_OK)."""
+    return int(lib().vs_check_status(_ptr(buf), _stream(stream)))

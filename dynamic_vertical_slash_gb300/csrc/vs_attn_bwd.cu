@@ -1,0 +1,989 @@
+// Sparse attention backward on the Vertical-Slash mask (tcgen05 / TMEM / TMA).
+//
+//   bwd_prep     D_n = rowsum(dO_n * O_n) and LSE in log2 units, per row.
+//   dq kernel    query-major, one CTA per (b, h, 128-row tile), same units as
+//                the forward: S = Q K^T, dP = dO V^T, dS = P (dP - D),
+//                dQ += dS K (A operand dS read from TMEM).
+//   bar kernel   key-major over gathered selected columns, one CTA per
+//                (b, h, 128-column chunk, row split): S^T = K Q^T,
+//                dP^T = V dO^T, dV += P^T dO, dK += dS^T Q over 64-row units
+//                from the chunk's first column to the end; fp32 partials.
+//   dkv kernel   key-major over slash units, one CTA per (b, KV head, 128-key
+//                tile), looping over the group's query heads so that the GQA
+//                sum happens in TMEM; its epilogue adds the bar partials of
+//                the keys that are selected columns, in a fixed order.
+// No floating-point atomics: every output element has one writer and a fixed
+// summation order.
+#include "vs_internal.h"
+#include <algorithm>
+#include "vs_kernel_common.cuh"
+
+namespace vs {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdStages = 3;
+constexpr int kMaxGroup = 64;  // query heads per KV head supported by the key-major kernel
+
+struct BwdLayout {
+  int64_t off_l2, off_d, off_bar_dk, off_bar_dv, total;
+  int smax;
+};
+
+BwdLayout bwd_layout(int B, int Hq, int Nq, int d, int kv) {
+  BwdLayout L;
+  const int64_t BH = int64_t(B) * Hq;
+  const int64_t KVP = (kv + kBarK - 1) / kBarK * kBarK;
+  const int64_t tiles = (Nq + kRowTile - 1) / kRowTile;
+  L.smax = int((tiles + kBarSplitTiles - 1) / kBarSplitTiles);
+  int64_t off = 256;
+  auto take = [&](int64_t bytes) {
+    const int64_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  L.off_l2 = take(BH * Nq * 4);
+  L.off_d = take(BH * Nq * 4);
+  L.off_bar_dk = take(int64_t(L.smax) * BH * KVP * d * 4);
+  L.off_bar_dv = take(int64_t(L.smax) * BH * KVP * d * 4);
+  L.total = off;
+  return L;
+}
+
+__device__ __forceinline__ BwdLayout bwd_layout_dev(const ArenaHeader* h, int d) {
+  BwdLayout L;
+  const int64_t BH = int64_t(h->B) * h->Hq;
+  const int64_t KVP = h->KVP;
+  const int64_t tiles = (h->Nq + kRowTile - 1) / kRowTile;
+  L.smax = int((tiles + kBarSplitTiles - 1) / kBarSplitTiles);
+  int64_t off = 256;
+  auto take = [&](int64_t bytes) {
+    const int64_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  L.off_l2 = take(BH * h->Nq * 4);
+  L.off_d = take(BH * h->Nq * 4);
+  L.off_bar_dk = take(int64_t(L.smax) * BH * KVP * d * 4);
+  L.off_bar_dv = take(int64_t(L.smax) * BH * KVP * d * 4);
+  L.total = off;
+  return L;
+}
+
+struct BwdParams {
+  const void* arena;
+  const uint8_t* q;
+  const uint8_t* k;
+  const uint8_t* v;
+  const uint8_t* o;
+  const uint8_t* dO;
+  const float* lse;
+  int64_t sq[3], sk[3], sv[3], so[3];
+  int B, Nq, Nk, Hq, Hkv;
+  float scale, scale_log2;
+  uint8_t* dq;
+  uint8_t* dk;
+  uint8_t* dv;
+  float* dq_acc;
+  uint8_t* ws;
+  size_t ws_bytes;
+  int bar_nchunk;  // chunks per (b, h) in the bar kernel's grid (>= KVP / 128)
+  int* err;
+};
+
+// Verifies the arena and the workspace size; returns false (and records the
+// error once) if the kernel must not run.
+__device__ __forceinline__ bool bwd_inputs_ok(const BwdParams& p, const ArenaView& av, int d) {
+  const bool arena_ok = (av.hdr->status == 0) && (av.hdr->magic == kArenaMagic) && av.hdr->Nq == p.Nq &&
+                        av.hdr->Hq == p.Hq && av.hdr->B == p.B;
+  const bool ws_ok = arena_ok && bwd_layout_dev(av.hdr, d).total <= int64_t(p.ws_bytes);
+  if (!(arena_ok && ws_ok) && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+    raise_error(p.err, !arena_ok ? (av.hdr->status ? av.hdr->status : int(VS_ERR_ARG)) : int(VS_ERR_WORKSPACE));
+  // a workspace already holding an error makes the call skip its work
+  return arena_ok && ws_ok && *reinterpret_cast<volatile int*>(p.err) == 0;
+}
+
+// ------------------------------------------------------------------ prepass
+__global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
+  const int64_t total = int64_t(p.B) * p.Hq * p.Nq;
+  const ArenaView av = arena_view(p.arena);
+  if (!bwd_inputs_ok(p, av, d)) return;
+  const BwdLayout L = bwd_layout_dev(av.hdr, d);
+  float* l2 = reinterpret_cast<float*>(p.ws + L.off_l2);
+  float* dd = reinterpret_cast<float*>(p.ws + L.off_d);
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t n = i % p.Nq, bh = i / p.Nq;
+    const int64_t b = bh / p.Hq, h = bh % p.Hq;
+    const int64_t off = (b * p.so[0] + n * p.so[1] + h * p.so[2]) * 2;
+    const uint4* orow = reinterpret_cast<const uint4*>(p.o + off);
+    const uint4* grow = reinterpret_cast<const uint4*>(p.dO + off);
+    float acc = 0.f;
+    for (int c = 0; c < d / 8; ++c) {
+      const uint4 a = orow[c], g = grow[c];
+      const uint32_t av4[4] = {a.x, a.y, a.z, a.w}, gv4[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(av4[e] << 16), __uint_as_float(gv4[e] << 16), acc);
+        acc = fmaf(__uint_as_float(av4[e] & 0xFFFF0000u), __uint_as_float(gv4[e] & 0xFFFF0000u), acc);
+      }
+    }
+    dd[i] = acc;
+    l2[i] = p.lse[i] * kLog2e;
+  }
+}
+
+// ---------------------------------------------------------------- dQ kernel
+constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColDS = 384;
+
+template <int D>
+struct DqSmem {
+  static constexpr int NH = D / 64;
+  uint8_t q[NH][kQTile * 128];
+  uint8_t g[NH][kQTile * 128];  // dO
+  uint8_t k[kBwdStages][NH][kKTile * 128];
+  uint8_t v[kBwdStages][NH][kKTile * 128];
+  uint64_t q_full;
+  uint64_t kv_full[kBwdStages], kv_empty[kBwdStages];
+  uint64_t s_full[2], s_free[2], ds_full[2], ds_done[2];
+  uint64_t fin, teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const BwdParams p) {
+  constexpr int NH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const ArenaView av = arena_view(p.arena);
+  const bool inputs_ok = bwd_inputs_ok(p, av, D);
+  const Geo G = geo_from(av.hdr, p.Hkv, D);
+  const int T = (p.Nq + kQTile - 1) / kQTile;
+  const int BH = p.B * p.Hq;
+  const int t = T - 1 - int(blockIdx.x) / BH;
+  const int bh = int(blockIdx.x) % BH;
+  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / G.g;
+  const int32_t* elist = av.elist + int64_t(bh) * G.EMAX;
+  const int32_t* vlist = av.vlist + int64_t(bh) * G.KVP;
+  const int64_t last_row = int64_t(t) * kQTile + kQTile - 1;
+  int nslash = 0, nbar = 0;
+  if (inputs_ok) {
+    nslash = count_le(elist, __ldg(av.ecount + bh), last_row);
+    const int vc = __ldg(av.vcount + bh);
+    int lo = 0, hi = (vc + kKTile - 1) / kKTile;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(vlist + mid * kKTile) <= last_row) lo = mid + 1;
+      else hi = mid;
+    }
+    nbar = lo;
+  }
+  const int U = nslash + nbar;
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    mbar_init(&s.q_full, 1);
+    for (int i = 0; i < kBwdStages; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], 128);
+      mbar_init(&s.ds_full[i], 128);
+      mbar_init(&s.ds_done[i], 1);
+    }
+    mbar_init(&s.fin, 1);
+    mbar_init(&s.teardown, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  const Abort ab{&s.abort_flag, p.err};
+  bool mma_issued = false;
+
+  if (warp == 0) {
+    int issued[kBwdStages];
+    for (int i = 0; i < kBwdStages; ++i) issued[i] = -1;
+    if (U > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&s.q_full, 2 * NH * kQTile * 128);
+        for (int hf = 0; hf < NH; ++hf) {
+          tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
+          tma_load_4d(s.g[hf], &tmG, &s.q_full, 64 * hf, h, t * kQTile, b);
+        }
+      }
+      const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
+      const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
+      for (int j = 0; j < U; ++j) {
+        const int st = j % kBwdStages;
+        if (j >= kBwdStages && !mbar_wait(&s.kv_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+        if (j < nslash) {
+          if (lane == 0) {
+            const int c = t * kQTile + 64 - __ldg(elist + j);
+            mbar_arrive_expect_tx(&s.kv_full[st], 2 * NH * kKTile * 128);
+            for (int hf = 0; hf < NH; ++hf) {
+              tma_load_4d(s.k[st][hf], &tmK, &s.kv_full[st], 64 * hf, hk, c, b);
+              tma_load_4d(s.v[st][hf], &tmV, &s.kv_full[st], 64 * hf, hk, c, b);
+            }
+          }
+        } else {
+          const int32_t* keys = vlist + (j - nslash) * kKTile;
+          gather_rows<D>(smem_u32(s.k[st][0]), kKTile, kb, p.sk[1], keys, kKTile, lane);
+          gather_rows<D>(smem_u32(s.v[st][0]), kKTile, vb, p.sv[1], keys, kKTile, lane);
+          asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.kv_full[st])) : "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.kv_full[st]);
+        }
+        issued[st] = j;
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && s.abort_flag) {
+      for (int i = 0; i < kBwdStages; ++i)
+        if (issued[i] >= 0) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(&s.kv_full[i], (issued[i] / kBwdStages) & 1) && global_ns() - t0 < kWaitBudgetNs) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && U > 0) {
+      const uint32_t idS = idesc_bf16(128, 64, 0, 0);
+      const uint32_t idQ = idesc_bf16(128, D, 0, 1);
+      bool ok = mbar_wait(&s.q_full, 0, ab, VS_ERR_TIMEOUT);
+      for (int j = 0; ok && j <= U; ++j) {
+        if (j < U) {
+          const int st = j % kBwdStages;
+          if (!(ok = mbar_wait(&s.kv_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
+          if (j >= nslash) fence_proxy_async_smem();
+          if (j >= 2 && !(ok = mbar_wait(&s.s_free[j & 1], ((j - 2) >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            mma_ss(tmem + kDqColS + (j & 1) * 64, dq_, dk_, idS, kk > 0);
+            mma_ss(tmem + kDqColDP + (j & 1) * 64, dg_, dv_, idS, kk > 0);
+          }
+          mma_issued = true;
+          mma_commit(&s.s_full[j & 1]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, st = jj % kBwdStages;
+          if (!(ok = mbar_wait(&s.ds_full[jj & 1], (jj >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kKTile / 16; ++kk) {
+            const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][0]) + kk * 2048, kKTile * 128, 1024);
+            mma_ts(tmem + kDqColAcc, tmem + kDqColDS + (jj & 1) * 32 + kk * 8, dk_, idQ, (jj > 0 || kk > 0));
+          }
+          mma_commit(&s.ds_done[jj & 1]);
+          mma_commit(&s.kv_empty[st]);
+        }
+      }
+      mma_commit(&s.fin);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
+    const int64_t n_loc = int64_t(t) * kQTile + r;
+    const bool row_ok = n_loc < p.Nq && inputs_ok;
+    const int64_t n_g = qpos_g(G, n_loc);
+    const uint64_t* offbits = av.offbits + int64_t(bh) * G.WG;
+    const uint64_t* colbits = av.colbits + int64_t(bh) * G.WG;
+    float Lr = 0.f, Dr = 0.f;
+    if (row_ok) {
+      const BwdLayout L = bwd_layout_dev(av.hdr, D);
+      Lr = reinterpret_cast<const float*>(p.ws + L.off_l2)[int64_t(bh) * p.Nq + n_loc];
+      Dr = reinterpret_cast<const float*>(p.ws + L.off_d)[int64_t(bh) * p.Nq + n_loc];
+    }
+    bool ok = true;
+    for (int j = 0; j < U; ++j) {
+      ok = mbar_wait(&s.s_full[j & 1], (j >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[64], pr[64];
+      tmem_ld32(tl + kDqColS + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tl + kDqColS + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tl + kDqColDP + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+      tmem_ld32(tl + kDqColDP + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.s_free[j & 1]);
+      uint64_t mask = 0;
+      if (row_ok) {
+        if (j < nslash) {
+          const int64_t c = int64_t(t) * kQTile + 64 - __ldg(elist + j);
+          mask = slash_row_mask(G, offbits, colbits, n_g, c);
+        } else {
+          const int4* kq = reinterpret_cast<const int4*>(vlist + (j - nslash) * kKTile);
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const int4 kk4 = __ldg(kq + q4);
+            const int kk[4] = {kk4.x, kk4.y, kk4.z, kk4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (kk[e] >= 0 && kpos_g(G, kk[e]) <= n_g) mask |= 1ull << (q4 * 4 + e);
+          }
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * i + e;
+          const float pv = ex2(__uint_as_float(sr[c]) * p.scale_log2 - Lr);
+          ds[e] = ((mask >> c) & 1ull) ? pv * (__uint_as_float(pr[c]) - Dr) : 0.f;
+        }
+        pk[i] = pack_bf16x2(ds[0], ds[1]);
+      }
+      if (j >= 2) ok = mbar_wait(&s.ds_done[j & 1], ((j - 2) >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st16(tl + kDqColDS + (j & 1) * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(tl + kDqColDS + (j & 1) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.ds_full[j & 1]);
+    }
+    if (ok && U > 0) ok = mbar_wait(&s.fin, 0, ab, VS_ERR_TIMEOUT);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (ok && inputs_ok) {
+      // TMEM reads are warp-collective: every lane loads, valid rows store
+      const bool store = n_loc < p.Nq;
+      uint8_t* drow = p.dq + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(h) * p.sq[2]) * 2;
+      float* acc = (p.dq_acc && store) ? p.dq_acc + ((int64_t(b) * p.Nq + n_loc) * p.Hq + h) * D : nullptr;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 16) {
+        uint32_t gv[16];
+        if (U > 0) {
+          tmem_ld16(tl + kDqColAcc + cc, gv);
+          tmem_ld_wait();
+        }
+        if (!store) continue;
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = U > 0 ? __uint_as_float(gv[i]) * p.scale : 0.f;
+        if (acc) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            float4 a4 = *reinterpret_cast<float4*>(acc + cc + i);
+            a4.x += y[i];
+            a4.y += y[i + 1];
+            a4.z += y[i + 2];
+            a4.w += y[i + 3];
+            *reinterpret_cast<float4*>(acc + cc + i) = a4;
+            y[i] = a4.x;
+            y[i + 1] = a4.y;
+            y[i + 2] = a4.z;
+            y[i + 3] = a4.w;
+          }
+        }
+        uint4 w0, w1;
+        w0.x = pack_bf16x2(y[0], y[1]);
+        w0.y = pack_bf16x2(y[2], y[3]);
+        w0.z = pack_bf16x2(y[4], y[5]);
+        w0.w = pack_bf16x2(y[6], y[7]);
+        w1.x = pack_bf16x2(y[8], y[9]);
+        w1.y = pack_bf16x2(y[10], y[11]);
+        w1.z = pack_bf16x2(y[12], y[13]);
+        w1.w = pack_bf16x2(y[14], y[15]);
+        *reinterpret_cast<uint4*>(drow + cc * 2) = w0;
+        *reinterpret_cast<uint4*>(drow + cc * 2 + 16) = w1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0 && mma_issued && s.abort_flag) {
+      mma_commit(&s.teardown);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&s.teardown, 0) && global_ns() - t0 < kWaitBudgetNs) {
+      }
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------ key-major dK / dV
+// TMEM: dK [0, 128), dV [128, 256), S^T [256, 320), dP^T [320, 384),
+//       P^T x2 [384, 448), dS^T x2 [448, 512)
+constexpr uint32_t kKvColDK = 0, kKvColDV = 128, kKvColS = 256, kKvColDP = 320, kKvColP = 384, kKvColDS = 448;
+
+template <int D>
+struct KvSmem {
+  static constexpr int NH = D / 64;
+  uint8_t k[NH][kBarK * 128];  // A operands: 128 keys
+  uint8_t v[NH][kBarK * 128];
+  uint8_t q[kBwdStages][NH][kRowTile * 128];  // B operands: 64 rows
+  uint8_t g[kBwdStages][NH][kRowTile * 128];
+  float l2[kBwdStages][kRowTile];
+  float dd[kBwdStages][kRowTile];
+  int32_t unit_head[kBwdStages];
+  int32_t unit_row[kBwdStages];
+  uint64_t kv_full;
+  uint64_t st_full[kBwdStages], st_empty[kBwdStages];
+  uint64_t s_full, s_free, p_full[2], mm_done[2];
+  uint64_t fin, teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Unit enumeration of a key-major CTA.
+//   slash (BAR = false): CTA (b, hk, key tile tau); units run over the query
+//     heads h of the group, then the head's flist entries f with
+//     128 tau + f <= Nq - 1, rows [128 tau + f, +64).
+//   bar (BAR = true): CTA (b, h, chunk c, split sp); units are 64-row tiles
+//     from the chunk's first block to the end, split in pieces of
+//     kBarSplitTiles tiles.
+struct KvWork {
+  int n_units;
+  int heads;         // slash: number of heads in the group
+  int cnt[kMaxGroup]; // slash: units per head
+  int64_t row0;      // bar: first row of the split
+};
+
+template <bool BAR>
+__device__ __forceinline__ void kv_unit(const KvWork& w, const ArenaView& av, const Geo& G, int b, int hk, int h_bar,
+                                        int64_t k0, int j, int* head_out, int64_t* row_out) {
+  if (BAR) {
+    *head_out = h_bar;
+    *row_out = w.row0 + int64_t(j) * kRowTile;
+    return;
+  }
+  int hh = 0;
+  while (hh < w.heads - 1 && j >= w.cnt[hh]) {
+    j -= w.cnt[hh];
+    ++hh;
+  }
+  const int h = hk * G.g + hh;
+  const int bh = b * G.Hq + h;
+  *head_out = h;
+  *row_out = k0 + __ldg(av.flist + int64_t(bh) * G.EMAX + j);
+}
+
+template <int D, bool BAR>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    vs_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                     const BwdParams p) {
+  constexpr int NH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  KvSmem<D>& s = *reinterpret_cast<KvSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const ArenaView av = arena_view(p.arena);
+  const bool inputs_ok = bwd_inputs_ok(p, av, D);
+  const Geo G = geo_from(av.hdr, p.Hkv, D);
+  const BwdLayout L = bwd_layout_dev(av.hdr, D);
+
+  // ---- work of this CTA
+  int b, hk, h_bar = 0, chunk = 0, split = 0;
+  int64_t k0 = 0;
+  KvWork w;
+  w.n_units = 0;
+  w.heads = 0;
+  w.row0 = 0;
+  bool cta_ok = inputs_ok;
+  if (!BAR) {
+    // early keys see the most rows: launch them first
+    const int BHK = p.B * p.Hkv;
+    const int bhk = int(blockIdx.x) % BHK;
+    b = bhk / p.Hkv;
+    hk = bhk % p.Hkv;
+    k0 = int64_t(int(blockIdx.x) / BHK) * kBarK;
+    if (cta_ok) {
+      w.heads = G.g;
+      for (int hh = 0; hh < G.g; ++hh) {
+        const int bh = b * p.Hq + hk * G.g + hh;
+        const int c = count_le(av.flist + int64_t(bh) * G.EMAX, __ldg(av.fcount + bh), int64_t(p.Nq) - 1 - k0);
+        w.cnt[hh] = c;
+        w.n_units += c;
+      }
+    }
+  } else {
+    split = int(blockIdx.x) % L.smax;
+    const int rest = int(blockIdx.x) / L.smax;
+    chunk = rest % p.bar_nchunk;
+    const int bh = rest / p.bar_nchunk;
+    b = bh / p.Hq;
+    h_bar = bh % p.Hq;
+    hk = h_bar / G.g;
+    k0 = int64_t(chunk) * kBarK;  // position in the vertical list
+    if (cta_ok) {
+      const int vc = __ldg(av.vcount + bh);
+      if (chunk * kBarK < vc && chunk * kBarK < G.KVP) {
+        const int64_t rs = (int64_t(__ldg(av.vlist + int64_t(bh) * G.KVP + chunk * kBarK)) / kBlk) * kBlk;
+        const int64_t tiles = (p.Nq - rs + kRowTile - 1) / kRowTile;
+        const int64_t first = int64_t(split) * kBarSplitTiles;
+        if (first < tiles) {
+          w.row0 = rs + first * kRowTile;
+          w.n_units = int(min(int64_t(kBarSplitTiles), tiles - first));
+        }
+      }
+    }
+  }
+  const int U = w.n_units;
+  const bool run = cta_ok && U > 0;
+  if (BAR && !run) return;  // nothing to write for this split
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    mbar_init(&s.kv_full, 1);
+    for (int i = 0; i < kBwdStages; ++i) {
+      mbar_init(&s.st_full[i], 1);
+      mbar_init(&s.st_empty[i], 1);
+    }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.s_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.mm_done[i], 1);
+    }
+    mbar_init(&s.fin, 1);
+    mbar_init(&s.teardown, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  const Abort ab{&s.abort_flag, p.err};
+  bool mma_issued = false;
+  const int32_t* bar_keys = BAR ? av.vlist + (int64_t(b) * p.Hq + h_bar) * G.KVP + k0 : nullptr;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued[kBwdStages];
+    for (int i = 0; i < kBwdStages; ++i) issued[i] = -1;
+    bool kv_issued = false;
+    if (run) {
+      if (!BAR) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s.kv_full, 2 * NH * kBarK * 128);
+          for (int hf = 0; hf < NH; ++hf) {
+            tma_load_4d(s.k[hf], &tmK, &s.kv_full, 64 * hf, hk, int(k0), b);
+            tma_load_4d(s.v[hf], &tmV, &s.kv_full, 64 * hf, hk, int(k0), b);
+          }
+        }
+      } else {
+        const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
+        const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
+        gather_rows<D>(smem_u32(s.k[0]), kBarK, kb, p.sk[1], bar_keys, kBarK, lane);
+        gather_rows<D>(smem_u32(s.v[0]), kBarK, vb, p.sv[1], bar_keys, kBarK, lane);
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.kv_full)) : "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.kv_full);
+      }
+      kv_issued = true;
+      const float* l2g = reinterpret_cast<const float*>(p.ws + L.off_l2);
+      const float* ddg = reinterpret_cast<const float*>(p.ws + L.off_d);
+      for (int j = 0; j < U; ++j) {
+        const int st = j % kBwdStages;
+        if (j >= kBwdStages && !mbar_wait(&s.st_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+        int h;
+        int64_t r0;
+        kv_unit<BAR>(w, av, G, b, hk, h_bar, k0, j, &h, &r0);
+        const int64_t bh = int64_t(b) * p.Hq + h;
+        for (int i = lane; i < kRowTile; i += 32) {
+          const int64_t n = r0 + i;
+          const bool in = n < p.Nq;
+          s.l2[st][i] = in ? l2g[bh * p.Nq + n] : 0.f;
+          s.dd[st][i] = in ? ddg[bh * p.Nq + n] : 0.f;
+        }
+        if (lane == 0) {
+          s.unit_head[st] = h;
+          s.unit_row[st] = int32_t(r0);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s.st_full[st], 2 * NH * kRowTile * 128);
+          for (int hf = 0; hf < NH; ++hf) {
+            tma_load_4d(s.q[st][hf], &tmQ, &s.st_full[st], 64 * hf, h, int(r0), b);
+            tma_load_4d(s.g[st][hf], &tmG, &s.st_full[st], 64 * hf, h, int(r0), b);
+          }
+        }
+        issued[st] = j;
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && s.abort_flag) {
+      const uint64_t t0 = global_ns();
+      if (kv_issued)
+        while (!mbar_try_wait(&s.kv_full, 0) && global_ns() - t0 < kWaitBudgetNs) {
+        }
+      for (int i = 0; i < kBwdStages; ++i)
+        if (issued[i] >= 0) {
+          const uint64_t t1 = global_ns();
+          while (!mbar_try_wait(&s.st_full[i], (issued[i] / kBwdStages) & 1) && global_ns() - t1 < kWaitBudgetNs) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && run) {
+      const uint32_t idS = idesc_bf16(128, kRowTile, 0, 0);
+      const uint32_t idG = idesc_bf16(128, D, 0, 1);
+      bool ok = mbar_wait(&s.kv_full, 0, ab, VS_ERR_TIMEOUT);
+      if (ok && BAR) fence_proxy_async_smem();
+      for (int j = 0; ok && j <= U; ++j) {
+        if (j < U) {
+          const int st = j % kBwdStages;
+          if (!(ok = mbar_wait(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
+          if (j >= 1 && !(ok = mbar_wait(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t da = sdesc_sw128(smem_u32(s.k[kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            mma_ss(tmem + kKvColS, da, dq_, idS, kk > 0);
+            mma_ss(tmem + kKvColDP, dva, dg_, idS, kk > 0);
+          }
+          mma_issued = true;
+          mma_commit(&s.s_full);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, st = jj % kBwdStages;
+          if (!(ok = mbar_wait(&s.p_full[jj & 1], (jj >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kRowTile / 16; ++kk) {
+            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][0]) + kk * 2048, kRowTile * 128, 1024);
+            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][0]) + kk * 2048, kRowTile * 128, 1024);
+            mma_ts(tmem + kKvColDV, tmem + kKvColP + (jj & 1) * 32 + kk * 8, dg_, idG, (jj > 0 || kk > 0));
+            mma_ts(tmem + kKvColDK, tmem + kKvColDS + (jj & 1) * 32 + kk * 8, dq_, idG, (jj > 0 || kk > 0));
+          }
+          mma_commit(&s.mm_done[jj & 1]);
+          mma_commit(&s.st_empty[st]);
+        }
+      }
+      mma_commit(&s.fin);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // key row of the tile
+    const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
+    int64_t kl;                          // local key index
+    if (BAR) kl = __ldg(bar_keys + r);
+    else kl = k0 + r;
+    const bool key_ok = run && kl >= 0 && kl < p.Nk;
+    const int64_t m_g = key_ok ? kpos_g(G, kl) : 0;
+    bool ok = true;
+    for (int j = 0; run && j < U; ++j) {
+      const int st = j % kBwdStages;
+      ok = mbar_wait(&s.s_full, j & 1, ab, VS_ERR_TIMEOUT) &&
+           mbar_wait(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[64], pr[64];
+      tmem_ld32(tl + kKvColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tl + kKvColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tl + kKvColDP, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+      tmem_ld32(tl + kKvColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.s_free);
+      const int h = s.unit_head[st];
+      const int64_t r0 = s.unit_row[st];
+      const int64_t bh = int64_t(b) * p.Hq + h;
+      uint64_t mask = 0;
+      if (key_ok) {
+        if (BAR) {
+          const int64_t n_g0 = qpos_g(G, r0);  // rows of a unit are one aligned block
+          const int64_t rows = int64_t(p.Nq) - r0;
+          const int64_t lim = m_g - n_g0;    // rows i >= lim are causal
+          uint64_t valid = rows >= 64 ? ~0ull : (rows <= 0 ? 0ull : ((1ull << rows) - 1));
+          if (lim >= 64) valid = 0;
+          else if (lim > 0) valid &= (~0ull) << lim;
+          mask = valid;
+        } else {
+          const uint64_t vw = __ldg(av.vlocbits + bh * G.WL + (kl >> 6));
+          if (!((vw >> (kl & 63)) & 1ull)) mask = slash_col_mask(G, av.offbits + bh * G.WG, kl, r0);
+        }
+      }
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float pv[2], ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * i + e;
+          const float x = ex2(__uint_as_float(sr[c]) * p.scale_log2 - s.l2[st][c]);
+          const bool on = (mask >> c) & 1ull;
+          pv[e] = on ? x : 0.f;
+          ds[e] = on ? x * (__uint_as_float(pr[c]) - s.dd[st][c]) : 0.f;
+        }
+        pk[i] = pack_bf16x2(pv[0], pv[1]);
+        dk[i] = pack_bf16x2(ds[0], ds[1]);
+      }
+      if (j >= 2) ok = mbar_wait(&s.mm_done[j & 1], ((j - 2) >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st16(tl + kKvColP + (j & 1) * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(tl + kKvColP + (j & 1) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      tmem_st16(tl + kKvColDS + (j & 1) * 32, *reinterpret_cast<uint32_t(*)[16]>(&dk[0]));
+      tmem_st16(tl + kKvColDS + (j & 1) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&dk[16]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[j & 1]);
+    }
+    if (ok && run) ok = mbar_wait(&s.fin, 0, ab, VS_ERR_TIMEOUT);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    // ------------------------------------------------------------ epilogue
+    if (ok && cta_ok) {
+      if (BAR) {
+        {
+          // TMEM reads are warp-collective: every lane loads, valid keys store
+          const int64_t bh = int64_t(b) * p.Hq + h_bar;
+          const int64_t rank = k0 + r;  // position in the vertical list
+          float* pdk = reinterpret_cast<float*>(p.ws + L.off_bar_dk) + ((int64_t(split) * p.B * p.Hq + bh) * G.KVP + rank) * D;
+          float* pdv = reinterpret_cast<float*>(p.ws + L.off_bar_dv) + ((int64_t(split) * p.B * p.Hq + bh) * G.KVP + rank) * D;
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 16) {
+            uint32_t a[16], c2[16];
+            tmem_ld16(tl + kKvColDK + cc, a);
+            tmem_ld16(tl + kKvColDV + cc, c2);
+            tmem_ld_wait();
+            if (!key_ok) continue;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              *reinterpret_cast<float4*>(pdk + cc + i) =
+                  make_float4(__uint_as_float(a[i]) * p.scale, __uint_as_float(a[i + 1]) * p.scale,
+                              __uint_as_float(a[i + 2]) * p.scale, __uint_as_float(a[i + 3]) * p.scale);
+              *reinterpret_cast<float4*>(pdv + cc + i) = make_float4(
+                  __uint_as_float(c2[i]), __uint_as_float(c2[i + 1]), __uint_as_float(c2[i + 2]), __uint_as_float(c2[i + 3]));
+            }
+          }
+        }
+      } else {
+        // slash part (TMEM) + the bar partials of every head that selected this key
+        uint8_t* okr = p.dk + (int64_t(b) * p.sk[0] + kl * p.sk[1] + int64_t(hk) * p.sk[2]) * 2;
+        uint8_t* ovr = p.dv + (int64_t(b) * p.sv[0] + kl * p.sv[1] + int64_t(hk) * p.sv[2]) * 2;
+        const float* bdk = reinterpret_cast<const float*>(p.ws + L.off_bar_dk);
+        const float* bdv = reinterpret_cast<const float*>(p.ws + L.off_bar_dv);
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 16) {
+          float yk[16], yv[16];
+          if (U > 0) {
+            uint32_t a[16], c2[16];
+            tmem_ld16(tl + kKvColDK + cc, a);
+            tmem_ld16(tl + kKvColDV + cc, c2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              yk[i] = __uint_as_float(a[i]) * p.scale;
+              yv[i] = __uint_as_float(c2[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) yk[i] = yv[i] = 0.f;
+          }
+          if (kl >= p.Nk) continue;  // past the end of the keys: load only
+          for (int hh = 0; hh < G.g; ++hh) {
+            const int64_t bh = int64_t(b) * p.Hq + hk * G.g + hh;
+            const uint64_t vw = __ldg(av.vlocbits + bh * G.WL + (kl >> 6));
+            if (!((vw >> (kl & 63)) & 1ull)) continue;
+            // this head selected the key as a column: add its bar partials
+            const int64_t rank =
+                __ldg(av.vlocpre + bh * G.WL + (kl >> 6)) + __popcll(vw & ((1ull << (kl & 63)) - 1));
+            const int64_t first = __ldg(av.vlist + bh * G.KVP + (rank / kBarK) * kBarK);
+            const int64_t rs = (first / kBlk) * kBlk;
+            const int64_t tiles = (p.Nq - rs + kRowTile - 1) / kRowTile;
+            const int nsplit = int((tiles + kBarSplitTiles - 1) / kBarSplitTiles);
+            for (int sp = 0; sp < nsplit; ++sp) {
+              const int64_t base = ((int64_t(sp) * p.B * p.Hq + bh) * G.KVP + rank) * D + cc;
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(bdk + base + i);
+                const float4 c4 = *reinterpret_cast<const float4*>(bdv + base + i);
+                yk[i] += a4.x;
+                yk[i + 1] += a4.y;
+                yk[i + 2] += a4.z;
+                yk[i + 3] += a4.w;
+                yv[i] += c4.x;
+                yv[i + 1] += c4.y;
+                yv[i + 2] += c4.z;
+                yv[i + 3] += c4.w;
+              }
+            }
+          }
+          uint4 k0w, k1w, v0w, v1w;
+          k0w.x = pack_bf16x2(yk[0], yk[1]);
+          k0w.y = pack_bf16x2(yk[2], yk[3]);
+          k0w.z = pack_bf16x2(yk[4], yk[5]);
+          k0w.w = pack_bf16x2(yk[6], yk[7]);
+          k1w.x = pack_bf16x2(yk[8], yk[9]);
+          k1w.y = pack_bf16x2(yk[10], yk[11]);
+          k1w.z = pack_bf16x2(yk[12], yk[13]);
+          k1w.w = pack_bf16x2(yk[14], yk[15]);
+          v0w.x = pack_bf16x2(yv[0], yv[1]);
+          v0w.y = pack_bf16x2(yv[2], yv[3]);
+          v0w.z = pack_bf16x2(yv[4], yv[5]);
+          v0w.w = pack_bf16x2(yv[6], yv[7]);
+          v1w.x = pack_bf16x2(yv[8], yv[9]);
+          v1w.y = pack_bf16x2(yv[10], yv[11]);
+          v1w.z = pack_bf16x2(yv[12], yv[13]);
+          v1w.w = pack_bf16x2(yv[14], yv[15]);
+          *reinterpret_cast<uint4*>(okr + cc * 2) = k0w;
+          *reinterpret_cast<uint4*>(okr + cc * 2 + 16) = k1w;
+          *reinterpret_cast<uint4*>(ovr + cc * 2) = v0w;
+          *reinterpret_cast<uint4*>(ovr + cc * 2 + 16) = v1w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0 && mma_issued && s.abort_flag) {
+      mma_commit(&s.teardown);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&s.teardown, 0) && global_ns() - t0 < kWaitBudgetNs) {
+      }
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+BwdParams make_params(const vs_shape* sh, const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
+                      float* dq_acc, void* ws, size_t ws_bytes) {
+  BwdParams p;
+  p.arena = arena;
+  p.q = static_cast<const uint8_t*>(q);
+  p.k = static_cast<const uint8_t*>(k);
+  p.v = static_cast<const uint8_t*>(v);
+  p.o = static_cast<const uint8_t*>(o);
+  p.dO = static_cast<const uint8_t*>(dO);
+  p.lse = lse;
+  for (int i = 0; i < 3; ++i) {
+    p.sq[i] = sh->sq[i];
+    p.sk[i] = sh->sk[i];
+    p.sv[i] = sh->sv[i];
+    p.so[i] = sh->so[i];
+  }
+  p.B = sh->B;
+  p.Nq = sh->Nq;
+  p.Nk = sh->Nk;
+  p.Hq = sh->Hq;
+  p.Hkv = sh->Hkv;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.dq = static_cast<uint8_t*>(dq);
+  p.dk = static_cast<uint8_t*>(dk);
+  p.dv = static_cast<uint8_t*>(dv);
+  p.dq_acc = dq_acc;
+  p.ws = static_cast<uint8_t*>(ws);
+  p.ws_bytes = ws_bytes;
+  p.err = static_cast<int*>(ws);
+  return p;
+}
+
+template <int D>
+vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, cudaStream_t st) {
+  CUtensorMap tq128, tg128, tk64, tv64, tk128, tv128, tq64, tg64;
+  vs_status rc;
+  if ((rc = make_tmap_bshd(&tq128, p.q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tg128, p.dO, sh->B, sh->Nq, sh->Hq, D, sh->so, kQTile)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tk64, p.k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kKTile)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tv64, p.v, sh->B, sh->Nk, sh->Hkv, D, sh->sv, kKTile)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tk128, p.k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kBarK)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tv128, p.v, sh->B, sh->Nk, sh->Hkv, D, sh->sv, kBarK)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tq64, p.q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kRowTile)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tg64, p.dO, sh->B, sh->Nq, sh->Hq, D, sh->so, kRowTile)) != VS_OK) return rc;
+  const size_t sm_dq = sizeof(DqSmem<D>) + 1024;
+  const size_t sm_kv = sizeof(KvSmem<D>) + 1024;
+  if (cudaFuncSetAttribute(vs_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_dq)) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(vs_bwd_kv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_kv)) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(vs_bwd_kv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm_kv)) !=
+          cudaSuccess)
+    return VS_ERR_CUDA;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t rows = int64_t(sh->B) * sh->Hq * sh->Nq;
+  const int prep_grid = int(std::min<int64_t>((rows + 255) / 256, int64_t(sms) * 8));
+  bwd_prep<<<prep_grid, 256, 0, st>>>(p, D);
+  // bar partials first: the slash kernel's epilogue reads them
+  vs_bwd_kv_kernel<D, true><<<unsigned(int64_t(sh->B) * sh->Hq * grid_per_bh), kBwdThreads, sm_kv, st>>>(
+      tk128, tv128, tq64, tg64, p);
+  const int TK = (sh->Nk + kBarK - 1) / kBarK;
+  vs_bwd_kv_kernel<D, false><<<unsigned(int64_t(sh->B) * sh->Hkv * TK), kBwdThreads, sm_kv, st>>>(
+      tk128, tv128, tq64, tg64, p);
+  const int T = (sh->Nq + kQTile - 1) / kQTile;
+  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tq128, tg128, tk64,
+                                                                                          tv64, p);
+  note_launch(4);
+  return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(const vs_shape* s, int kv) {
+  return size_t(bwd_layout(s->B, s->Hq, s->Nq, s->d, kv).total);
+}
+
+vs_status launch_bwd(const vs_shape* s, const Geo&, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
+                     float* dq_acc, void* ws, size_t ws_bytes, cudaStream_t st) {
+  BwdParams p = make_params(s, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, ws, ws_bytes);
+  // Grid of the bar kernel: (KVP / 128) chunks x splits per (b, h).  KVP
+  // lives in the arena header on the device; the largest value the
+  // workspace can hold bounds it, and CTAs beyond the real count exit.
+  const BwdLayout L1 = bwd_layout(s->B, s->Hq, s->Nq, s->d, kBarK);
+  const int64_t per_chunk = int64_t(L1.smax) * s->B * s->Hq * kBarK * s->d * 4 * 2;
+  const int64_t room = int64_t(ws_bytes) - L1.off_bar_dk;
+  int64_t nchunk = room > 0 ? room / per_chunk : 1;
+  const int64_t cap = (int64_t(s->Nk) + kBarK - 1) / kBarK;
+  if (nchunk > cap) nchunk = cap;
+  if (nchunk < 1) nchunk = 1;
+  p.bar_nchunk = int(nchunk);
+  const int grid_per_bh = int(nchunk * L1.smax);
+  if (s->d == 128) return launch_bwd_d<128>(s, p, grid_per_bh, st);
+  if (s->d == 64) return launch_bwd_d<64>(s, p, grid_per_bh, st);
+  return VS_ERR_SHAPE;
+}
+
+}  // namespace vs

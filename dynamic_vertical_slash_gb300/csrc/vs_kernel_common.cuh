@@ -1,0 +1,81 @@
+// Device helpers shared by the attention kernels: geometry from the arena
+// header, per-unit masks, fast exp2, the bar-chunk gather.
+#pragma once
+#include "sm100_ptx.cuh"
+#include "vs_common.cuh"
+
+namespace vs {
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ Geo geo_from(const ArenaHeader* h, int Hkv, int d) {
+  Geo G;
+  G.B = h->B;
+  G.Nq = h->Nq;
+  G.Nk = h->Nk;
+  G.Hq = h->Hq;
+  G.Hkv = Hkv;
+  G.d = d;
+  G.g = h->Hq / Hkv;
+  G.world = h->world;
+  G.q_rank = h->q_rank;
+  G.kv_rank = h->kv_rank;
+  G.WG = h->WG;
+  G.WL = h->WL;
+  G.EMAX = h->EMAX;
+  G.KVP = h->KVP;
+  G.N_global = h->N_global;
+  return G;
+}
+
+// Slash-tile mask of one query row against the 64 keys starting at local key
+// c (query-major passes).  Bit k set iff offset n_g - m_g(c + k) is selected,
+// key c + k is not a selected column, and the key exists (c + k >= 0).  The
+// 64 keys are globally contiguous (unstriped, or c block-aligned).
+__device__ __forceinline__ uint64_t slash_row_mask(const Geo& G, const uint64_t* offbits, const uint64_t* colbits,
+                                                   int64_t n_g, int64_t c) {
+  const int64_t m0 = (c >= 0) ? kpos_g(G, c) : c;  // c < 0 only without striping
+  const int64_t base = n_g - m0;                    // offset of key k is base - k
+  const uint64_t x = bits64(offbits, base - 63, G.WG);
+  uint64_t m = __brevll(x);                          // bit k <-> offset base - k
+  m &= ~bits64(colbits, m0, G.WG);                   // vertical entries belong to the bars
+  if (c < 0) m &= (~0ull) << (-c);
+  return m;
+}
+
+// Key-major slash mask of one key (local index kl) against the 64 rows
+// starting at local row r0: bit i set iff offset n_g(r0 + i) - m_g(kl) is
+// selected and row r0 + i exists.  The caller clears the whole mask when the
+// key is a selected column of the head.
+__device__ __forceinline__ uint64_t slash_col_mask(const Geo& G, const uint64_t* offbits, int64_t kl, int64_t r0) {
+  const int64_t base = qpos_g(G, r0) - kpos_g(G, kl);
+  uint64_t m = bits64(offbits, base, G.WG);
+  const int64_t rows = int64_t(G.Nq) - r0;
+  if (rows < 64) m &= (rows <= 0) ? 0ull : ((1ull << rows) - 1);
+  return m;
+}
+
+// Issues the cp.async gather of `nrows` key rows (index list `keys`, -1 =
+// zero row) of a [*, Hkv, d] bf16 tensor into a 128B-swizzled K-major tile:
+// row r, 16-byte chunk j of half hf lands at dst + hf*rows*128 + r*128 +
+// ((j ^ (r & 7)) * 16).  Called by all 32 lanes of a warp.
+template <int D>
+__device__ __forceinline__ void gather_rows(uint32_t dst, int rows_in_tile, const uint8_t* base, int64_t s_tok,
+                                            const int32_t* keys, int nrows, int lane) {
+  constexpr int NH = D / 64;
+  for (int idx = lane; idx < nrows * 8 * NH; idx += 32) {
+    const int r = idx / (8 * NH);
+    const int rem = idx % (8 * NH);
+    const int hf = rem / 8, j = rem % 8;
+    const int key = __ldg(keys + r);
+    const uint8_t* src = base + (key >= 0 ? int64_t(key) * s_tok * 2 : 0) + hf * 128 + j * 16;
+    const uint32_t d = dst + hf * rows_in_tile * 128 + r * 128 + ((j ^ (r & 7)) << 4);
+    cp_async_16(d, src, key >= 0 ? 16u : 0u);
+  }
+}
+
+}  // namespace vs

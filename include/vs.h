@@ -1,0 +1,206 @@
+/*
+ * vs.h -- C ABI of the GB300 (sm_103a) Vertical-Slash sparse attention library
+ * (libvs.so).
+ *
+ * The library implements the hot path of MTraining's dynamic sparse
+ * attention ("MTraining: Distributed Dynamic Sparse Attention for Efficient
+ * Ultra-Long Context Training"): the online Vertical-Slash estimator of
+ * Algorithm 1, the sparse index (Algorithm 1 `sparseformat`, Algorithm 2
+ * `convert_index`), causal GQA attention forward and backward restricted to
+ * the selected columns and diagonals (Eq. 1, Eq. 2), and the 64-token
+ * block-level striping of Balanced Sparse Ring Attention (section 4.2).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors live in device memory and are token-major "BSHD": element
+ *    (b, n, h, c) of x is at x + b*s[0] + n*s[1] + h*s[2] + c, in elements,
+ *    with the channel dimension contiguous.  Q, K, V, O, dO, dQ, dK, dV are
+ *    bf16; LSE is fp32 [B][Hq][Nq] (contiguous); scores are fp32 [B][Hq][N].
+ *    Strides must be multiples of 8 elements (16 bytes) and base pointers
+ *    16-byte aligned (TMA requirement).
+ *  - The KV head of query head h is h / (Hq / Hkv) (GQA grouping).
+ *  - The caller owns every buffer.  The library never allocates, frees or
+ *    synchronises, except vs_check_status, which synchronises `stream`.
+ *  - Every compute call is asynchronous on `stream`.
+ *  - Argument and shape errors are returned synchronously and nothing is
+ *    launched.  Errors found on the device (bad index lists, a bounded wait
+ *    that ran out) are recorded in the first 32-bit word of the workspace or
+ *    index arena that the call received; kernels never trap.  Read them with
+ *    vs_check_status.
+ *  - Same inputs give the same output bits: no floating-point atomics touch
+ *    any output or score.
+ *  - Supported: head_dim d in {64, 128}; N a multiple of 64; Hq a multiple of
+ *    Hkv; 1 <= kv, ks <= N; last_q == 64.
+ */
+#ifndef VS_H_
+#define VS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VS_OK = 0,
+  VS_ERR_ARG = 1,       /* null pointer or bad scalar argument */
+  VS_ERR_SHAPE = 2,     /* unsupported shape, stride or alignment */
+  VS_ERR_WORKSPACE = 3, /* workspace or index arena too small */
+  VS_ERR_INDEX = 4,     /* (device) index list out of range, unsorted or duplicated */
+  VS_ERR_TIMEOUT = 5,   /* (device) a bounded wait ran out */
+  VS_ERR_CUDA = 6       /* CUDA runtime error while encoding or launching */
+} vs_status;
+
+/* Problem shape.  Nq / Nk are the local query / key lengths (equal unless a
+ * striped shard pairs one worker's queries with another worker's keys).
+ * Strides are in elements: [0] batch, [1] token, [2] head.
+ *   sq: Q, dQ      sk: K, dK      sv: V, dV      so: O, dO               */
+typedef struct {
+  int B, Nq, Nk, Hq, Hkv, d;
+  int64_t sq[3], sk[3], sv[3], so[3];
+} vs_shape;
+
+/* Striped-shard description (Balanced Sparse Ring Attention, section 4.2 (ii)
+ * and Algorithm 2).  Global 64-token block j lives on worker j mod world at
+ * local block j / world.  The local queries belong to worker q_rank and the
+ * local keys to worker kv_rank; N_global = world * Nq.  Pass NULL for an
+ * unstriped problem (world 1, identity positions). */
+typedef struct {
+  int world, stripe, q_rank, kv_rank;
+  int64_t N_global;
+} vs_stripe;
+
+/* ---------------------------------------------------------------------------
+ * vs_estimate -- online Vertical-Slash estimation (Algorithm 1, first four
+ * lines; section 4.1 (i)).
+ *
+ * For every (b, h): the observation window is the last `last_q` query rows
+ * n_i = N - last_q + i.  A_hat = softmax(scale * Q[n_i] K^T) over causal keys
+ * m <= n_i.  Vertical score v[m] = sum_i A_hat[i, m]; slash score
+ * s[o] = sum_i A_hat[i, n_i - o].  Then v_idx = argtopk(v, kv) and
+ * s_idx = argtopk(s, ks) under the total order (score descending, index
+ * ascending), each list written sorted ascending.
+ *
+ *   shape     Nq == Nk == N (global, unstriped tensors)
+ *   q, k      bf16 BSHD
+ *   last_q    must be 64
+ *   kv, ks    budgets, 1..N
+ *   v_idx     int32 [B][Hq][kv]      (out)
+ *   s_idx     int32 [B][Hq][ks]      (out)
+ *   v_score   fp32 [B][Hq][N] or NULL (out; kept in the workspace if NULL)
+ *   s_score   fp32 [B][Hq][N] or NULL
+ *   ws        device workspace of at least vs_estimate_workspace() bytes
+ * ------------------------------------------------------------------------- */
+size_t vs_estimate_workspace(const vs_shape* shape, int last_q);
+vs_status vs_estimate(const vs_shape* shape, const void* q, const void* k, int last_q, int kv, int ks, float scale,
+                      int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * vs_build_block_index -- the sparse index (Algorithm 1 `sparseformat`,
+ * Algorithm 2 `convert_index`).
+ *
+ * Turns the selected columns (v_idx, global, sorted) and diagonals (s_idx,
+ * global offsets n - m, sorted) into the arena the attention kernels read.
+ * The mask it encodes is exact at token level:
+ *     M[n, m] = (m <= n) and (m in v_idx or n - m in s_idx)
+ * on global positions.  It is covered by
+ *   - slash tiles: 128 query rows x 64 keys, holding the entries with a
+ *     selected offset whose key is not a selected column, and
+ *   - vertical bars: the selected columns gathered into chunks (64 keys for
+ *     the query-major passes, 128 for the key-major pass), holding every
+ *     causal entry of those columns,
+ * so each entry of M is computed exactly once.  With `stripe` set, the arena
+ * describes one ring step: worker q_rank's queries against worker kv_rank's
+ * keys.  The arena begins with a 256-byte header whose first int32 is the
+ * device status word.
+ *
+ *   v_idx  int32 [B][Hq][kv]; s_idx int32 [B][Hq][ks] (device)
+ *   arena  device buffer of at least vs_block_index_bytes() bytes; fully
+ *          rewritten by this call
+ * Device errors: VS_ERR_INDEX when a list is out of range, unsorted or has
+ * duplicates (the arena then describes an empty mask).
+ * ------------------------------------------------------------------------- */
+size_t vs_block_index_bytes(const vs_shape* shape, int kv, int ks, const vs_stripe* stripe);
+vs_status vs_build_block_index(const vs_shape* shape, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
+                               const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t stream);
+
+/* Work counts of an arena, for FLOP accounting (copies 4 x int64 per (b, h)
+ * to host memory; synchronises the stream):
+ *   [0] query-major slash tiles (128 x 64)    [1] query-major bar chunks (128 x 64)
+ *   [2] key-major slash units (128 x 64)      [3] key-major bar units (128 x 64)
+ * out: int64 [B][Hq][4] in host memory. */
+vs_status vs_index_counts(const void* arena, int64_t* out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * vs_attn_fwd -- dynamic sparse FlashAttention forward, y = sparse(softmax(
+ * Q K^T * scale) V, ivs) (Algorithm 1, last line; `block_bar_sparse_attention
+ * _forward` of Algorithm 2).
+ *
+ * For every query row n with a non-empty mask row: O_n = sum_{m in M(n)}
+ * softmax(S)_nm v_m and LSE_n = log sum_{m in M(n)} exp(S_nm), S = scale Q K^T.
+ * Rows with an empty mask get O = 0 and LSE = -inf.
+ *
+ *   q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] bf16; o [B,Nq,Hq,d] bf16 (out)
+ *   lse    fp32 [B][Hq][Nq] (out; in accumulate mode also in)
+ *   o_acc  NULL, or fp32 [B][Nq][Hq][d] contiguous: accumulate mode
+ *          (`merge_out_and_lse` of Algorithm 2).  The call merges its partial
+ *          result into (o_acc, lse): LSE' = log(e^LSE + e^LSE_step),
+ *          O' = (e^LSE O_acc + e^LSE_step O_step) / e^LSE', and writes o =
+ *          bf16(O').  Start a ring with o_acc = 0 and lse = -inf.
+ *   arena  from vs_build_block_index for the same shape (and stripe)
+ *   ws     at least vs_attn_fwd_workspace() bytes
+ * ------------------------------------------------------------------------- */
+size_t vs_attn_fwd_workspace(const vs_shape* shape);
+vs_status vs_attn_fwd(const vs_shape* shape, const void* q, const void* k, const void* v, const void* arena,
+                      float scale, void* o, float* lse, float* o_acc, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * vs_attn_bwd -- sparse backward on the same mask (section 3.2: the backward
+ * inherits the forward's sparsity; Eq. 1, Eq. 2).
+ *
+ *   D_n   = rowsum(dO_n * O_n)                 (= rowsum(dA * A))
+ *   P     = exp(S - LSE), dA = dO V^T
+ *   dS    = P * (dA - D)                       (Eq. 1)
+ *   dV    = P^T dO, dQ = scale dS K, dK = scale dS^T Q   (Eq. 2)
+ * dK and dV of a KV head are summed over its query heads.  All products are
+ * restricted to M.
+ *
+ *   o, lse     the forward's outputs (in a ring: the merged ones)
+ *   dO         bf16 [B,Nq,Hq,d] (strides so)
+ *   dq         bf16 out; dk, dv bf16 out [B,Nk,Hkv,d]
+ *   dq_acc     NULL, or fp32 [B][Nq][Hq][d] contiguous: accumulate mode for a
+ *              ring step (dq_acc += dQ_step; dq = bf16(dq_acc))
+ *   ws         at least vs_attn_bwd_workspace() bytes
+ * ------------------------------------------------------------------------- */
+size_t vs_attn_bwd_workspace(const vs_shape* shape, int kv);
+vs_status vs_attn_bwd(const vs_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
+                      float* dq_acc, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * striped_permute -- block-level striping (section 4.2 (ii), 64-token
+ * stripes): global block j of x [B, N, H, d] goes to shard j mod world at
+ * local block j / world of y [world, B, N/world, H, d] (both contiguous bf16).
+ * inverse = 1 maps shards back.  only_rank >= 0 writes just that shard
+ * (y then holds one shard [B, N/world, H, d]); -1 writes all.
+ * ------------------------------------------------------------------------- */
+vs_status striped_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int stripe, int inverse,
+                          int only_rank, cudaStream_t stream);
+
+/* Reads the device status word at the start of a workspace or index arena,
+ * resets it to VS_OK, and returns the code it held.  Synchronises `stream`. */
+vs_status vs_check_status(void* ws_or_arena, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* vs_status_string(vs_status status);
+
+/* Number of kernels the library launched since load (for launch counting). */
+int64_t vs_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VS_H_ */
