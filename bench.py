@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of the Vertical-Slash sparse attention hot path on GB300.
+
+One step = the whole path over one batch of synthetic input: online
+estimation (vertical / slash selection), sparse index build, sparse forward
+and sparse backward.  The headline workload is one Qwen2.5-3B-shaped
+attention layer at 128K tokens (B=1, N=131072, Hq=16, Hkv=2, d=128,
+kv=1024, ks=2048, last_q=64).
+
+Prints ONE JSON line (rank 0).  ``value`` is the executed sparse FLOPs of the
+forward + backward (the query-major cover credited at 4 d and 10 d per
+covered entry) divided by the device time of a whole step, summed over
+ranks.  Usage:
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "VS-sparse attn fwd+bwd effective TFLOP/s at 128K; % BF16 tensor peak; x vs dense"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"bf16_burst": float(d["bf16_tflops"]), "bf16_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _gpu_id(dev_index: int) -> str:
+    import torch
+
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev_index).uuid)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_sample(x, w, target_s: float = 12.0, rows_hint: int = 0):
+    """Times the CPU oracle on a bounded sample of the workload: head 0 (and
+    its KV head), the last R query rows, forward (O, LSE) and the query-side
+    backward (dQ).  Credited FLOPs: 10 d per mask entry of those rows (4 d
+    forward, 6 d for the S recompute, dP and dQ products)."""
+    import oracle
+    import synth
+
+    q = synth.bf16_to_f32(x["q"][:, :, 0:1]).astype(np.float64)
+    k = synth.bf16_to_f32(x["k"][:, :, 0:1]).astype(np.float64)
+    v = synth.bf16_to_f32(x["v"][:, :, 0:1]).astype(np.float64)
+    do = synth.bf16_to_f32(x["dout"][:, :, 0:1]).astype(np.float64)
+    t0 = time.perf_counter()
+    vs_, ss_ = oracle.estimate(q[:1], k[:1], w.last_q, w.scale)
+    iv, is_ = oracle.select(vs_, ss_, w.kv, w.ks)
+    t_est = time.perf_counter() - t0
+    p = oracle.Problem(q[:1], k[:1], v[:1], iv, is_, w.scale, dout=do[:1])
+    N = w.N
+
+    def run(R):
+        rows = np.array([(0, 0, n) for n in range(N - R, N)], np.int32)
+        t = time.perf_counter()
+        oracle.rows(p, rows)
+        dt = time.perf_counter() - t
+        return dt, rows
+
+    R = rows_hint or 64
+    if not rows_hint:
+        dt, _ = run(R)
+        R = int(max(16, min(N, R * target_s / max(dt, 1e-3))))
+    return p, run, R, t_est
+
+
+def _mask_entries(p, R, N):
+    import oracle
+
+    sub = oracle.Problem(p.q[:, N - R:], p.k, p.v, p.iv, p.is_, p.scale, qpos=np.arange(N - R, N), n_global=N)
+    return oracle.mask_count(sub)
+
+
+def reference_arm(args, w, x):
+    """--impl reference: the oracle as it stands, on the host cores."""
+    import oracle
+
+    p, run, R, t_est = _oracle_sample(x, w, target_s=max(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    entries = _mask_entries(p, R, w.N)
+    flops = 10.0 * w.d * entries
+    for _ in range(args.warmup):
+        run(R)
+    times = [run(R)[0] for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    value = flops / (ms * 1e-3) / 1e12
+    sample = ("query head 0, last %d rows of the %s workload: forward (O, LSE) + dQ, fp64, %d mask entries; "
+              "credited 10 d FLOPs per entry" % (R, w.name, entries))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def _config(w):
+    return {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "kv": w.kv, "ks": w.ks,
+            "last_q": w.last_q, "parallelism": "replicas",
+            "l2": "256 MiB buffer written between timed steps; Q/dO/O/dQ also exceed L2"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def ours(args, w, x, rank, world):
+    import torch
+
+    import dynamic_vertical_slash_gb300 as vs
+    from dynamic_vertical_slash_gb300.pipeline import dense_causal_flops, flop_counts
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v, do = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["dout"])
+    attn = vs.VSAttention(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, device=dev, last_q=w.last_q, scale=w.scale)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        attn.forward(q, k, v)
+        attn.backward(do)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    attn.check()
+    counts = attn.counts()
+    fl = flop_counts(counts, w.d)
+    executed = fl["fwd_executed"] + fl["bwd_executed"]
+
+    # ---------------- timed region: K steps, L2 flushed between them
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    vs.trace_reset()
+    launches0 = vs.launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(_gpu_id(dev.index)) as clk:
+        vs.trace_enable(True)
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+        vs.trace_enable(False)
+        torch.cuda.synchronize()
+    launches = vs.launch_count() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    trace = vs.trace_report()
+    vs.trace_reset()
+    attn.check()
+    ms = statistics.mean(step_ms)
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+        torch.distributed.barrier()
+    value = world * executed / (ms_max * 1e-3) / 1e12
+
+    # per-kernel breakdown and the roofline of the dominant attention kernel
+    per_kernel = {name: {"launches": c, "ms_total": t, "ms_avg": t / max(c, 1)} for name, (c, t) in trace.items()}
+    units = fl["units"]
+    tile = 128 * 64 * w.d
+    issued_per_step = {"fwd": 4.0 * tile * (units[0] + units[1]), "bwd_dq": 6.0 * tile * (units[0] + units[1]),
+                       "bwd_dkv_slash": 8.0 * tile * units[2], "bwd_dkv_bar": 8.0 * tile * units[3]}
+    peaks = _peaks()
+    att = {kname: per_kernel[kname] for kname in issued_per_step if kname in per_kernel}
+    dom = max(att, key=lambda kname: att[kname]["ms_total"]) if att else None
+    roofline = None
+    if dom:
+        achieved = issued_per_step[dom] / (att[dom]["ms_avg"] * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"], "traffic": None,
+                    "peak_kind": "sustained bf16 (%s): the kernel is timed inside a long step" % peaks["source"]}
+        for kname in att:
+            att[kname]["issued_tflops"] = issued_per_step[kname] / (att[kname]["ms_avg"] * 1e-3) / 1e12
+    attn_ms = sum(per_kernel[kname]["ms_avg"] for kname in att)
+
+    extra = {}
+    # ---------------- same kernels on the dense causal mask (every offset selected)
+    if rank == 0 and not args.no_dense:
+        ks_all = torch.arange(w.N, dtype=torch.int32, device=dev).repeat(w.B, w.Hq, 1).contiguous()
+        arena_d = vs.vs_build_block_index(q, k, attn.v_idx, ks_all)
+        o_d, lse_d = torch.empty_like(q), torch.empty(w.B, w.Hq, w.N, device=dev)
+        dq_d, dk_d, dv_d = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        import ctypes
+        ws_b = torch.zeros(vs.lib().vs_attn_bwd_workspace(ctypes.byref(vs.make_shape(q, k)), w.kv), dtype=torch.uint8,
+                           device=dev)
+        ws_f = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+        def dense_step():
+            vs.vs_attn_fwd(q, k, v, arena_d, w.scale, o_d, lse_d, None, ws_f)
+            vs.vs_attn_bwd(q, k, v, o_d, lse_d, do, arena_d, w.kv, w.scale, dq_d, dk_d, dv_d, None, ws_b)
+
+        dense_step()
+        torch.cuda.synchronize()
+        dts = []
+        for _ in range(args.dense_steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dense_step()
+            b.record()
+            torch.cuda.synchronize()
+            dts.append(a.elapsed_time(b))
+        if vs.vs_check_status(ws_f) or vs.vs_check_status(ws_b) or vs.vs_check_status(arena_d):
+            raise RuntimeError("dense comparison recorded a device error")
+        dense_ms = statistics.mean(dts)
+        dfl = dense_causal_flops(w.B, w.N, w.Hq, w.d)
+        extra["dense"] = {"ms_fwd_bwd": dense_ms, "tflops": (dfl["fwd"] + dfl["bwd"]) / (dense_ms * 1e-3) / 1e12}
+        extra["x_vs_dense"] = dense_ms / ms
+        extra["x_vs_dense_attention_only"] = dense_ms / attn_ms if attn_ms else None
+        del arena_d, o_d, dq_d, dk_d, dv_d, ws_b
+
+    # ---------------- end to end through the public API, host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        hq, hk, hv, hdo = (pin(t) for t in (q, k, v, do))
+        for h, t in ((hq, q), (hk, k), (hv, v), (hdo, do)):
+            h.copy_(t)
+        ho, hdq, hdk, hdv = pin(q), pin(q), pin(k), pin(v)
+        dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(t) for t in (q, k, v, do))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
+
+        def e2e_step():
+            dq_in.copy_(hq, non_blocking=True)
+            dk_in.copy_(hk, non_blocking=True)
+            dv_in.copy_(hv, non_blocking=True)
+            ddo_in.copy_(hdo, non_blocking=True)
+            o, _ = attn.forward(dq_in, dk_in, dv_in)
+            gq, gk, gv = attn.backward(ddo_in)
+            ho.copy_(o, non_blocking=True)
+            hdq.copy_(gq, non_blocking=True)
+            hdk.copy_(gk, non_blocking=True)
+            hdv.copy_(gv, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        attn.check()
+        e2e = {"value": world * executed / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "VSAttention.forward/backward (C ABI) with pinned host inputs and outputs"}
+
+    dense_f = dense_causal_flops(w.B, w.N, w.Hq, w.d)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+            "pct_bf16_peak": 100.0 * value / world / peaks["bf16_burst"],
+            "flops": {"executed_per_step": executed, "issued_per_step": fl["fwd_issued"] + fl["bwd_issued"],
+                      "dense_causal_per_step": dense_f["fwd"] + dense_f["bwd"],
+                      "executed_density": executed / (dense_f["fwd"] + dense_f["bwd"]), "units": units},
+            "kernels": per_kernel, "attention_ms_per_step": attn_ms, "step_ms_all": step_ms}
+    line.update(extra)
+    return line, clk.summary()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3b-128k")
+    ap.add_argument("--dense-steps", type=int, default=2)
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    import synth
+
+    w = synth.workloads()[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = synth.make_batch(w)
+        print(json.dumps(reference_arm(args, w, x)), flush=True)
+        return
+
+    import torch
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import datetime
+
+        torch.distributed.init_process_group("nccl", timeout=datetime.timedelta(minutes=10))
+    x = synth.make_batch(w)
+    line, clocks = ours(args, w, x, rank, world)
+    line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        p, run, R, t_est = _oracle_sample(x, w)
+        dt, _ = run(R)
+        entries = _mask_entries(p, R, w.N)
+        line["cpu_baseline"] = {"value": 10.0 * w.d * entries / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+                                "kind": "oracle",
+                                "sample": "query head 0, last %d rows of %s: forward (O, LSE) + dQ in fp64 "
+                                          "(%d mask entries, credited 10 d FLOPs each), %.1f s; the oracle's "
+                                          "estimator on that head took %.1f s" % (R, w.name, entries, dt, t_est)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -9,7 +9,8 @@ Python binding of the same names.
     striped_permute       64-token block-level striping
     vs_check_status       device status word of a workspace or arena
 """
-from ._binding import (VSError, make_shape, make_stripe, striped_permute, vs_attn_bwd, vs_attn_fwd,
+from ._binding import (VSError, make_shape, make_stripe, striped_permute, trace_enable, trace_report, trace_reset,
+                       vs_attn_bwd, vs_attn_fwd,
                        vs_build_block_index, vs_check_status, vs_estimate, vs_index_counts, lib, launch_count,
                        status_string)
 from .pipeline import VSAttention, flop_counts

@@ -223,3 +223,28 @@ def striped_permute(x, world: int, stripe: int = 64, inverse: bool = False, only
 def vs_check_status(buf, stream=None) -> int:
     """Device status word of a workspace or arena (reset to VS_OK)."""
     return int(lib().vs_check_status(_ptr(buf), _stream(stream)))
+
+
+# ------------------------------------------------------------------ tracing
+def trace_enable(on: bool = True):
+    lib().vs_trace_enable(1 if on else 0)
+
+
+def trace_reset():
+    lib().vs_trace_reset()
+
+
+def trace_report() -> dict:
+    """{kernel name: (launches, total ms)} since the last reset (synchronises)."""
+    L = lib()
+    L.vs_trace_report.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    L.vs_trace_report.restype = ctypes.c_int
+    n_max = 64
+    names = ctypes.create_string_buffer(4096)
+    counts = np.zeros(n_max, np.int64)
+    ms = np.zeros(n_max, np.float64)
+    n = L.vs_trace_report(names, 4096, ctypes.c_void_p(counts.ctypes.data), ctypes.c_void_p(ms.ctypes.data), n_max)
+    if n < 0:
+        raise VSError(VS_ERR_CUDA, "vs_trace_report")
+    keys = names.raw.split(b"\0")[:n]
+    return {k.decode(): (int(c), float(t)) for k, c, t in zip(keys, counts[:n], ms[:n])}

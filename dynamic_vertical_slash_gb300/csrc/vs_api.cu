@@ -2,12 +2,43 @@
 // handling and dispatch to the kernels.
 #include <atomic>
 #include <cstring>
+#include <string>
+#include <vector>
 #include "vs_internal.h"
 
 namespace vs {
 
 static std::atomic<int64_t> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ------------------------------------------------------------------ tracing
+struct TraceRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+static bool g_trace = false;
+static std::vector<TraceRec> g_recs;
+static cudaEvent_t g_open = nullptr;
+static const char* g_open_name = nullptr;
+
+void trace_begin(const char* name, cudaStream_t st) {
+  if (!g_trace) return;
+  if (cudaEventCreate(&g_open) != cudaSuccess) {
+    g_open = nullptr;
+    return;
+  }
+  g_open_name = name;
+  cudaEventRecord(g_open, st);
+}
+
+void trace_end(cudaStream_t st) {
+  if (!g_trace || !g_open) return;
+  cudaEvent_t e;
+  if (cudaEventCreate(&e) != cudaSuccess) return;
+  cudaEventRecord(e, st);
+  g_recs.push_back({g_open_name, g_open, e});
+  g_open = nullptr;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -80,6 +111,49 @@ const char* vs_status_string(vs_status st) {
 }
 
 int64_t vs_launch_count(void) { return g_launches.load(); }
+
+void vs_trace_enable(int on) { g_trace = on != 0; }
+
+void vs_trace_reset(void) {
+  for (auto& r : g_recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_recs.clear();
+}
+
+int vs_trace_report(char* names, int names_len, int64_t* counts, double* ms, int max_kernels) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  std::vector<std::string> keys;
+  std::vector<int64_t> cnt;
+  std::vector<double> tot;
+  for (auto& r : g_recs) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -1;
+    size_t i = 0;
+    while (i < keys.size() && keys[i] != r.name) ++i;
+    if (i == keys.size()) {
+      keys.push_back(r.name);
+      cnt.push_back(0);
+      tot.push_back(0.0);
+    }
+    cnt[i] += 1;
+    tot[i] += t;
+  }
+  int pos = 0;
+  for (size_t i = 0; i < keys.size() && int(i) < max_kernels; ++i) {
+    if (counts) counts[i] = cnt[i];
+    if (ms) ms[i] = tot[i];
+    if (names) {
+      const int len = int(keys[i].size()) + 1;
+      if (pos + len <= names_len) {
+        memcpy(names + pos, keys[i].c_str(), size_t(len));
+        pos += len;
+      }
+    }
+  }
+  return int(keys.size());
+}
 
 vs_status vs_check_status(void* ws, cudaStream_t stream) {
   if (!ws) return VS_ERR_ARG;

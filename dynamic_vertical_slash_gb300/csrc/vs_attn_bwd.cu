@@ -945,16 +945,24 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t rows = int64_t(sh->B) * sh->Hq * sh->Nq;
   const int prep_grid = int(std::min<int64_t>((rows + 255) / 256, int64_t(sms) * 8));
+  trace_begin("bwd_prep", st);
   bwd_prep<<<prep_grid, 256, 0, st>>>(p, D);
+  trace_end(st);
   // bar partials first: the slash kernel's epilogue reads them
+  trace_begin("bwd_dkv_bar", st);
   vs_bwd_kv_kernel<D, true><<<unsigned(int64_t(sh->B) * sh->Hq * grid_per_bh), kBwdThreads, sm_kv, st>>>(
       tk128, tv128, tq64, tg64, p);
+  trace_end(st);
   const int TK = (sh->Nk + kBarK - 1) / kBarK;
+  trace_begin("bwd_dkv_slash", st);
   vs_bwd_kv_kernel<D, false><<<unsigned(int64_t(sh->B) * sh->Hkv * TK), kBwdThreads, sm_kv, st>>>(
       tk128, tv128, tq64, tg64, p);
+  trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;
+  trace_begin("bwd_dq", st);
   vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tq128, tg128, tk64,
                                                                                           tv64, p);
+  trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }

@@ -420,7 +420,9 @@ vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const v
     return VS_ERR_CUDA;
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   const dim3 grid(unsigned(T) * sh->B * sh->Hq);
+  trace_begin("fwd", st);
   vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, p);
+  trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }

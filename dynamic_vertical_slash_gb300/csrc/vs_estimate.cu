@@ -344,9 +344,15 @@ vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, 
   if (cudaFuncSetAttribute(est_rowstats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm1)) != cudaSuccess ||
       cudaFuncSetAttribute(est_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm2)) != cudaSuccess)
     return VS_ERR_CUDA;
+  trace_begin("est_rowstats", st);
   est_rowstats<<<dim3(BH, kSplits), kEstThreads, sm1, st>>>(p);
+  trace_end(st);
+  trace_begin("est_scores", st);
   est_scores<<<dim3(BH, s->Nk / 64), kEstThreads, sm2, st>>>(p);
+  trace_end(st);
+  trace_begin("est_scombine", st);
   est_scombine<<<dim3((s->Nk + 255) / 256, BH), 256, 0, st>>>(p);
+  trace_end(st);
   TopkParams tp;
   tp.score = p.v;
   tp.score2 = p.s;
@@ -355,7 +361,9 @@ vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, 
   tp.N = s->Nk;
   tp.k = kv;
   tp.k2 = ks;
+  trace_begin("est_topk", st);
   est_topk<<<dim3(BH, 2), kTopkThreads, 0, st>>>(tp);
+  trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }

@@ -259,7 +259,9 @@ vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s
   P.v_idx = v_idx;
   P.s_idx = s_idx;
   if (cudaMemsetAsync(arena, 0, sizeof(int32_t), st) != cudaSuccess) return VS_ERR_CUDA;
+  trace_begin("index", st);
   vs_index_kernel<<<s->B * s->Hq, kIdxThreads, 0, st>>>(P);
+  trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }

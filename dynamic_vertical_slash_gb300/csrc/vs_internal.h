@@ -10,6 +10,10 @@ namespace vs {
 // Launch counter (all kernels launched by the library).
 void note_launch(int n = 1);
 
+// Tracing: brackets one kernel launch with CUDA events when tracing is on.
+void trace_begin(const char* name, cudaStream_t st);
+void trace_end(cudaStream_t st);
+
 // Encodes a 4-D BSHD bf16 tensor map: dims {d, H, N, B}, box {64, 1, rows, 1},
 // 128-byte swizzle.  Returns VS_OK or VS_ERR_CUDA / VS_ERR_SHAPE.
 vs_status make_tmap_bshd(CUtensorMap* m, const void* base, int B, int N, int H, int d, const int64_t s[3],

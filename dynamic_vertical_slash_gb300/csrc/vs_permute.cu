@@ -62,7 +62,9 @@ vs_status launch_permute(const void* x, void* y, int B, int64_t N, int H, int d,
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (p.total_vec + 255) / 256;
   const int grid = int(want < int64_t(sms) * 16 ? (want > 0 ? want : 1) : int64_t(sms) * 16);
+  trace_begin("striped_permute", st);
   vs_permute_kernel<<<grid, 256, 0, st>>>(p);
+  trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }

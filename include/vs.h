@@ -200,6 +200,21 @@ const char* vs_status_string(vs_status status);
 /* Number of kernels the library launched since load (for launch counting). */
 int64_t vs_launch_count(void);
 
+/* ---------------------------------------------------------------------------
+ * Kernel tracing (profiling aid; not part of the method).  While enabled,
+ * every kernel the library launches is bracketed by a pair of CUDA events
+ * recorded on the launching stream.  vs_trace_report synchronises the device,
+ * then returns, per kernel name in first-launch order, the launch count and
+ * the summed event time in milliseconds; it writes at most `max_kernels`
+ * entries, names as NUL-separated strings into `names` (capacity names_len),
+ * and returns the number of distinct kernels (or -1 on a CUDA error).
+ * vs_trace_enable(0) stops recording; vs_trace_reset drops the records.
+ * Not thread-safe; not for use during CUDA graph capture.
+ * ------------------------------------------------------------------------- */
+void vs_trace_enable(int on);
+void vs_trace_reset(void);
+int vs_trace_report(char* names, int names_len, int64_t* counts, double* ms, int max_kernels);
+
 #ifdef __cplusplus
 }
 #endif

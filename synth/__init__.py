@@ -5,8 +5,8 @@ the CUDA side.  It holds none of the method's arithmetic: it only draws
 Gaussian tensors, applies rotary position embeddings and plants vertical and
 slash structure, then rounds to bf16.
 
-Recipe for one sequence (seeded numpy PCG64, float32 until the final
-round-to-nearest-even bf16):
+Recipe for one sequence (seeded numpy PCG64 streams spawned from the seed,
+float32 until the final round-to-nearest-even bf16):
 
 1. Q, K, V, dO ~ i.i.d. N(0, 1) with shape [N, H, d].
 2. Rotate-half RoPE on Q and K, theta_i = 10000^(-2i/d) for i < d/2, pairing
@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 from typing import List, Optional, Sequence
 
 import numpy as np
@@ -126,17 +127,47 @@ def workloads() -> dict:
     return W
 
 
+def _chunks(N: int):
+    """Fixed token chunking (depends on N only, so results do not depend on
+    the number of worker threads)."""
+    n = max(1, min(64, N // 1024))
+    b = np.linspace(0, N, n + 1).astype(np.int64)
+    return [(int(b[i]), int(b[i + 1])) for i in range(n)]
+
+
+def _pool():
+    import concurrent.futures as cf
+
+    return cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+
+
 def make_sequence(N: int, Hq: int, Hkv: int, d: int, spec: SeqSpec, with_dout: bool = True):
     """One sequence: dict of bf16 bit arrays q, k, v, dout ([N, H, d] uint16)
-    plus the planted columns / offsets for reference."""
-    rng = np.random.Generator(np.random.PCG64(spec.seed))
-    q = rng.standard_normal((N, Hq, d), dtype=np.float32)
-    k = rng.standard_normal((N, Hkv, d), dtype=np.float32)
-    v = rng.standard_normal((N, Hkv, d), dtype=np.float32)
-    dout = rng.standard_normal((N, Hq, d), dtype=np.float32) if with_dout else None
+    plus the planted columns / offsets for reference.
+
+    Random streams: the seed's SeedSequence spawns one stream for the plant
+    choices and one per fixed token chunk (its K, V, Q, dO draws, in that
+    order)."""
+    ss = np.random.SeedSequence(spec.seed)
+    main_ss, chunk_ss = ss.spawn(2)
+    chunks = _chunks(N)
+    gens = [np.random.Generator(np.random.PCG64(c)) for c in chunk_ss.spawn(len(chunks))]
+    rng = np.random.Generator(np.random.PCG64(main_ss))
     cos, sin = rope_tables(N, d)
-    apply_rope(q, cos, sin)
-    apply_rope(k, cos, sin)
+    k = np.empty((N, Hkv, d), np.float32)
+    v16 = np.empty((N, Hkv, d), np.uint16)
+    q16 = np.empty((N, Hq, d), np.uint16)
+    do16 = np.empty((N, Hq, d), np.uint16) if with_dout else None
+
+    def kv_part(i):
+        a, b = chunks[i]
+        g = gens[i]
+        kk = g.standard_normal((b - a, Hkv, d), dtype=np.float32)
+        k[a:b] = apply_rope(kk, cos[a:b], sin[a:b])
+        v16[a:b] = bf16_round(g.standard_normal((b - a, Hkv, d), dtype=np.float32))
+
+    with _pool() as ex:
+        list(ex.map(kv_part, range(len(chunks))))
     cols = np.zeros((Hkv, spec.n_out), np.int64)
     for hk in range(Hkv):
         if spec.n_out:
@@ -149,28 +180,43 @@ def make_sequence(N: int, Hq: int, Hkv: int, d: int, spec: SeqSpec, with_dout: b
         offs = np.sort(rng.choice(np.arange(1, hi), size=min(spec.n_slash, hi - 1), replace=False))
     else:
         offs = np.zeros(0, np.int64)
-    if offs.size:
-        g = Hq // Hkv
-        c = np.float32(spec.gamma / math.sqrt(offs.size))
+    g_rep = Hq // Hkv
+    c = np.float32(spec.gamma / math.sqrt(offs.size)) if offs.size else np.float32(0)
+
+    def plant(a, b):
+        """c * sum over planted o of k[n - o] for n in [a, b), [b - a, Hkv, d]."""
         if spec.band:
-            # contiguous band [1, w]: add[n] = sum_{m = n-w}^{n-1} k[m], via
-            # an fp64 exclusive prefix sum over positions
-            pre = np.zeros((N + 1, Hkv, d), np.float64)
-            np.cumsum(k, axis=0, dtype=np.float64, out=pre[1:])
-            n = np.arange(N)
-            lo = np.maximum(n - offs.size, 0)
-            add = (pre[n] - pre[lo]).astype(np.float32)
-            del pre
+            w = offs.size
+            lo = max(0, a - w)
+            pre = np.zeros((b - lo + 1, Hkv, d), np.float64)
+            np.cumsum(k[lo:b], axis=0, dtype=np.float64, out=pre[1:])
+            n = np.arange(a, b)
+            add = (pre[n - lo] - pre[np.maximum(n - w, 0) - lo]).astype(np.float32)
         else:
-            add = np.zeros((N, Hkv, d), np.float32)
+            add = np.zeros((b - a, Hkv, d), np.float32)
             for o in offs:
-                add[o:] += k[: N - o]
+                s0 = max(a, int(o))
+                if s0 < b:
+                    add[s0 - a:] += k[s0 - o:b - o]
         add *= c
-        q += np.repeat(add, g, axis=1)
-    out = {"q": bf16_round(q), "k": bf16_round(k), "v": bf16_round(v),
-           "planted_cols": cols, "planted_offsets": offs}
+        return add
+
+    def q_part(i):
+        a, b = chunks[i]
+        g = gens[i]
+        qq = g.standard_normal((b - a, Hq, d), dtype=np.float32)
+        apply_rope(qq, cos[a:b], sin[a:b])
+        if offs.size:
+            qq += np.repeat(plant(a, b), g_rep, axis=1)
+        q16[a:b] = bf16_round(qq)
+        if with_dout:
+            do16[a:b] = bf16_round(g.standard_normal((b - a, Hq, d), dtype=np.float32))
+
+    with _pool() as ex:
+        list(ex.map(q_part, range(len(chunks))))
+    out = {"q": q16, "k": bf16_round(k), "v": v16, "planted_cols": cols, "planted_offsets": offs}
     if with_dout:
-        out["dout"] = bf16_round(dout)
+        out["dout"] = do16
     return out
 
 
