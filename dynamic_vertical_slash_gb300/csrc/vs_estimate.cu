@@ -369,3 +369,107 @@ vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, 
 }
 
 }  // namespace vs
+
+// ===========================================================================
+// vs_estimate_noalloc: the estimator for callers that cannot allocate device
+// memory while they run (see include/vs.h).  Its scratch is a fixed array in
+// the module's static device memory, shared by every call on a device.
+// ===========================================================================
+#include <mutex>
+
+static constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up once
+// per device (host code may not use the array's name as a device address).
+void* noalloc_scratch_address(int dev) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+// Scratch layout: 256-byte status header, per-split row statistics,
+// per-tile slash partials.  Returns the bytes needed.
+int64_t noalloc_layout(const vs_shape* s, int64_t* off_part, int64_t* off_spart) {
+  const int64_t BH = int64_t(s->B) * s->Hq, N = s->Nk, NT = N / 64;
+  int64_t off = 256;
+  *off_part = off;
+  off += (BH * vs::kSplits * vs::kLastQ * 8 + 255) / 256 * 256;
+  *off_spart = off;
+  off += (BH * NT * 128 * 4 + 255) / 256 * 256;
+  return off;
+}
+
+}  // namespace
+
+extern "C" vs_status vs_estimate_noalloc(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks,
+                                         float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score,
+                                         cudaStream_t stream) {
+  using namespace vs;
+  // every check happens on the host, before any CUDA call
+  if (!s || !q || !k || !v_idx || !s_idx || !v_score || !s_score) return VS_ERR_ARG;
+  if (s->B < 1 || s->Nk < 64 || s->Hq < 1 || s->Hkv < 1 || (s->d != 64 && s->d != 128)) return VS_ERR_SHAPE;
+  if (s->Nq != s->Nk || s->Nk % 64 || s->Hq % s->Hkv) return VS_ERR_SHAPE;
+  for (int i = 0; i < 3; ++i)
+    if (s->sq[i] <= 0 || s->sk[i] <= 0 || s->sq[i] % 8 || s->sk[i] % 8) return VS_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return VS_ERR_SHAPE;
+  if (last_q != 64) return VS_ERR_ARG;
+  if (kv < 1 || ks < 1 || kv > s->Nk || ks > s->Nk || !(scale > 0.f)) return VS_ERR_ARG;
+  int64_t off_part = 0, off_spart = 0;
+  if (size_t(noalloc_layout(s, &off_part, &off_spart)) > kNoAllocScratchBytes) return VS_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return VS_ERR_CUDA;
+  uint8_t* W = static_cast<uint8_t*>(noalloc_scratch_address(dev));
+  if (!W) return VS_ERR_CUDA;
+  // The kernels write every scratch element they later read within the
+  // call; only the status header is cleared.
+  if (cudaMemsetAsync(W, 0, 256, stream) != cudaSuccess) return VS_ERR_CUDA;
+  EstParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  for (int i = 0; i < 3; ++i) {
+    p.sq[i] = s->sq[i];
+    p.sk[i] = s->sk[i];
+  }
+  p.B = s->B;
+  p.N = s->Nk;
+  p.Hq = s->Hq;
+  p.Hkv = s->Hkv;
+  p.d = s->d;
+  p.scale_log2 = scale * kLog2e;
+  p.part = reinterpret_cast<float2*>(W + off_part);
+  p.v = v_score;
+  p.spart = reinterpret_cast<float*>(W + off_spart);
+  p.s = s_score;
+  const int BH = s->B * s->Hq;
+  const int pitch = s->d + 4;
+  const size_t sm1 = size_t(kLastQ + kChunk) * pitch * 4;
+  const size_t sm2 = (size_t(kLastQ + 64) * pitch + 64 * 65 + 64) * 4;
+  if (cudaFuncSetAttribute(est_rowstats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm1)) != cudaSuccess ||
+      cudaFuncSetAttribute(est_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm2)) != cudaSuccess)
+    return VS_ERR_CUDA;
+  est_rowstats<<<dim3(BH, kSplits), kEstThreads, sm1, stream>>>(p);
+  est_scores<<<dim3(BH, s->Nk / 64), kEstThreads, sm2, stream>>>(p);
+  est_scombine<<<dim3((s->Nk + 255) / 256, BH), 256, 0, stream>>>(p);
+  TopkParams tp;
+  tp.score = p.v;
+  tp.score2 = p.s;
+  tp.out = v_idx;
+  tp.out2 = s_idx;
+  tp.N = s->Nk;
+  tp.k = kv;
+  tp.k2 = ks;
+  est_topk<<<dim3(BH, 2), kTopkThreads, 0, stream>>>(tp);
+  note_launch(4);
+  return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}

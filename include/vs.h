@@ -99,6 +99,37 @@ vs_status vs_estimate(const vs_shape* shape, const void* q, const void* k, int l
                       cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * vs_estimate_noalloc -- vs_estimate without a caller workspace.  (The paper
+ * has no counterpart: this is a deployment convenience of this library.)
+ *
+ * Some callers cannot hand the library a workspace of their own: operator or
+ * plugin code run inside an engine that owns all device memory and forbids
+ * allocation while it executes, or latency-critical loops where cudaMalloc's
+ * implicit device-wide synchronisation would stall every other stream.  This
+ * entry point computes exactly what vs_estimate computes, with the same
+ * kernels, but keeps its scratch (row statistics and slash partials) in a
+ * fixed 32 MiB array of the library's static device memory, which every GPU
+ * that loads the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments as for vs_estimate, except that v_score and s_score are
+ *   required (the scores live in the caller's buffers, not in the scratch).
+ *   Scratch needed: 256 + B*Hq*32 KiB + B*Hq*N*8 bytes (each term rounded up
+ *   to 256); larger problems are rejected with VS_ERR_WORKSPACE before any
+ *   launch (for example B*Hq = 16 fits N up to 257984).
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array:
+ * calls that overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.  Each call writes every scratch element
+ * it reads, so stale contents from a previous call do not matter.
+ * ------------------------------------------------------------------------- */
+vs_status vs_estimate_noalloc(const vs_shape* shape, const void* q, const void* k, int last_q, int kv, int ks,
+                              float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score,
+                              cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * vs_build_block_index -- the sparse index (Algorithm 1 `sparseformat`,
  * Algorithm 2 `convert_index`).
  *
