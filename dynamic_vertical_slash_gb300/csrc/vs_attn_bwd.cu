@@ -21,8 +21,9 @@
 namespace vs {
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdStages = 3;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdCompute = 256;  // two warps per TMEM lane quarter, each owning half the columns
+constexpr int kBwdStages = 4;
 constexpr int kMaxGroup = 64;  // query heads per KV head supported by the key-major kernel
 
 struct BwdLayout {
@@ -146,9 +147,51 @@ struct DqSmem {
   uint64_t kv_full[kBwdStages], kv_empty[kBwdStages];
   uint64_t s_full[2], s_free[2], ds_full[2], ds_done[2];
   uint64_t fin, teardown;
+  uint64_t mask[kBwdStages][kQTile];  // per-stage row masks, written by the producer
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Row masks of one query-major unit (128 rows), written by the producer warp:
+// slash tiles from the offset / column bitmaps, bar chunks from the gathered
+// columns' positions.  Shared by the forward and dQ kernels' layouts.
+__device__ __forceinline__ void unit_row_masks(uint64_t* out, const Geo& G, const ArenaView& av, int64_t bh,
+                                               int t, int Nq, bool slash, int64_t c, const int32_t* keys, int lane) {
+  if (slash) {
+    const uint64_t* offbits = av.offbits + bh * G.WG;
+    const uint64_t* colbits = av.colbits + bh * G.WG;
+#pragma unroll
+    for (int rr = 0; rr < kQTile / 32; ++rr) {
+      const int row = rr * 32 + lane;
+      const int64_t nl = int64_t(t) * kQTile + row;
+      out[row] = nl < Nq ? slash_row_mask(G, offbits, colbits, qpos_g(G, nl), c) : 0ull;
+    }
+  } else {
+    int64_t kg[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = __ldg(keys + e * 32 + lane);
+      kg[e] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
+    }
+#pragma unroll
+    for (int rr = 0; rr < kQTile / 32; ++rr) {
+      const int row = rr * 32 + lane;
+      const int64_t nl = int64_t(t) * kQTile + row;
+      const int64_t ng = qpos_g(G, nl);
+      uint64_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t kge = kg[e];
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+          const int64_t mg = __shfl_sync(0xffffffffu, kge, kk);
+          m |= uint64_t(mg <= ng) << (32 * e + kk);
+        }
+      }
+      out[row] = nl < Nq ? m : 0ull;
+    }
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -192,8 +235,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], 128);
-      mbar_init(&s.ds_full[i], 128);
+      mbar_init(&s.s_free[i], kBwdCompute);
+      mbar_init(&s.ds_full[i], kBwdCompute);
       mbar_init(&s.ds_done[i], 1);
     }
     mbar_init(&s.fin, 1);
@@ -227,6 +270,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int j = 0; j < U; ++j) {
         const int st = j % kBwdStages;
         if (j >= kBwdStages && !mbar_wait(&s.kv_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+        // row masks computed ahead of the compute warps (hides the bitmap reads)
+        unit_row_masks(s.mask[st], G, av, bh, t, p.Nq, j < nslash,
+                       j < nslash ? int64_t(t) * kQTile + 64 - __ldg(elist + j) : 0,
+                       vlist + (j < nslash ? 0 : (j - nslash) * kKTile), lane);
+        __syncwarp();
         if (j < nslash) {
           if (lane == 0) {
             const int c = t * kQTile + 64 - __ldg(elist + j);
@@ -297,13 +345,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // which 32 of the 64 key columns
     const int r = quarter * 32 + lane;
     const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
     const int64_t n_loc = int64_t(t) * kQTile + r;
     const bool row_ok = n_loc < p.Nq && inputs_ok;
-    const int64_t n_g = qpos_g(G, n_loc);
-    const uint64_t* offbits = av.offbits + int64_t(bh) * G.WG;
-    const uint64_t* colbits = av.colbits + int64_t(bh) * G.WG;
     float Lr = 0.f, Dr = 0.f;
     if (row_ok) {
       const BwdLayout L = bwd_layout_dev(av.hdr, D);
@@ -318,40 +364,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[64], pr[64];
-      tmem_ld32(tl + kDqColS + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tl + kDqColS + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tl + kDqColDP + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-      tmem_ld32(tl + kDqColDP + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      uint32_t sr[32], pr[32];
+      tmem_ld32(tl + kDqColS + (j & 1) * 64 + 32 * half, sr);
+      tmem_ld32(tl + kDqColDP + (j & 1) * 64 + 32 * half, pr);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.s_free[j & 1]);
-      uint64_t mask = 0;
-      if (row_ok) {
-        if (j < nslash) {
-          const int64_t c = int64_t(t) * kQTile + 64 - __ldg(elist + j);
-          mask = slash_row_mask(G, offbits, colbits, n_g, c);
-        } else {
-          const int4* kq = reinterpret_cast<const int4*>(vlist + (j - nslash) * kKTile);
-#pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const int4 kk4 = __ldg(kq + q4);
-            const int kk[4] = {kk4.x, kk4.y, kk4.z, kk4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (kk[e] >= 0 && kpos_g(G, kk[e]) <= n_g) mask |= 1ull << (q4 * 4 + e);
-          }
-        }
+      // masks written by the producer before it released the stage
+      const int st = j % kBwdStages;
+      ok = mbar_wait(&s.kv_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
-      uint32_t pk[32];
+      const uint32_t mask = row_ok ? uint32_t(s.mask[st][r] >> (32 * half)) : 0u;
+      uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         float ds[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int c = 2 * i + e;
-          const float pv = ex2(__uint_as_float(sr[c]) * p.scale_log2 - Lr);
-          ds[e] = ((mask >> c) & 1ull) ? pv * (__uint_as_float(pr[c]) - Dr) : 0.f;
+          float pv = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -Lr));
+          pv = ((mask >> c) & 1u) ? pv : 0.f;  // one select: dS inherits the zero
+          ds[e] = pv * (__uint_as_float(pr[c]) - Dr);
         }
         pk[i] = pack_bf16x2(ds[0], ds[1]);
       }
@@ -361,8 +397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      tmem_st16(tl + kDqColDS + (j & 1) * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(tl + kDqColDS + (j & 1) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      tmem_st16(tl + kDqColDS + (j & 1) * 32 + 16 * half, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ds_full[j & 1]);
@@ -371,12 +406,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok && inputs_ok) {
-      // TMEM reads are warp-collective: every lane loads, valid rows store
+      // TMEM reads are warp-collective: every lane loads, valid rows store;
+      // each half writes its half of the d columns
       const bool store = n_loc < p.Nq;
       uint8_t* drow = p.dq + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(h) * p.sq[2]) * 2;
       float* acc = (p.dq_acc && store) ? p.dq_acc + ((int64_t(b) * p.Nq + n_loc) * p.Hq + h) * D : nullptr;
 #pragma unroll 1
-      for (int cc = 0; cc < D; cc += 16) {
+      for (int cc = (D / 2) * half; cc < (D / 2) * (half + 1); cc += 16) {
         uint32_t gv[16];
         if (U > 0) {
           tmem_ld16(tl + kDqColAcc + cc, gv);
@@ -442,8 +478,8 @@ struct KvSmem {
   uint8_t v[NH][kBarK * 128];
   uint8_t q[kBwdStages][NH][kRowTile * 128];  // B operands: 64 rows
   uint8_t g[kBwdStages][NH][kRowTile * 128];
-  float l2[kBwdStages][kRowTile];
-  float dd[kBwdStages][kRowTile];
+  alignas(16) float l2[kBwdStages][kRowTile];
+  alignas(16) float dd[kBwdStages][kRowTile];
   int32_t unit_head[kBwdStages];
   int32_t unit_row[kBwdStages];
   uint64_t kv_full;
@@ -559,9 +595,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&s.st_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
-    mbar_init(&s.s_free, 128);
+    mbar_init(&s.s_free, kBwdCompute);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.p_full[i], kBwdCompute);
       mbar_init(&s.mm_done[i], 1);
     }
     mbar_init(&s.fin, 1);
@@ -692,6 +728,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ compute
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // which 32 of the unit's 64 rows
     const int r = quarter * 32 + lane;  // key row of the tile
     const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
     int64_t kl;                          // local key index
@@ -709,11 +746,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[64], pr[64];
-      tmem_ld32(tl + kKvColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tl + kKvColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tl + kKvColDP, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-      tmem_ld32(tl + kKvColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      uint32_t sr[32], pr[32];
+      tmem_ld32(tl + kKvColS + 32 * half, sr);
+      tmem_ld32(tl + kKvColDP + 32 * half, pr);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.s_free);
@@ -735,17 +770,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!((vw >> (kl & 63)) & 1ull)) mask = slash_col_mask(G, av.offbits + bh * G.WG, kl, r0);
         }
       }
-      uint32_t pk[32], dk[32];
+      const uint32_t hm = uint32_t(mask >> (32 * half));
+      float l2v[32], ddv[32];
+      const float4* l4 = reinterpret_cast<const float4*>(&s.l2[st][32 * half]);
+      const float4* d4 = reinterpret_cast<const float4*>(&s.dd[st][32 * half]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 8; ++i) {
+        const float4 a = l4[i], c = d4[i];
+        l2v[4 * i] = a.x;
+        l2v[4 * i + 1] = a.y;
+        l2v[4 * i + 2] = a.z;
+        l2v[4 * i + 3] = a.w;
+        ddv[4 * i] = c.x;
+        ddv[4 * i + 1] = c.y;
+        ddv[4 * i + 2] = c.z;
+        ddv[4 * i + 3] = c.w;
+      }
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
         float pv[2], ds[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int c = 2 * i + e;
-          const float x = ex2(__uint_as_float(sr[c]) * p.scale_log2 - s.l2[st][c]);
-          const bool on = (mask >> c) & 1ull;
-          pv[e] = on ? x : 0.f;
-          ds[e] = on ? x * (__uint_as_float(pr[c]) - s.dd[st][c]) : 0.f;
+          float x = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2v[c]));
+          x = ((hm >> c) & 1u) ? x : 0.f;  // one select: dS inherits the zero
+          pv[e] = x;
+          ds[e] = x * (__uint_as_float(pr[c]) - ddv[c]);
         }
         pk[i] = pack_bf16x2(pv[0], pv[1]);
         dk[i] = pack_bf16x2(ds[0], ds[1]);
@@ -756,10 +807,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after();
-      tmem_st16(tl + kKvColP + (j & 1) * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(tl + kKvColP + (j & 1) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-      tmem_st16(tl + kKvColDS + (j & 1) * 32, *reinterpret_cast<uint32_t(*)[16]>(&dk[0]));
-      tmem_st16(tl + kKvColDS + (j & 1) * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&dk[16]));
+      tmem_st16(tl + kKvColP + (j & 1) * 32 + 16 * half, pk);
+      tmem_st16(tl + kKvColDS + (j & 1) * 32 + 16 * half, dk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.p_full[j & 1]);
@@ -777,7 +826,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float* pdk = reinterpret_cast<float*>(p.ws + L.off_bar_dk) + ((int64_t(split) * p.B * p.Hq + bh) * G.KVP + rank) * D;
           float* pdv = reinterpret_cast<float*>(p.ws + L.off_bar_dv) + ((int64_t(split) * p.B * p.Hq + bh) * G.KVP + rank) * D;
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 16) {
+          for (int cc = (D / 2) * half; cc < (D / 2) * (half + 1); cc += 16) {
             uint32_t a[16], c2[16];
             tmem_ld16(tl + kKvColDK + cc, a);
             tmem_ld16(tl + kKvColDV + cc, c2);
@@ -800,7 +849,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float* bdk = reinterpret_cast<const float*>(p.ws + L.off_bar_dk);
         const float* bdv = reinterpret_cast<const float*>(p.ws + L.off_bar_dv);
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 16) {
+        for (int cc = (D / 2) * half; cc < (D / 2) * (half + 1); cc += 16) {
           float yk[16], yv[16];
           if (U > 0) {
             uint32_t a[16], c2[16];
