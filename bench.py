@@ -13,6 +13,11 @@ covered entry) divided by the device time of a whole step, summed over
 ranks.  Usage:
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+``--workload qwen3b-512k-striped8`` runs worker 0 of the 8-worker striped
+ring instead (524288 global tokens, 64-token stripes) and adds each ring
+step's executed FLOPs and time and their imbalance to the line.
 """
 from __future__ import annotations
 
@@ -346,6 +351,106 @@ def ours(args, w, x, rank, world):
     return line, clk.summary()
 
 
+def striped(args, w, x, rank, world):
+    """Striped-shard workload: worker 0 of ``w.world`` runs the whole ring on
+    one GPU (global selection, one index per ring step, forward merging each
+    step's partial, backward accumulating dQ and emitting each source shard's
+    dK / dV).  Reports per ring step the executed FLOPs and device time and
+    their imbalance (max / mean)."""
+    import torch
+
+    import dynamic_vertical_slash_gb300 as vs
+    from dynamic_vertical_slash_gb300.pipeline import dense_causal_flops, flop_counts
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    W = w.world
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    q0 = vs.striped_permute(q, W, w.stripe, only_rank=0)
+    do0 = vs.striped_permute(to_dev(x["dout"]), W, w.stripe, only_rank=0)
+    ksh, vsh = vs.striped_permute(k, W, w.stripe), vs.striped_permute(v, W, w.stripe)
+    wk = vs.StripedWorker(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, W, rank=0, stripe=w.stripe, device=dev,
+                          last_q=w.last_q, scale=w.scale)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        wk.select(q, k)
+        wk.build_index(q0, ksh)
+        wk.forward(q0, ksh, vsh)
+        wk.backward(do0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    wk.check()
+    counts = wk.counts()
+    per = [flop_counts(c, w.d) for c in counts]
+    executed = sum(f["fwd_executed"] + f["bwd_executed"] for f in per)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    vs.trace_reset()
+    launches0 = vs.launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(_gpu_id(dev.index)) as clk:
+        vs.trace_enable(True)
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+        vs.trace_enable(False)
+        torch.cuda.synchronize()
+    launches = vs.launch_count() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ring_ms = wk.step_times()  # the last timed step's ring steps
+    trace = vs.trace_report()
+    vs.trace_reset()
+    wk.check()
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * executed / (ms * 1e-3) / 1e12
+    per_kernel = {name: {"launches": c, "ms_total": t, "ms_avg": t / max(c, 1)} for name, (c, t) in trace.items()}
+    peaks = _peaks()
+    tile = 128 * 64 * w.d
+    units = np.sum([f["units"] for f in per], axis=0)
+    issued = {"fwd": 4.0 * tile * (units[0] + units[1]), "bwd_dq": 6.0 * tile * (units[0] + units[1]),
+              "bwd_dkv_slash": 8.0 * tile * units[2], "bwd_dkv_bar": 8.0 * tile * units[3]}
+    att = {kn: per_kernel[kn] for kn in issued if kn in per_kernel}
+    dom = max(att, key=lambda kn: att[kn]["ms_total"])
+    achieved = issued[dom] / (att[dom]["ms_total"] / args.steps * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"], "traffic": None,
+                "peak_kind": "sustained bf16 (%s): all ring steps of the kernel per timed step" % peaks["source"]}
+    ring = []
+    for s in range(W):
+        f = per[s]
+        ring.append({"step": s, "src": wk.source(s), "executed_flops": f["fwd_executed"] + f["bwd_executed"],
+                     "units": f["units"], "ms_fwd": ring_ms[s][0], "ms_bwd": ring_ms[s][1]})
+    fl = np.array([r["executed_flops"] for r in ring])
+    tm = np.array([r["ms_fwd"] + r["ms_bwd"] for r in ring])
+    dense_f = dense_causal_flops(w.B, w.N, w.Hq, w.d)
+    cfg = _config(w)
+    cfg.update({"world": W, "stripe": w.stripe, "worker": 0, "ring": "src = -s mod world, KV shards local"})
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg, "roofline": roofline,
+            "e2e": None, "gpu_launches": launches,
+            "pct_bf16_peak": 100.0 * value / world / peaks["bf16_burst"],
+            "flops": {"executed_per_step": executed,
+                      "dense_causal_worker_per_step": (dense_f["fwd"] + dense_f["bwd"]) / W,
+                      "executed_density": executed / ((dense_f["fwd"] + dense_f["bwd"]) / W)},
+            "ring_steps": ring,
+            "imbalance": {"flops_max_over_mean": float(fl.max() / fl.mean()),
+                          "ms_max_over_mean": float(tm.max() / tm.mean())},
+            "kernels": per_kernel, "step_ms_all": step_ms}
+    return line, clk.summary()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -383,9 +488,9 @@ def main():
 
         torch.distributed.init_process_group("nccl", timeout=datetime.timedelta(minutes=10))
     x = synth.make_batch(w)
-    line, clocks = ours(args, w, x, rank, world)
+    line, clocks = (striped if w.world > 1 else ours)(args, w, x, rank, world)
     line["clocks"] = clocks
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and w.world == 1 and not args.no_cpu_baseline:
         import oracle
 
         p, run, R, t_est = _oracle_sample(x, w)

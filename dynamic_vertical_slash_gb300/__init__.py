@@ -13,8 +13,8 @@ from ._binding import (VSError, make_shape, make_stripe, striped_permute, trace_
                        vs_attn_bwd, vs_attn_fwd,
                        vs_build_block_index, vs_check_status, vs_estimate, vs_index_counts, lib, launch_count,
                        status_string)
-from .pipeline import VSAttention, flop_counts
+from .pipeline import StripedWorker, VSAttention, flop_counts
 
 __all__ = ["VSError", "make_shape", "make_stripe", "striped_permute", "vs_attn_bwd", "vs_attn_fwd",
            "vs_build_block_index", "vs_check_status", "vs_estimate", "vs_index_counts", "lib", "launch_count",
-           "status_string", "VSAttention", "flop_counts"]
+           "status_string", "VSAttention", "StripedWorker", "flop_counts"]

@@ -83,9 +83,16 @@ class VSAttention:
         self.ws_bwd = torch.zeros(L.vs_attn_bwd_workspace(ctypes.byref(sh), kv), dtype=torch.uint8, device=dev)
         self._qkv = None
 
-    def forward(self, q, k, v, stream=None):
-        B_.vs_estimate(q, k, self.kv, self.ks, self.scale, self.last_q, self.v_idx, self.s_idx, self.v_score,
-                       self.s_score, self.ws_est, stream)
+    def forward(self, q, k, v, stream=None, selection=None):
+        """Estimate, index, sparse forward.  ``selection`` = (v_idx, s_idx)
+        int32 device tensors [B, Hq, kv] / [B, Hq, ks] (sorted ascending)
+        replaces the estimator, e.g. to reuse one layer's selection."""
+        if selection is None:
+            B_.vs_estimate(q, k, self.kv, self.ks, self.scale, self.last_q, self.v_idx, self.s_idx, self.v_score,
+                           self.s_score, self.ws_est, stream)
+        else:
+            self.v_idx.copy_(selection[0])
+            self.s_idx.copy_(selection[1])
         B_.vs_build_block_index(q, k, self.v_idx, self.s_idx, None, self.arena, stream)
         B_.vs_attn_fwd(q, k, v, self.arena, self.scale, self.o, self.lse, None, self.ws_fwd, stream)
         self._qkv = (q, k, v)
@@ -106,3 +113,119 @@ class VSAttention:
 
     def counts(self) -> np.ndarray:
         return B_.vs_index_counts(self.arena)
+
+
+class StripedWorker:
+    """One worker's side of the striped ring on one GPU (MTraining, section
+    4.2 (ii) and Algorithm 2): the sequence of N_global tokens is cut into
+    ``stripe``-token blocks dealt round-robin to ``world`` workers; worker
+    ``rank`` keeps its query shard and, at ring step s, attends to the KV
+    shard of source ``(rank - s) mod world`` with the index built on global
+    positions, merging each step's (O, LSE) into the running result.
+
+    The KV shards of every source sit in this GPU's memory (the ring's
+    point-to-point rotation is not run); each step's forward and backward are
+    timed with CUDA events so per-step load and its imbalance can be read
+    off.  Buffers are preallocated; the selection is made once, on the
+    global sequence, by ``select``.
+    """
+
+    def __init__(self, B: int, N_global: int, Hq: int, Hkv: int, d: int, kv: int, ks: int, world: int,
+                 rank: int = 0, stripe: int = 64, device="cuda", last_q: int = 64, scale: Optional[float] = None):
+        if N_global % (world * stripe):
+            raise ValueError("N_global must be a multiple of world * stripe")
+        self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N_global, Hq, Hkv, d, kv, ks
+        self.world, self.rank, self.stripe, self.last_q = world, rank, stripe, last_q
+        self.scale = 1.0 / math.sqrt(d) if scale is None else scale
+        dev = torch.device(device)
+        Nl = N_global // world
+        self.Nl = Nl
+        L = B_.lib()
+        import ctypes
+        qg = torch.empty(B, N_global, Hq, d, dtype=torch.bfloat16, device="meta")
+        kg = torch.empty(B, N_global, Hkv, d, dtype=torch.bfloat16, device="meta")
+        shg = B_.make_shape(qg, kg)
+        self.v_idx = torch.empty(B, Hq, kv, dtype=torch.int32, device=dev)
+        self.s_idx = torch.empty(B, Hq, ks, dtype=torch.int32, device=dev)
+        self.v_score = torch.empty(B, Hq, N_global, dtype=torch.float32, device=dev)
+        self.s_score = torch.empty(B, Hq, N_global, dtype=torch.float32, device=dev)
+        self.ws_est = torch.zeros(max(256, L.vs_estimate_workspace(ctypes.byref(shg), last_q)), dtype=torch.uint8,
+                                  device=dev)
+        ql = torch.empty(B, Nl, Hq, d, dtype=torch.bfloat16, device=dev)
+        kl = torch.empty(B, Nl, Hkv, d, dtype=torch.bfloat16, device=dev)
+        shl = B_.make_shape(ql, kl)
+        self.stripes = [B_.make_stripe(world, rank, self.source(s), N_global, stripe) for s in range(world)]
+        self.arenas = [torch.empty(L.vs_block_index_bytes(ctypes.byref(shl), kv, ks, ctypes.byref(st)),
+                                   dtype=torch.uint8, device=dev) for st in self.stripes]
+        self.o = torch.empty_like(ql)
+        self.lse = torch.empty(B, Hq, Nl, dtype=torch.float32, device=dev)
+        self.o_acc = torch.empty(B, Nl, Hq, d, dtype=torch.float32, device=dev)
+        self.ws_fwd = torch.zeros(256, dtype=torch.uint8, device=dev)
+        self.dq = torch.empty_like(ql)
+        self.dq_acc = torch.empty(B, Nl, Hq, d, dtype=torch.float32, device=dev)
+        self.dk = torch.empty(world, B, Nl, Hkv, d, dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty_like(self.dk)
+        self.ws_bwd = torch.zeros(L.vs_attn_bwd_workspace(ctypes.byref(shl), kv), dtype=torch.uint8, device=dev)
+        # per ring step: forward start / end, backward start / end
+        self.events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(world)]
+        self._qkv = None
+
+    def source(self, s: int) -> int:
+        """The KV shard worker ``rank`` attends to at ring step s."""
+        return (self.rank - s) % self.world
+
+    def select(self, q_global, k_global, stream=None):
+        """Vertical / slash selection on the global sequence (Algorithm 1's
+        estimate over the last ``last_q`` global queries)."""
+        B_.vs_estimate(q_global, k_global, self.kv, self.ks, self.scale, self.last_q, self.v_idx, self.s_idx,
+                       self.v_score, self.s_score, self.ws_est, stream)
+        return self.v_idx, self.s_idx
+
+    def build_index(self, q_shard, k_shards, stream=None):
+        """One index per ring step, on global positions through the stripe map."""
+        for s in range(self.world):
+            B_.vs_build_block_index(q_shard, k_shards[self.source(s)], self.v_idx, self.s_idx, self.stripes[s],
+                                    self.arenas[s], stream)
+
+    def forward(self, q_shard, k_shards, v_shards, stream=None):
+        """World ring steps; each merges its partial (O, LSE) into the running
+        result (merge_out_and_lse).  Returns (o bf16, lse fp32)."""
+        self.lse.fill_(-math.inf)
+        self.o_acc.zero_()
+        for s in range(self.world):
+            src = self.source(s)
+            self.events[s][0].record(stream)
+            B_.vs_attn_fwd(q_shard, k_shards[src], v_shards[src], self.arenas[s], self.scale, self.o, self.lse,
+                           self.o_acc, self.ws_fwd, stream)
+            self.events[s][1].record(stream)
+        self._qkv = (q_shard, k_shards, v_shards)
+        return self.o, self.lse
+
+    def backward(self, dO_shard, stream=None):
+        """dQ accumulated over the ring steps; dK / dV of each source shard
+        from this worker's queries (what goes back to the shard's owner)."""
+        q, ks_, vs_ = self._qkv
+        self.dq_acc.zero_()
+        for s in range(self.world):
+            src = self.source(s)
+            self.events[s][2].record(stream)
+            B_.vs_attn_bwd(q, ks_[src], vs_[src], self.o, self.lse, dO_shard, self.arenas[s], self.kv, self.scale,
+                           self.dq, self.dk[src], self.dv[src], self.dq_acc, self.ws_bwd, stream)
+            self.events[s][3].record(stream)
+        return self.dq, self.dk, self.dv
+
+    def step_times(self):
+        """Per ring step (forward ms, backward ms) of the last forward /
+        backward pair (after a synchronize)."""
+        return [(e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3])) for e in self.events]
+
+    def check(self):
+        """Raises if any kernel recorded a device error."""
+        for buf in [self.ws_est, self.ws_fwd, self.ws_bwd] + self.arenas:
+            code = B_.vs_check_status(buf)
+            if code:
+                raise B_.VSError(code, "device status")
+
+    def counts(self) -> np.ndarray:
+        """Work units per ring step: [world, B, Hq, 4]."""
+        return np.stack([B_.vs_index_counts(a) for a in self.arenas])

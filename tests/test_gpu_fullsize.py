@@ -1,0 +1,216 @@
+"""Parity at the full sizes of the named workloads, through the same buffers
+and launches the benchmark times (``VSAttention`` / ``StripedWorker``), on
+outputs the fp64 oracle computes one at a time:
+
+* selection: the GPU's fp32 scores against the oracle's fp64 estimate
+  (within 1e-4 of the largest score), the GPU's indices bit-exact under the
+  replay rule (the oracle's top-k on the GPU's own scores), and every index
+  on which the two selections differ inside the tolerance band of the k-th
+  score;
+* attention, on the oracle's own selection: O, LSE and dQ of sampled query
+  rows (first, last and random rows of every head) and dK / dV of sampled
+  keys (the last keys of the sequence, vertical ones among them, and a key in
+  the middle that only slash lines reach), with O / dQ / dK / dV relative L2
+  <= 1e-2 over the sample and LSE absolute <= 1e-3.
+
+The oracle widens only the rows it needs: the query / dO rows of the sampled
+rows and of every row that reaches a sampled key.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from vs_testutil import dev_bf16, host_f64, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+SCORE_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def vs():
+    import dynamic_vertical_slash_gb300 as m
+
+    m.lib()
+    return m
+
+
+def _f64(bits):
+    return synth.bf16_to_f32(bits).astype(np.float64)
+
+
+def _oracle_scores(x, w):
+    """Oracle estimate: only the last ``last_q`` query rows are read, so the
+    rest of q is left as zeros (never widened)."""
+    B, N, Hq, d = x["q"].shape
+    q = np.zeros((B, N, Hq, d), np.float64)
+    q[:, N - w.last_q:] = _f64(x["q"][:, N - w.last_q:])
+    return oracle.estimate(q, _f64(x["k"]), w.last_q, w.scale)
+
+
+def _check_selection(v_gpu, s_gpu, iv_gpu, is_gpu, v_ref, s_ref, iv_ref, is_ref, kv, ks):
+    B, Hq, N = v_ref.shape
+    for b in range(B):
+        for h in range(Hq):
+            for sc_g, sc_r, idx_g, idx_r, k in ((v_gpu, v_ref, iv_gpu, iv_ref, kv), (s_gpu, s_ref, is_gpu, is_ref, ks)):
+                top = sc_r[b, h].max()
+                assert np.max(np.abs(sc_g[b, h] - sc_r[b, h])) <= SCORE_TOL * top, (b, h)
+                np.testing.assert_array_equal(oracle.topk(sc_g[b, h], k), idx_g[b, h])
+                diff = np.setxor1d(idx_g[b, h], idx_r[b, h])
+                if diff.size:
+                    kth = np.sort(sc_r[b, h])[::-1][k - 1]
+                    assert np.all(np.abs(sc_r[b, h][diff] - kth) <= 2 * SCORE_TOL * top), (b, h, diff)
+
+
+def _sample_rows(N, rng, count=6):
+    mid = rng.choice(np.arange(2, N - 2), count - 4, replace=False)
+    return np.unique(np.concatenate([[0, 1, N - 2, N - 1], mid]))
+
+
+def _rows_reaching(m, ivh, ish, N):
+    """Every row n >= m whose mask holds key m in one of the given heads."""
+    rows = set()
+    for iv_row, is_row in zip(ivh, ish):
+        if m in set(iv_row.tolist()):
+            rows.update(range(m, N))
+        rows.update(int(m + o) for o in is_row if m + o < N)
+    return rows
+
+
+def _sample_keys(b, hk, g, iv, is_, N, rng, dense):
+    """Keys of KV head hk: the last ones (vertical ones preferred) and one
+    mid-sequence key no vertical list holds."""
+    tail = 128 if dense else 2048
+    ivh = iv[b, hk * g:(hk + 1) * g]
+    vert = sorted({int(m) for m in ivh.ravel() if m >= N - tail})
+    keys = vert[-2:] + sorted(rng.choice(np.arange(N - tail, N), 3, replace=False).tolist())
+    if not dense:
+        held = set(ivh.ravel().tolist())
+        for m in rng.permutation(np.arange(N // 4, 3 * N // 4)):
+            if int(m) not in held:
+                keys.append(int(m))
+                break
+    return sorted(set(keys))
+
+
+def _compare_rows(p, rows_bhn, o_gpu, lse_gpu, dq_gpu):
+    o_ref, lse_ref, dq_ref = oracle.rows(p, rows_bhn)
+    assert rel_l2(o_gpu, o_ref) <= TOL
+    assert rel_l2(dq_gpu, dq_ref) <= TOL
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_array_equal(np.isfinite(lse_gpu), fin)
+    assert np.max(np.abs(lse_gpu[fin] - lse_ref[fin]), initial=0.0) <= 1e-3
+
+
+@pytest.mark.parametrize("name", ["qwen3b-32k", "qwen3b-128k", "batch4-64k", "dense-64k"])
+def test_fullsize_sampled_parity(vs, name):
+    w = synth.workloads()[name]
+    x = synth.make_batch(w)
+    B, N, Hq, Hkv, d, g = w.B, w.N, w.Hq, w.Hkv, w.d, w.Hq // w.Hkv
+    dense = w.ks >= N
+    q, k, v, do = (dev_bf16(x[n]) for n in ("q", "k", "v", "dout"))
+    att = vs.VSAttention(B, N, Hq, Hkv, d, w.kv, w.ks, last_q=w.last_q, scale=w.scale)
+
+    # ---- selection: the pipeline's own estimator against the oracle's
+    att.forward(q, k, v)
+    torch.cuda.synchronize()
+    att.check()
+    v_gpu, s_gpu = att.v_score.cpu().numpy(), att.s_score.cpu().numpy()
+    iv_gpu, is_gpu = att.v_idx.cpu().numpy(), att.s_idx.cpu().numpy()
+    v_ref, s_ref = _oracle_scores(x, w)
+    iv, is_ = oracle.select(v_ref, s_ref, w.kv, w.ks)
+    _check_selection(v_gpu, s_gpu, iv_gpu, is_gpu, v_ref, s_ref, iv, is_, w.kv, w.ks)
+
+    # ---- attention on the oracle's selection, same buffers and launches
+    att.forward(q, k, v, selection=(torch.from_numpy(iv).cuda(), torch.from_numpy(is_).cuda()))
+    dq, dk, dv = att.backward(do)
+    torch.cuda.synchronize()
+    att.check()
+    o_h, lse_h = host_f64(att.o), att.lse.cpu().numpy().astype(np.float64)
+    dq_h, dk_h, dv_h = host_f64(dq), host_f64(dk), host_f64(dv)
+    kf, vf = _f64(x["k"]), _f64(x["v"])
+    rng = np.random.default_rng(99)
+    for b in range(B):
+        rows = _sample_rows(N, rng)
+        keys = {hk: _sample_keys(b, hk, g, iv, is_, N, rng, dense) for hk in range(Hkv)}
+        need = set(rows.tolist())
+        for hk, ks_ in keys.items():
+            for m in ks_:
+                need |= _rows_reaching(m, iv[b, hk * g:(hk + 1) * g], is_[b, hk * g:(hk + 1) * g], N)
+        pos = np.array(sorted(need), np.int64)
+        loc = {int(n): i for i, n in enumerate(pos)}
+        p = oracle.Problem(_f64(x["q"][b:b + 1, pos]), kf[b:b + 1], vf[b:b + 1], iv[b:b + 1], is_[b:b + 1],
+                           w.scale, dout=_f64(x["dout"][b:b + 1, pos]), qpos=pos, n_global=N)
+        rb = np.array([(0, h, loc[int(n)]) for h in range(Hq) for n in rows], np.int32)
+        _compare_rows(p, rb, np.stack([o_h[b, n, h] for h in range(Hq) for n in rows]),
+                      np.array([lse_h[b, h, n] for h in range(Hq) for n in rows]),
+                      np.stack([dq_h[b, n, h] for h in range(Hq) for n in rows]))
+        kb = np.array([(0, hk, m) for hk in range(Hkv) for m in keys[hk]], np.int32)
+        dk_ref, dv_ref = oracle.keys(p, kb)
+        assert rel_l2(np.stack([dk_h[b, m, hk] for hk in range(Hkv) for m in keys[hk]]), dk_ref) <= TOL
+        assert rel_l2(np.stack([dv_h[b, m, hk] for hk in range(Hkv) for m in keys[hk]]), dv_ref) <= TOL
+
+
+def test_fullsize_striped_ring_sampled_parity(vs):
+    """Worker 0 of the 8-worker striped ring at 524288 global tokens, in the
+    benchmark's launches: global selection, one index per ring step, merged
+    forward, accumulated dQ and per-source dK / dV, against the oracle's
+    global computation on worker 0's rows."""
+    w = synth.workloads()["qwen3b-512k-striped8"]
+    x = synth.make_batch(w)
+    B, N, Hq, Hkv, d, W, g = w.B, w.N, w.Hq, w.Hkv, w.d, w.world, w.Hq // w.Hkv
+    q, k, v, do = (dev_bf16(x[n]) for n in ("q", "k", "v", "dout"))
+    q0 = vs.striped_permute(q, W, w.stripe, only_rank=0)
+    do0 = vs.striped_permute(do, W, w.stripe, only_rank=0)
+    ksh, vsh = vs.striped_permute(k, W, w.stripe), vs.striped_permute(v, W, w.stripe)
+    del do
+    wk = vs.StripedWorker(B, N, Hq, Hkv, d, w.kv, w.ks, W, rank=0, stripe=w.stripe, last_q=w.last_q, scale=w.scale)
+    wk.select(q, k)
+    torch.cuda.synchronize()
+    v_ref, s_ref = _oracle_scores(x, w)
+    iv, is_ = oracle.select(v_ref, s_ref, w.kv, w.ks)
+    _check_selection(wk.v_score.cpu().numpy(), wk.s_score.cpu().numpy(), wk.v_idx.cpu().numpy(),
+                     wk.s_idx.cpu().numpy(), v_ref, s_ref, iv, is_, w.kv, w.ks)
+    wk.v_idx.copy_(torch.from_numpy(iv))
+    wk.s_idx.copy_(torch.from_numpy(is_))
+    wk.build_index(q0, ksh)
+    wk.forward(q0, ksh, vsh)
+    dq, dk, dv = wk.backward(do0)
+    torch.cuda.synchronize()
+    wk.check()
+    c = wk.counts()
+    assert c.shape == (W, B, Hq, 4) and np.all(c[:, :, :, 0] > 0)
+
+    pos0 = oracle.stripe_positions(N, W, w.stripe, 0)
+    rng = np.random.default_rng(7)
+    li = np.unique(np.concatenate([[0, 1, len(pos0) - 1], rng.choice(len(pos0), 5, replace=False)]))
+    tail = pos0[pos0 >= N - 2048]
+    need = np.unique(np.concatenate([pos0[li], tail]))
+    p = oracle.Problem(_f64(x["q"][:, need]), _f64(x["k"]), _f64(x["v"]), iv, is_, w.scale,
+                       dout=_f64(x["dout"][:, need]), qpos=need, n_global=N)
+    loc = {int(n): i for i, n in enumerate(need)}
+    o_h, lse_h, dq_h = host_f64(wk.o), wk.lse.cpu().numpy().astype(np.float64), host_f64(dq)
+    rb = np.array([(0, h, loc[int(pos0[i])]) for h in range(Hq) for i in li], np.int32)
+    _compare_rows(p, rb, np.stack([o_h[0, i, h] for h in range(Hq) for i in li]),
+                  np.array([lse_h[0, h, i] for h in range(Hq) for i in li]),
+                  np.stack([dq_h[0, i, h] for h in range(Hq) for i in li]))
+    # dK / dV of the last keys of each source shard, from worker 0's rows
+    # (rows >= N - 2048 are all in the problem, so every row reaching a key
+    # m >= N - 2048 is present)
+    dk_h, dv_h = host_f64(dk), host_f64(dv)
+    got_k, got_v, kb = [], [], []
+    for src in range(W):
+        kpos = oracle.stripe_positions(N, W, w.stripe, src)
+        for j in np.nonzero(kpos >= N - 2048)[0][-2:]:
+            for hk in range(Hkv):
+                kb.append((0, hk, int(kpos[j])))
+                got_k.append(dk_h[src, 0, j, hk])
+                got_v.append(dv_h[src, 0, j, hk])
+    dk_ref, dv_ref = oracle.keys(p, np.array(kb, np.int32))
+    assert rel_l2(np.stack(got_k), dk_ref) <= TOL
+    assert rel_l2(np.stack(got_v), dv_ref) <= TOL
