@@ -47,6 +47,47 @@ __device__ __forceinline__ uint64_t slash_row_mask(const Geo& G, const uint64_t*
   return m;
 }
 
+// The same slash-tile masks for all 128 rows of query tile t at once, built by
+// one warp: the lane's rows are rr * 32 + lane (rr = 0..3), returned in m[rr].
+// Within a 64-row block the rows' global positions are contiguous, so the
+// offset windows of its 64 rows lie in three consecutive bitmap words; lanes
+// 0-5 load the words of both blocks and lanes 6-7 the two column-bitmap words
+// (one memory round trip per tile), and every row's window is cut out of the
+// shuffled words.  Equal to slash_row_mask for every row.
+__device__ __forceinline__ void slash_tile_masks(const Geo& G, const uint64_t* offbits, const uint64_t* colbits,
+                                                 int t, int64_t c, int Nq, int lane, uint64_t (&m)[4]) {
+  const int64_t m0 = (c >= 0) ? kpos_g(G, c) : c;
+  int64_t L0[2];
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) L0[blk] = qpos_g(G, int64_t(t) * kQTile + 64 * blk) - m0 - 63;
+  uint64_t wv = 0;
+  if (lane < 6) {
+    const int64_t w = ((lane < 3 ? L0[0] : L0[1]) >> 6) + lane % 3;
+    wv = (w >= 0 && w < G.WG) ? __ldg(offbits + w) : 0ull;
+  } else if (lane < 8) {
+    const int64_t w = (m0 >> 6) + (lane - 6);
+    wv = (w >= 0 && w < G.WG) ? __ldg(colbits + w) : 0ull;
+  }
+  uint64_t W[6];
+#pragma unroll
+  for (int j = 0; j < 6; ++j) W[j] = __shfl_sync(0xffffffffu, wv, j);
+  const uint64_t C0 = __shfl_sync(0xffffffffu, wv, 6), C1 = __shfl_sync(0xffffffffu, wv, 7);
+  const int shc = int(m0 & 63);
+  const uint64_t colw = shc ? ((C0 >> shc) | (C1 << (64 - shc))) : C0;
+  const uint64_t keep = ~colw & ((c < 0) ? ((~0ull) << (-c)) : ~0ull);
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int blk = rr >> 1;
+    const int o = int(L0[blk] & 63) + (rr & 1) * 32 + lane;  // bit offset in the block's first word, 0..126
+    const uint64_t a = (o >> 6) ? W[3 * blk + 1] : W[3 * blk];
+    const uint64_t b = (o >> 6) ? W[3 * blk + 2] : W[3 * blk + 1];
+    const int sh = o & 63;
+    const uint64_t x = sh ? ((a >> sh) | (b << (64 - sh))) : a;
+    const int64_t nl = int64_t(t) * kQTile + rr * 32 + lane;
+    m[rr] = nl < Nq ? (__brevll(x) & keep) : 0ull;
+  }
+}
+
 // Key-major slash mask of one key (local index kl) against the 64 rows
 // starting at local row r0: bit i set iff offset n_g(r0 + i) - m_g(kl) is
 // selected and row r0 + i exists.  The caller clears the whole mask when the
