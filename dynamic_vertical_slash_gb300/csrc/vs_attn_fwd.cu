@@ -10,22 +10,24 @@
 // pair: fp32 online softmax on the exact token mask in registers (one thread
 // per row), P (bf16) back into TMEM.
 //
-// Warp roles (352 threads): warp 0 issues the loads, warp 10 builds each
-// pair's row masks, warp 1 issues MMAs (one lane), warps 2-5 and 6-9 are two
-// softmax warpgroups that take alternate pairs (even / odd).  Each group
-// keeps its own running maximum, sum and O accumulator, so the groups never
-// wait for each other; the epilogue merges the two partial results the way
-// merge_out_and_lse of Algorithm 2 merges ring steps.
+// Warp roles (352 threads): warp 0 issues the loads, warp 10 publishes, per
+// unit, the few words every row's mask is cut from, warp 1 issues MMAs (one
+// lane), warps 2-5 and 6-9 are two softmax warpgroups that take alternate pairs
+// (even / odd).  Each group keeps its own running maximum, sum and O
+// accumulator, so the groups never wait for each other; the epilogue merges
+// the two partial results the way merge_out_and_lse of Algorithm 2 merges
+// ring steps.
 //
 // TMEM columns: O_g [128 g, 128 g + d), S_g [256 + 128 g, +128) for group g.
-// P_g overwrites the first 64 columns of S_g once the scores are in
+// The P of a pair's first unit (keys 0-63) overwrites columns 0-31 of S_g and
+// that of its second unit columns 64-95, each once those scores are in
 // registers, so the MMA issues S of pair i + 2 into S_g only after the PV of
 // pair i; since S of pair i completes after the PV of pair i - 2, a group
 // never has to wait for its own PV before it rescales O or writes P.
 //
 // Shared memory: Q, a ring of slots that each hold K or V of one pair (128
 // rows), filled and released in the MMA's order S0 S1 PV0 S2 PV1 S3 ..., and
-// a ring of per-pair row masks.
+// a ring of per-pair mask records.
 #include "vs_internal.h"
 #include "vs_kernel_common.cuh"
 
@@ -33,25 +35,61 @@ namespace vs {
 namespace {
 
 constexpr int kFwdThreads = 352;
-constexpr int kFwdMaskWarp = 10;
+constexpr int kFwdRecWarp = 10;
 constexpr int kFwdGroup = 128;  // threads per softmax warpgroup
 constexpr int kPairKeys = 2 * kKTile;
 constexpr int kFwdSlots = 5;
-constexpr int kMaskRing = 4;
+constexpr int kRecRing = 8;
 constexpr uint32_t kColO = 0, kColS = 256, kTmemCols = 512;
 constexpr float kRefSlack = 18446744073709551616.0f;  // 2^64: largest masked pair sum accepted against the reference
+
+// What a unit's 128 row masks are cut from (written by the loader).
+//   slash tile: bits [L0 + i, L0 + i + 64) of the head's offset bitmap give
+//     row i of a 64-row block (reversed: bit k <-> offset base - k), with
+//     L0 = n_g(block row 0) - m_g(first key) - 63; W holds the three bitmap
+//     words from floor(L0 / 64) of both blocks, lo6 = L0 mod 64, and keep
+//     clears the selected columns (owned by the bars) and keys before 0;
+//   bar chunk: the 64 keys' global positions, ascending (padding last), so a
+//     row's mask is the prefix of keys at or before it.
+struct MaskRec {
+  int kind;  // 0: no unit (odd last pair), 1: slash tile, 2: bar chunk
+  int lo6[2];
+  uint64_t W[6];
+  uint64_t keep;
+  int64_t kg[kKTile];
+};
+
+// Row r's mask (bit k: key k of the unit) from its unit's record.
+__device__ __forceinline__ uint64_t rec_row_mask(const MaskRec& rc, int kind, int r, int64_t ng) {
+  if (kind == 1) {
+    const int blk = r >> 6;
+    const int o = rc.lo6[blk] + (r & 63);
+    const uint64_t a = rc.W[3 * blk + (o >> 6)], b = rc.W[3 * blk + (o >> 6) + 1];
+    const int sh = o & 63;
+    const uint64_t x = sh ? ((a >> sh) | (b << (64 - sh))) : a;
+    return __brevll(x) & rc.keep;
+  }
+  if (kind == 2) {
+    int pos = 0;
+#pragma unroll
+    for (int step = 32; step > 0; step >>= 1)
+      if (rc.kg[pos + step - 1] <= ng) pos += step;
+    const int cnt = (rc.kg[kKTile - 1] <= ng) ? kKTile : pos;
+    return cnt == kKTile ? ~0ull : ((1ull << cnt) - 1);
+  }
+  return 0ull;
+}
 
 template <int D>
 struct FwdSmem {
   static constexpr int NH = D / 64;
   uint8_t q[NH][kQTile * 128];
   uint8_t slot[kFwdSlots][NH][kPairKeys * 128];  // K or V of one pair, 128B-swizzled, per d-half
-  uint64_t mask[kMaskRing][2][kQTile];           // row masks of a pair's two units (mask warp)
-  int64_t bar_keys[kKTile];                      // mask warp: global positions of a bar chunk's keys
-  int key0[8][2];                                // loader: first key of each slash half, by pair
+  MaskRec rec[kRecRing][2];                      // mask records of a pair's two units
+  int key0[kRecRing][2];                         // loader: first key of each slash half, by pair
   uint64_t q_full;
   uint64_t slot_full[kFwdSlots], slot_empty[kFwdSlots];
-  uint64_t mask_full[kMaskRing], mask_empty[kMaskRing];
+  uint64_t rec_full[kRecRing], rec_empty[kRecRing];
   uint64_t s_full[2], p_full[2];  // per softmax group
   uint64_t o_final, teardown;
   float red_m[2][kQTile];  // per group: reference maximum (log2 units)
@@ -85,20 +123,21 @@ __device__ __forceinline__ void for_each_block(int P, F&& f) {
   }
 }
 
-// Moves a row's reference maximum for one pair (the rows with `need` set)
-// and writes the pair's P: exact masked maximum from the scores still in
-// TMEM, O and the running sum rescaled where the maximum grows, P recomputed
-// half by half against the new references and stored as it is made (P half
-// hh lands on score columns the recomputation has already read).  Rare (the
-// row's first pair, or an entry 2^64 above the reference), so it lives out
-// of line and keeps the common path's registers free.  Warp-collective.
+// Moves the rows' reference maxima for one pair (the exact online-softmax
+// update, for every row of the warp) and writes the pair's P: exact masked
+// maximum from the scores still in TMEM, O and the running sum rescaled where
+// the maximum grows, P recomputed
+// unit by unit against the new references and stored as it is made (the P
+// of unit hh lands on score columns of that unit the recomputation has
+// already read).  Rare (the row's first pair, or an entry 2^64 above the
+// reference), so it lives out of line and keeps the common path's registers
+// free.  Warp-collective.
 struct RowRef {
   float m_run, l_run;
 };
 template <int D>
 __device__ __noinline__ RowRef fwd_rebase_pair(uint32_t tl, uint32_t colS, uint32_t colO, uint64_t mask0,
-                                               uint64_t mask1, bool need, float m_run, float l_run,
-                                               float scale_log2) {
+                                               uint64_t mask1, float m_run, float l_run, float scale_log2) {
   float mx[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
@@ -113,11 +152,9 @@ __device__ __noinline__ RowRef fwd_rebase_pair(uint32_t tl, uint32_t colS, uint3
     for (int k = 0; k < 64; ++k)
       if ((mask >> k) & 1ull) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]) * scale_log2);
   }
-  const float mt =
-      need ? fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])))
-           : -INFINITY;
-  const bool grow = need && (m_run != -INFINITY) && (mt > m_run);
-  if (need && m_run == -INFINITY) m_run = mt;  // first entries: the O row is still zero
+  const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const bool grow = (m_run != -INFINITY) && (mt > m_run);
+  if (m_run == -INFINITY) m_run = mt;  // first entries (or still none): the O row is zero
   if (__any_sync(0xffffffffu, grow)) {
     const float alpha = grow ? ex2(m_run - mt) : 1.f;
 #pragma unroll 1
@@ -155,9 +192,82 @@ __device__ __noinline__ RowRef fwd_rebase_pair(uint32_t tl, uint32_t colS, uint3
       ps[k & 7] += p0 + p1;
       pk[k] = pack_bf16x2(p0, p1);
     }
-    tmem_st16(tl + colS + 32 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-    tmem_st16(tl + colS + 32 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+    tmem_st16(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+    tmem_st16(tl + colS + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
   }
+  l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+  return RowRef{m_run, l_run};
+}
+
+// The same for the pair's second unit once the first unit's P (against the
+// old references) is already in TMEM: the maximum comes from the second
+// unit's scores, and where it grows O, the running sum and the stored P of
+// the first unit are rescaled too.  A row whose reference was still unset
+// has no entry in the first unit, so its stored P is zero.
+template <int D>
+__device__ __noinline__ RowRef fwd_rebase_second(uint32_t tl, uint32_t colS, uint32_t colO, uint64_t mask1,
+                                                 float m_run, float l_run, float scale_log2) {
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+  {
+    uint32_t sr[64];
+    tmem_ld32(tl + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+    tmem_ld32(tl + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 64; ++k)
+      if ((mask1 >> k) & 1ull) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]) * scale_log2);
+  }
+  const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const bool grow = (m_run != -INFINITY) && (mt > m_run);
+  if (m_run == -INFINITY) m_run = mt;
+  if (__any_sync(0xffffffffu, grow)) {
+    const float alpha = grow ? ex2(m_run - mt) : 1.f;
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 16) {
+      uint32_t ov[16];
+      tmem_ld16(tl + colO + cc, ov);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+      tmem_st16(tl + colO + cc, ov);
+    }
+    tmem_st_wait();  // also the first unit's P stores
+#pragma unroll 1
+    for (int cc = 0; cc < 32; cc += 16) {
+      uint32_t pv[16];
+      tmem_ld16(tl + colS + cc, pv);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        pv[k] = pack_bf16x2(__uint_as_float(pv[k] << 16) * alpha, __uint_as_float(pv[k] & 0xFFFF0000u) * alpha);
+      tmem_st16(tl + colS + cc, pv);
+    }
+    if (grow) {
+      l_run *= alpha;
+      m_run = mt;
+    }
+  }
+  const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
+  float ps[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+  uint32_t sr[64], pk[32];
+  tmem_ld32(tl + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+  tmem_ld32(tl + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+  tmem_ld_wait();
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    float p0 = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, nref));
+    float p1 = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, nref));
+    p0 = ((mask1 >> (2 * k)) & 1ull) ? p0 : 0.f;
+    p1 = ((mask1 >> (2 * k + 1)) & 1ull) ? p1 : 0.f;
+    ps[k & 7] += p0 + p1;
+    pk[k] = pack_bf16x2(p0, p1);
+  }
+  tmem_st16(tl + colS + 64, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+  tmem_st16(tl + colS + 80, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
   l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
   return RowRef{m_run, l_run};
 }
@@ -213,9 +323,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&s.slot_full[i], 1);
       mbar_init(&s.slot_empty[i], 1);
     }
-    for (int i = 0; i < kMaskRing; ++i) {
-      mbar_init(&s.mask_full[i], 1);
-      mbar_init(&s.mask_empty[i], kFwdGroup);
+    for (int i = 0; i < kRecRing; ++i) {
+      mbar_init(&s.rec_full[i], 1);
+      mbar_init(&s.rec_empty[i], kFwdGroup);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -269,7 +379,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               e_pref = j < nslash ? __ldg(elist + j) : 0;
             }
             const int e = __shfl_sync(0xffffffffu, e_pref, u & 31);
-            if (lane == 0) s.key0[i & 7][hh] = t * kQTile + 64 - e;
+            if (lane == 0) s.key0[i % kRecRing][hh] = t * kQTile + 64 - e;
           }
           __syncwarp();
         }
@@ -300,7 +410,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int hh = 0; hh < 2; ++hh) {
               const int u = 2 * i + hh;
               if (u >= nslash) continue;
-              const int key0 = s.key0[i & 7][hh];
+              const int key0 = s.key0[i % kRecRing][hh];
               for (int hf = 0; hf < NH; ++hf)
                 tma_load_4d(s.slot[sl][hf] + hh * kKTile * 128, tm, &s.slot_full[sl], 64 * hf, hk, key0, b);
             }
@@ -322,60 +432,83 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
     }
-  } else if (warp == kFwdMaskWarp) {
-    // ------------------------------------------------------------ row masks
-    // Builds the 128 row masks of both units of each pair (bitmap reads for
-    // slash tiles, position compares for bar chunks, zero for the missing
-    // half of an odd last pair); runs as far ahead as the mask ring allows.
+  } else if (warp == kFwdRecWarp) {
+    // ------------------------------------------------------------ mask records
+    // Per pair: the bitmap words of its slash tiles (lanes 0-7 for the first
+    // unit, 8-15 for the second) and the key positions of its bar chunks are
+    // all requested before any is used, so a pair costs one memory round
+    // trip; runs as far ahead as the record ring allows.
     const uint64_t* offbits_p = av.offbits + int64_t(bh) * G.WG;
     const uint64_t* colbits_p = av.colbits + int64_t(bh) * G.WG;
     int e_win = -1, e_pref = 0;  // elist[32 e_win + lane]
     for (int i = 0; i < P; ++i) {
-      const int mi = i % kMaskRing;
-      if (i >= kMaskRing && !mbar_wait(&s.mask_empty[mi], ((i / kMaskRing) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+      const int ri = i % kRecRing;
+      if (i >= kRecRing && !mbar_wait(&s.rec_empty[ri], ((i / kRecRing) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+      int kind[2];
+      int64_t cc[2], m0[2], L0a[2], L0b[2];
+#pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int u = 2 * i + hh;
-        uint64_t* mrow = s.mask[mi][hh];
-        uint64_t m[kQTile / 32];
-        if (u >= U) {
-#pragma unroll
-          for (int rr = 0; rr < kQTile / 32; ++rr) m[rr] = 0ull;
-        } else if (u < nslash) {
+        kind[hh] = (u >= U) ? 0 : (u < nslash ? 1 : 2);
+        cc[hh] = 0;
+        if (kind[hh] == 1) {
           if ((u >> 5) != e_win) {
             e_win = u >> 5;
             const int j = 32 * e_win + lane;
             e_pref = j < nslash ? __ldg(elist + j) : 0;
           }
-          const int e = __shfl_sync(0xffffffffu, e_pref, u & 31);
-          slash_tile_masks(G, offbits_p, colbits_p, t, int64_t(t) * kQTile + 64 - e, p.Nq, lane, m);
-        } else {
-          // bar chunk: ascending keys (padding last), so a row's mask is the
-          // prefix of keys at or before the row
-          const int32_t* keys = vlist + (u - nslash) * kKTile;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = __ldg(keys + e * 32 + lane);
-            s.bar_keys[e * 32 + lane] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
-          }
-          __syncwarp();
-#pragma unroll
-          for (int rr = 0; rr < kQTile / 32; ++rr) {
-            const int64_t nl = int64_t(t) * kQTile + rr * 32 + lane;
-            const int64_t ng = qpos_g(G, nl);
-            int pos = 0;
-#pragma unroll
-            for (int step = 32; step > 0; step >>= 1)
-              if (s.bar_keys[pos + step - 1] <= ng) pos += step;
-            const int cnt = (s.bar_keys[kKTile - 1] <= ng) ? kKTile : pos;
-            m[rr] = nl < p.Nq ? (cnt == kKTile ? ~0ull : ((1ull << cnt) - 1)) : 0ull;
-          }
-          __syncwarp();
+          cc[hh] = int64_t(t) * kQTile + 64 - __shfl_sync(0xffffffffu, e_pref, u & 31);
         }
+        m0[hh] = (cc[hh] >= 0) ? kpos_g(G, cc[hh]) : cc[hh];  // c < 0 only without striping
+        L0a[hh] = qpos_g(G, int64_t(t) * kQTile) - m0[hh] - 63;
+        L0b[hh] = qpos_g(G, int64_t(t) * kQTile + 64) - m0[hh] - 63;
+      }
+      // issue every load of the pair
+      uint64_t wv = 0;
+      {
+        const int hh = lane >> 3, j = lane & 7;
+        const bool sec = hh == 1;  // lanes 8-15 serve the second unit
+        const int kh = sec ? kind[1] : kind[0];
+        if (hh < 2 && kh == 1) {
+          const int64_t la = sec ? L0a[1] : L0a[0], lb = sec ? L0b[1] : L0b[0], mm = sec ? m0[1] : m0[0];
+          const int64_t w = j < 6 ? (((j < 3 ? la : lb) >> 6) + j % 3) : ((mm >> 6) + (j - 6));
+          const uint64_t* bm = j < 6 ? offbits_p : colbits_p;
+          wv = (w >= 0 && w < G.WG) ? __ldg(bm + w) : 0ull;
+        }
+      }
+      int key[2][2];
 #pragma unroll
-        for (int rr = 0; rr < kQTile / 32; ++rr) mrow[rr * 32 + lane] = m[rr];
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          key[hh][e] = kind[hh] == 2 ? __ldg(vlist + (2 * i + hh - nslash) * kKTile + e * 32 + lane) : -1;
+      // publish
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        MaskRec& rc = s.rec[ri][hh];
+        if (kind[hh] == 1) {
+          const uint64_t c1 = __shfl_sync(0xffffffffu, wv, 8 * hh + 7);
+          if ((lane >> 3) == hh) {
+            const int j = lane & 7;
+            if (j < 6) rc.W[j] = wv;
+            if (j == 6) {
+              const int shc = int(m0[hh] & 63);
+              const uint64_t colw = shc ? ((wv >> shc) | (c1 << (64 - shc))) : wv;
+              rc.keep = ~colw & ((cc[hh] < 0) ? ((~0ull) << (-cc[hh])) : ~0ull);
+            }
+          }
+          if (lane == 0) {
+            rc.lo6[0] = int(L0a[hh] & 63);
+            rc.lo6[1] = int(L0b[hh] & 63);
+          }
+        } else if (kind[hh] == 2) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) rc.kg[e * 32 + lane] = key[hh][e] >= 0 ? kpos_g(G, key[hh][e]) : INT64_MAX;
+        }
+        if (lane == 0) rc.kind = kind[hh];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.mask_full[mi]);
+      if (lane == 0) mbar_arrive(&s.rec_full[ri]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -408,7 +541,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int nk = (2 * i + 1 < U) ? kPairKeys / 16 : kKTile / 16;
           for (int kk = 0; kk < nk; ++kk) {
             const uint64_t dv = sdesc_sw128(smem_u32(s.slot[sl][0]) + kk * 2048, kPairKeys * 128, 1024);
-            mma_ts(tmem + kColO + 128 * g, tmem + kColS + 128 * g + kk * 8, dv, idO, (i >= 2 || kk > 0));
+            const uint32_t a_p = tmem + kColS + 128 * g + (kk >> 2) * 64 + (kk & 3) * 8;  // P of unit kk / 4
+            mma_ts(tmem + kColO + 128 * g, a_p, dv, idO, (i >= 2 || kk > 0));
           }
         }
         mma_commit(&s.slot_empty[sl]);
@@ -428,59 +562,79 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t colO = kColO + 128 * grp, colS = kColS + 128 * grp;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    const int64_t n_g = qpos_g(G, n_loc);
     for (int i = grp; i < P; i += 2) {
-      const int mi = i % kMaskRing;
+      const int ri = i % kRecRing;
       ok = mbar_wait(&s.s_full[grp], (i >> 1) & 1, ab, VS_ERR_TIMEOUT) &&
-           mbar_wait(&s.mask_full[mi], (i / kMaskRing) & 1, ab, VS_ERR_TIMEOUT);
+           mbar_wait(&s.rec_full[ri], (i / kRecRing) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint64_t mask0 = s.mask[mi][0][r], mask1 = s.mask[mi][1][r];
-      mbar_arrive(&s.mask_empty[mi]);
-      // P against the row's reference maximum m_run (log2 units).  The
-      // reference is lazy: it only moves when a pair's masked sum shows an
-      // entry more than 2^64 above it (or for the row's first entries); the
-      // sum bounds every single entry, so P stays <= 2^64.  S of pair i
-      // completing means the group's PV of pair i - 2 has completed too, so
-      // O may be rescaled here.
-      uint32_t pk[64];
-      float pair_sum = 0.f;
-      auto make_p = [&](float ref) {
+      const MaskRec& rc0 = s.rec[ri][0];
+      const MaskRec& rc1 = s.rec[ri][1];
+      const uint64_t mask0 = row_ok ? rec_row_mask(rc0, rc0.kind, r, n_g) : 0ull;
+      const uint64_t mask1 = row_ok ? rec_row_mask(rc1, rc1.kind, r, n_g) : 0ull;
+      mbar_arrive(&s.rec_empty[ri]);
+      // P against the row's reference maximum m_run (log2 units), one unit at
+      // a time.  The reference is lazy: it only moves when a unit's masked sum
+      // shows an entry more than 2^64 above it (or for the row's first
+      // entries); the sum bounds every single entry, so P stays <= 2^64.  S
+      // of pair i completing means the group's PV of pair i - 2 has completed
+      // too, so O may be rescaled here.
+      uint32_t pk[32];
+      float unit_sum;
+      auto make_p = [&](int hh, uint64_t mask, float ref) {
         float ps[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) ps[k] = 0.f;
         const float nref = -ref;
+        uint32_t sr[64];
+        tmem_ld32(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tl + colS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_wait();
+        const uint32_t mlo = uint32_t(mask), mhi = uint32_t(mask >> 32);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint64_t mask = hh ? mask1 : mask0;
-          uint32_t sr[64];
-          tmem_ld32(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(tl + colS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            float p0 = ex2(fmaf(__uint_as_float(sr[2 * k]), p.scale_log2, nref));
-            float p1 = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), p.scale_log2, nref));
-            p0 = ((mask >> (2 * k)) & 1ull) ? p0 : 0.f;
-            p1 = ((mask >> (2 * k + 1)) & 1ull) ? p1 : 0.f;
-            ps[k & 7] += p0 + p1;
-            pk[32 * hh + k] = pack_bf16x2(p0, p1);
-          }
+        for (int k = 0; k < 32; ++k) {
+          // bit (2k, 2k + 1) of the mask moved to the sign and spread over the
+          // word: an AND keeps or clears the fp32 numerator
+          const uint32_t w = k < 16 ? mlo : mhi;
+          const uint32_t keep0 = uint32_t(int32_t(w << (31 - ((2 * k) & 31))) >> 31);
+          const uint32_t keep1 = uint32_t(int32_t(w << (31 - ((2 * k + 1) & 31))) >> 31);
+          const float p0 = __uint_as_float(
+              __float_as_uint(ex2(fmaf(__uint_as_float(sr[2 * k]), p.scale_log2, nref))) & keep0);
+          const float p1 = __uint_as_float(
+              __float_as_uint(ex2(fmaf(__uint_as_float(sr[2 * k + 1]), p.scale_log2, nref))) & keep1);
+          ps[k & 7] += p0 + p1;
+          pk[k] = pack_bf16x2(p0, p1);
         }
-        pair_sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        unit_sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       };
-      make_p(m_run == -INFINITY ? 0.f : m_run);
-      const bool need = ((mask0 | mask1) != 0ull) && (m_run == -INFINITY || !(pair_sum <= kRefSlack));
-      if (__any_sync(0xffffffffu, need)) {
-        const RowRef rr = fwd_rebase_pair<D>(tl, colS, colO, mask0, mask1, need, m_run, l_run, p.scale_log2);
+      auto store_p = [&](int hh) {
+        tmem_st16(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tl + colS + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      };
+      make_p(0, mask0, m_run == -INFINITY ? 0.f : m_run);
+      const bool need0 = (mask0 != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
+      if (__any_sync(0xffffffffu, need0)) {
+        const RowRef rr = fwd_rebase_pair<D>(tl, colS, colO, mask0, mask1, m_run, l_run, p.scale_log2);
         m_run = rr.m_run;
         l_run = rr.l_run;
       } else {
-        l_run += pair_sum;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_st16(tl + colS + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * k]));
+        store_p(0);
+        l_run += unit_sum;
+        // a row whose reference is still unset has no entry in the first unit
+        make_p(1, mask1, m_run == -INFINITY ? 0.f : m_run);
+        const bool need1 = (mask1 != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
+        if (__any_sync(0xffffffffu, need1)) {
+          const RowRef rr = fwd_rebase_second<D>(tl, colS, colO, mask1, m_run, l_run, p.scale_log2);
+          m_run = rr.m_run;
+          l_run = rr.l_run;
+        } else {
+          store_p(1);
+          l_run += unit_sum;
+        }
       }
       tmem_st_wait();
       tc_fence_before();
