@@ -8,13 +8,14 @@ Python binding of the same names.
     vs_attn_bwd           sparse attention backward (dQ, dK, dV)
     striped_permute       64-token block-level striping
     vs_check_status       device status word of a workspace or arena
+    vs_selftest_wait_timeout  failure-detection self-test (a bounded wait runs out)
 """
 from ._binding import (VSError, make_shape, make_stripe, striped_permute, trace_enable, trace_report, trace_reset,
                        vs_attn_bwd, vs_attn_fwd,
-                       vs_build_block_index, vs_check_status, vs_estimate, vs_index_counts, lib, launch_count,
-                       status_string)
+                       vs_build_block_index, vs_check_status, vs_estimate, vs_index_counts, vs_selftest_wait_timeout,
+                       lib, launch_count, status_string)
 from .pipeline import StripedWorker, VSAttention, flop_counts
 
 __all__ = ["VSError", "make_shape", "make_stripe", "striped_permute", "vs_attn_bwd", "vs_attn_fwd",
            "vs_build_block_index", "vs_check_status", "vs_estimate", "vs_index_counts", "lib", "launch_count",
-           "status_string", "VSAttention", "StripedWorker", "flop_counts"]
+           "status_string", "VSAttention", "StripedWorker", "flop_counts", "vs_selftest_wait_timeout"]

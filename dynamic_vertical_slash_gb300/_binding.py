@@ -75,11 +75,12 @@ def lib(build_if_missing: bool = True):
     L.striped_permute.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     L.vs_check_status.argtypes = [_P, _P]
+    L.vs_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, _P]
     L.vs_status_string.argtypes = [ctypes.c_int]
     L.vs_status_string.restype = ctypes.c_char_p
     L.vs_launch_count.restype = ctypes.c_int64
     for name in ("vs_estimate", "vs_build_block_index", "vs_index_counts", "vs_attn_fwd", "vs_attn_bwd",
-                 "striped_permute", "vs_check_status"):
+                 "striped_permute", "vs_check_status", "vs_selftest_wait_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -218,6 +219,12 @@ def striped_permute(x, world: int, stripe: int = 64, inverse: bool = False, only
     _check(lib().striped_permute(_ptr(x), _ptr(y), B, N, H, d, world, stripe, int(inverse), only_rank,
                                  _stream(stream)), "striped_permute")
     return y
+
+
+def vs_selftest_wait_timeout(ws, stream=None):
+    """Launches the failure-detection self-test kernel (a bounded wait that
+    runs out) on a uint8 workspace of at least 256 bytes."""
+    _check(lib().vs_selftest_wait_timeout(_ptr(ws), ws.numel(), _stream(stream)), "vs_selftest_wait_timeout")
 
 
 def vs_check_status(buf, stream=None) -> int:

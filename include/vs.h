@@ -225,6 +225,17 @@ vs_status striped_permute(const void* x, void* y, int B, int64_t N, int H, int d
  * resets it to VS_OK, and returns the code it held.  Synchronises `stream`. */
 vs_status vs_check_status(void* ws_or_arena, cudaStream_t stream);
 
+/* Failure-detection self-test (no counterpart in the pages: it checks the
+ * bounded waits every kernel above relies on).  Launches one CTA whose two
+ * warps wait on mbarriers that nothing arrives on.  The first wait runs out
+ * after the kernels' wait budget (about two seconds), records VS_ERR_TIMEOUT
+ * in the device status word at the start of `ws` (ws_bytes >= 256) and
+ * raises the CTA's abort flag, on which the other warp gives up; both warps
+ * then return, and each adds 1 to the int at byte offset 4 of `ws` (100 if a
+ * wait had completed).  Returns VS_OK once launched; vs_check_status(ws)
+ * then reports VS_ERR_TIMEOUT.  The CUDA context stays usable. */
+vs_status vs_selftest_wait_timeout(void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* vs_status_string(vs_status status);
 
