@@ -615,26 +615,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st16(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
         tmem_st16(tl + colS + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
       };
-      make_p(0, mask0, m_run == -INFINITY ? 0.f : m_run);
-      const bool need0 = (mask0 != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
-      if (__any_sync(0xffffffffu, need0)) {
-        const RowRef rr = fwd_rebase_pair<D>(tl, colS, colO, mask0, mask1, m_run, l_run, p.scale_log2);
-        m_run = rr.m_run;
-        l_run = rr.l_run;
-      } else {
-        store_p(0);
-        l_run += unit_sum;
-        // a row whose reference is still unset has no entry in the first unit
-        make_p(1, mask1, m_run == -INFINITY ? 0.f : m_run);
-        const bool need1 = (mask1 != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
-        if (__any_sync(0xffffffffu, need1)) {
-          const RowRef rr = fwd_rebase_second<D>(tl, colS, colO, mask1, m_run, l_run, p.scale_log2);
+      // one copy of the unit body (the hot loops of all warp roles share the
+      // SM's instruction cache): unit 0, then unit 1 unless unit 0 sent the
+      // pair to re-basing
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint64_t mask = hh ? mask1 : mask0;
+        make_p(hh, mask, m_run == -INFINITY ? 0.f : m_run);
+        // (a row whose reference is still unset at unit 1 has no entry in unit 0)
+        const bool need = (mask != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
+        if (__any_sync(0xffffffffu, need)) {
+          const RowRef rr = hh ? fwd_rebase_second<D>(tl, colS, colO, mask1, m_run, l_run, p.scale_log2)
+                               : fwd_rebase_pair<D>(tl, colS, colO, mask0, mask1, m_run, l_run, p.scale_log2);
           m_run = rr.m_run;
           l_run = rr.l_run;
-        } else {
-          store_p(1);
-          l_run += unit_sum;
+          break;
         }
+        store_p(hh);
+        l_run += unit_sum;
       }
       tmem_st_wait();
       tc_fence_before();
