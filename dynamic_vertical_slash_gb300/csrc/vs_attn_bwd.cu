@@ -148,49 +148,43 @@ struct DqSmem {
   uint64_t s_full[2], s_free[2], ds_full[2], ds_done[2];
   uint64_t fin, teardown;
   uint64_t mask[kBwdStages][kQTile];  // per-stage row masks, written by the producer
+  int64_t bar_keys[kKTile];           // producer: a bar chunk's key positions
   uint32_t tmem_base;
   int abort_flag;
 };
 
 // Row masks of one query-major unit (128 rows), written by the producer warp:
-// slash tiles from the offset / column bitmaps, bar chunks from the gathered
-// columns' positions.  Shared by the forward and dQ kernels' layouts.
-__device__ __forceinline__ void unit_row_masks(uint64_t* out, const Geo& G, const ArenaView& av, int64_t bh,
-                                               int t, int Nq, bool slash, int64_t c, const int32_t* keys, int lane) {
+// slash tiles cut from the offset / column bitmaps (one memory round trip per
+// unit), bar chunks as the prefix of the chunk's ascending keys at or before
+// each row (binary search over the keys' positions in `scratch`).
+__device__ __forceinline__ void unit_row_masks(uint64_t* out, int64_t* scratch, const Geo& G, const ArenaView& av,
+                                               int64_t bh, int t, int Nq, bool slash, int64_t c,
+                                               const int32_t* keys, int lane) {
+  uint64_t m[kQTile / 32];
   if (slash) {
-    const uint64_t* offbits = av.offbits + bh * G.WG;
-    const uint64_t* colbits = av.colbits + bh * G.WG;
-#pragma unroll
-    for (int rr = 0; rr < kQTile / 32; ++rr) {
-      const int row = rr * 32 + lane;
-      const int64_t nl = int64_t(t) * kQTile + row;
-      out[row] = nl < Nq ? slash_row_mask(G, offbits, colbits, qpos_g(G, nl), c) : 0ull;
-    }
+    slash_tile_masks(G, av.offbits + bh * G.WG, av.colbits + bh * G.WG, t, c, Nq, lane, m);
   } else {
-    int64_t kg[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int key = __ldg(keys + e * 32 + lane);
-      kg[e] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
+      scratch[e * 32 + lane] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
     }
+    __syncwarp();
 #pragma unroll
     for (int rr = 0; rr < kQTile / 32; ++rr) {
-      const int row = rr * 32 + lane;
-      const int64_t nl = int64_t(t) * kQTile + row;
+      const int64_t nl = int64_t(t) * kQTile + rr * 32 + lane;
       const int64_t ng = qpos_g(G, nl);
-      uint64_t m = 0;
+      int pos = 0;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int64_t kge = kg[e];
-#pragma unroll 8
-        for (int kk = 0; kk < 32; ++kk) {
-          const int64_t mg = __shfl_sync(0xffffffffu, kge, kk);
-          m |= uint64_t(mg <= ng) << (32 * e + kk);
-        }
-      }
-      out[row] = nl < Nq ? m : 0ull;
+      for (int step = 32; step > 0; step >>= 1)
+        if (scratch[pos + step - 1] <= ng) pos += step;
+      const int cnt = (scratch[kKTile - 1] <= ng) ? kKTile : pos;
+      m[rr] = nl < Nq ? (cnt == kKTile ? ~0ull : ((1ull << cnt) - 1)) : 0ull;
     }
+    __syncwarp();
   }
+#pragma unroll
+  for (int rr = 0; rr < kQTile / 32; ++rr) out[rr * 32 + lane] = m[rr];
 }
 
 template <int D>
@@ -271,7 +265,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = j % kBwdStages;
         if (j >= kBwdStages && !mbar_wait(&s.kv_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
         // row masks computed ahead of the compute warps (hides the bitmap reads)
-        unit_row_masks(s.mask[st], G, av, bh, t, p.Nq, j < nslash,
+        unit_row_masks(s.mask[st], s.bar_keys, G, av, bh, t, p.Nq, j < nslash,
                        j < nslash ? int64_t(t) * kQTile + 64 - __ldg(elist + j) : 0,
                        vlist + (j < nslash ? 0 : (j - nslash) * kKTile), lane);
         __syncwarp();
@@ -482,6 +476,7 @@ struct KvSmem {
   alignas(16) float dd[kBwdStages][kRowTile];
   int32_t unit_head[kBwdStages];
   int32_t unit_row[kBwdStages];
+  int32_t head_units[kMaxGroup];  // slash: units of each head of the group
   uint64_t kv_full;
   uint64_t st_full[kBwdStages], st_empty[kBwdStages];
   uint64_t s_full, s_free, p_full[2], mm_done[2];
@@ -500,28 +495,8 @@ struct KvSmem {
 struct KvWork {
   int n_units;
   int heads;         // slash: number of heads in the group
-  int cnt[kMaxGroup]; // slash: units per head
   int64_t row0;      // bar: first row of the split
 };
-
-template <bool BAR>
-__device__ __forceinline__ void kv_unit(const KvWork& w, const ArenaView& av, const Geo& G, int b, int hk, int h_bar,
-                                        int64_t k0, int j, int* head_out, int64_t* row_out) {
-  if (BAR) {
-    *head_out = h_bar;
-    *row_out = w.row0 + int64_t(j) * kRowTile;
-    return;
-  }
-  int hh = 0;
-  while (hh < w.heads - 1 && j >= w.cnt[hh]) {
-    j -= w.cnt[hh];
-    ++hh;
-  }
-  const int h = hk * G.g + hh;
-  const int bh = b * G.Hq + h;
-  *head_out = h;
-  *row_out = k0 + __ldg(av.flist + int64_t(bh) * G.EMAX + j);
-}
 
 template <int D, bool BAR>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -557,7 +532,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int hh = 0; hh < G.g; ++hh) {
         const int bh = b * p.Hq + hk * G.g + hh;
         const int c = count_le(av.flist + int64_t(bh) * G.EMAX, __ldg(av.fcount + bh), int64_t(p.Nq) - 1 - k0);
-        w.cnt[hh] = c;
+        if (threadIdx.x == 0) s.head_units[hh] = c;
         w.n_units += c;
       }
     }
@@ -642,12 +617,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       kv_issued = true;
       const float* l2g = reinterpret_cast<const float*>(p.ws + L.off_l2);
       const float* ddg = reinterpret_cast<const float*>(p.ws + L.off_d);
+      int cur_h = 0, cur_j = 0;  // slash: head of the group and its entry for unit j
       for (int j = 0; j < U; ++j) {
         const int st = j % kBwdStages;
         if (j >= kBwdStages && !mbar_wait(&s.st_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
         int h;
         int64_t r0;
-        kv_unit<BAR>(w, av, G, b, hk, h_bar, k0, j, &h, &r0);
+        if (BAR) {
+          h = h_bar;
+          r0 = w.row0 + int64_t(j) * kRowTile;
+        } else {
+          while (cur_h < w.heads - 1 && cur_j >= s.head_units[cur_h]) {
+            cur_j = 0;
+            ++cur_h;
+          }
+          h = hk * G.g + cur_h;
+          r0 = k0 + __ldg(av.flist + (int64_t(b) * G.Hq + h) * G.EMAX + cur_j);
+          ++cur_j;
+        }
         const int64_t bh = int64_t(b) * p.Hq + h;
         for (int i = lane; i < kRowTile; i += 32) {
           const int64_t n = r0 + i;
