@@ -40,6 +40,23 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def _traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture of this
+    workload, or None when there is none or the kernel sources have changed
+    since it was taken (the capture records the sources' digest)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_%s.json" % workload)
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        from dynamic_vertical_slash_gb300 import _build
+
+        if d.get("csrc_digest") != _build._digest():
+            return None
+        return float(d["bytes_per_launch"][kernel])
+    except Exception:
+        return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -251,7 +268,8 @@ def ours(args, w, x, rank, world):
     if dom:
         achieved = issued_per_step[dom] / (att[dom]["ms_avg"] * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"], "traffic": None,
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
+                    "traffic": _traffic(w.name, dom), "traffic_unit": "bytes per launch (ncu dram read + write)",
                     "peak_kind": "sustained bf16 (%s): the kernel is timed inside a long step" % peaks["source"]}
         for kname in att:
             att[kname]["issued_tflops"] = issued_per_step[kname] / (att[kname]["ms_avg"] * 1e-3) / 1e12
