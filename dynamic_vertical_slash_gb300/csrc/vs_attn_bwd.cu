@@ -134,16 +134,18 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
 }
 
 // ---------------------------------------------------------------- dQ kernel
-constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColDS = 384;
+// TMEM: dQ [0, 128), S and dP double-buffered [128, 256) / [256, 384), dS
+// (bf16, double-buffered) [384, 448), dO (bf16, the A operand of dP, loaded
+// once per tile) [448, 512).
+constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColDS = 384, kDqColDO = 448;
 
 template <int D>
 struct DqSmem {
   static constexpr int NH = D / 64;
   uint8_t q[NH][kQTile * 128];
-  uint8_t g[NH][kQTile * 128];  // dO
   uint8_t k[kBwdStages][NH][kKTile * 128];
   uint8_t v[kBwdStages][NH][kKTile * 128];
-  uint64_t q_full;
+  uint64_t q_full, do_full;
   uint64_t kv_full[kBwdStages], kv_empty[kBwdStages];
   uint64_t s_full[2], s_free[2], ds_full[2], ds_done[2];
   uint64_t fin, teardown;
@@ -189,9 +191,8 @@ __device__ __forceinline__ void unit_row_masks(uint64_t* out, int64_t* scratch, 
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
-                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const BwdParams p) {
+    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(&s.q_full, 1);
+    mbar_init(&s.do_full, kBwdCompute);
     for (int i = 0; i < kBwdStages; ++i) {
       mbar_init(&s.kv_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
@@ -253,11 +255,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < kBwdStages; ++i) issued[i] = -1;
     if (U > 0) {
       if (lane == 0) {
-        mbar_arrive_expect_tx(&s.q_full, 2 * NH * kQTile * 128);
-        for (int hf = 0; hf < NH; ++hf) {
-          tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
-          tma_load_4d(s.g[hf], &tmG, &s.q_full, 64 * hf, h, t * kQTile, b);
-        }
+        mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
+        for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
       }
       const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
       const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && U > 0) {
       const uint32_t idS = idesc_bf16(128, 64, 0, 0);
       const uint32_t idQ = idesc_bf16(128, D, 0, 1);
-      bool ok = mbar_wait(&s.q_full, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait(&s.q_full, 0, ab, VS_ERR_TIMEOUT) && mbar_wait(&s.do_full, 0, ab, VS_ERR_TIMEOUT);
       for (int j = 0; ok && j <= U; ++j) {
         if (j < U) {
           const int st = j % kBwdStages;
@@ -313,11 +312,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[kk / 4]) + (kk % 4) * 32, 16, 1024);
-            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
             mma_ss(tmem + kDqColS + (j & 1) * 64, dq_, dk_, idS, kk > 0);
-            mma_ss(tmem + kDqColDP + (j & 1) * 64, dg_, dv_, idS, kk > 0);
+            mma_ts(tmem + kDqColDP + (j & 1) * 64, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
           }
           mma_issued = true;
           mma_commit(&s.s_full[j & 1]);
@@ -349,6 +347,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdLayout L = bwd_layout_dev(av.hdr, D);
       Lr = reinterpret_cast<const float*>(p.ws + L.off_l2)[int64_t(bh) * p.Nq + n_loc];
       Dr = reinterpret_cast<const float*>(p.ws + L.off_d)[int64_t(bh) * p.Nq + n_loc];
+    }
+    {
+      // dO row r, d columns [half D/2, (half + 1) D/2), into TMEM as bf16 pairs
+      uint32_t w[D / 4];
+      const uint8_t* src = p.dO + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(h) * p.so[2]) * 2 + half * D;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const uint4 x = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
+        w[4 * c] = x.x;
+        w[4 * c + 1] = x.y;
+        w[4 * c + 2] = x.z;
+        w[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_st16(tl + kDqColDO + half * (D / 4) + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.do_full);
     }
     bool ok = true;
     for (int j = 0; j < U; ++j) {
@@ -996,8 +1013,7 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   trace_begin("bwd_dq", st);
-  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tq128, tg128, tk64,
-                                                                                          tv64, p);
+  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tq128, tk64, tv64, p);
   trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
