@@ -480,13 +480,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ------------------------------------------------------ key-major dK / dV
 // TMEM: dK [0, 128), dV [128, 256), S^T [256, 320), dP^T [320, 384),
 //       P^T x2 [384, 448), dS^T x2 [448, 512)
-constexpr uint32_t kKvColDK = 0, kKvColDV = 128, kKvColS = 256, kKvColDP = 320, kKvColP = 384, kKvColDS = 448;
+// TMEM: dK [0, 128), dV [128, 256), S^T [256, 320), dP^T [320, 384), P^T (bf16)
+// [384, 416), dS^T (bf16) [416, 448), K (bf16, the A operand of S^T = K Q^T,
+// loaded once per tile) [448, 512).
+constexpr uint32_t kKvColDK = 0, kKvColDV = 128, kKvColS = 256, kKvColDP = 320, kKvColP = 384, kKvColDS = 416,
+                   kKvColK = 448;
 
 template <int D>
 struct KvSmem {
   static constexpr int NH = D / 64;
-  uint8_t k[NH][kBarK * 128];  // A operands: 128 keys
-  uint8_t v[NH][kBarK * 128];
+  uint8_t v[NH][kBarK * 128];  // A operand of dP^T = V dO^T: 128 keys
   uint8_t q[kBwdStages][NH][kRowTile * 128];  // B operands: 64 rows
   uint8_t g[kBwdStages][NH][kRowTile * 128];
   alignas(16) float l2[kBwdStages][kRowTile];
@@ -494,9 +497,9 @@ struct KvSmem {
   int32_t unit_head[kBwdStages];
   int32_t unit_row[kBwdStages];
   int32_t head_units[kMaxGroup];  // slash: units of each head of the group
-  uint64_t kv_full;
+  uint64_t kv_full, k_tmem;
   uint64_t st_full[kBwdStages], st_empty[kBwdStages];
-  uint64_t s_full, s_free, p_full[2], mm_done[2];
+  uint64_t s_full, s_free, p_full, mm_done;
   uint64_t fin, teardown;
   uint32_t tmem_base;
   int abort_flag;
@@ -582,16 +585,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(&s.kv_full, 1);
+    mbar_init(&s.k_tmem, kBwdCompute);
     for (int i = 0; i < kBwdStages; ++i) {
       mbar_init(&s.st_full[i], 1);
       mbar_init(&s.st_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
     mbar_init(&s.s_free, kBwdCompute);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.p_full[i], kBwdCompute);
-      mbar_init(&s.mm_done[i], 1);
-    }
+    mbar_init(&s.p_full, kBwdCompute);
+    mbar_init(&s.mm_done, 1);
     mbar_init(&s.fin, 1);
     mbar_init(&s.teardown, 1);
     fence_mbar_init();
@@ -616,16 +618,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (run) {
       if (!BAR) {
         if (lane == 0) {
-          mbar_arrive_expect_tx(&s.kv_full, 2 * NH * kBarK * 128);
-          for (int hf = 0; hf < NH; ++hf) {
-            tma_load_4d(s.k[hf], &tmK, &s.kv_full, 64 * hf, hk, int(k0), b);
-            tma_load_4d(s.v[hf], &tmV, &s.kv_full, 64 * hf, hk, int(k0), b);
-          }
+          mbar_arrive_expect_tx(&s.kv_full, NH * kBarK * 128);
+          for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.v[hf], &tmV, &s.kv_full, 64 * hf, hk, int(k0), b);
         }
       } else {
-        const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
         const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
-        gather_rows<D>(smem_u32(s.k[0]), kBarK, kb, p.sk[1], bar_keys, kBarK, lane);
         gather_rows<D>(smem_u32(s.v[0]), kBarK, vb, p.sv[1], bar_keys, kBarK, lane);
         asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.kv_full)) : "memory");
         __syncwarp();
@@ -692,7 +689,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && run) {
       const uint32_t idS = idesc_bf16(128, kRowTile, 0, 0);
       const uint32_t idG = idesc_bf16(128, D, 0, 1);
-      bool ok = mbar_wait(&s.kv_full, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait(&s.kv_full, 0, ab, VS_ERR_TIMEOUT) && mbar_wait(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT);
       if (ok && BAR) fence_proxy_async_smem();
       for (int j = 0; ok && j <= U; ++j) {
         if (j < U) {
@@ -702,11 +699,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t da = sdesc_sw128(smem_u32(s.k[kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ss(tmem + kKvColS, da, dq_, idS, kk > 0);
+            mma_ts(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
             mma_ss(tmem + kKvColDP, dva, dg_, idS, kk > 0);
           }
           mma_issued = true;
@@ -714,16 +710,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         if (j >= 1) {
           const int jj = j - 1, st = jj % kBwdStages;
-          if (!(ok = mbar_wait(&s.p_full[jj & 1], (jj >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+          if (!(ok = mbar_wait(&s.p_full, jj & 1, ab, VS_ERR_TIMEOUT))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kRowTile / 16; ++kk) {
             const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][0]) + kk * 2048, kRowTile * 128, 1024);
             const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][0]) + kk * 2048, kRowTile * 128, 1024);
-            mma_ts(tmem + kKvColDV, tmem + kKvColP + (jj & 1) * 32 + kk * 8, dg_, idG, (jj > 0 || kk > 0));
-            mma_ts(tmem + kKvColDK, tmem + kKvColDS + (jj & 1) * 32 + kk * 8, dq_, idG, (jj > 0 || kk > 0));
+            mma_ts(tmem + kKvColDV, tmem + kKvColP + kk * 8, dg_, idG, (jj > 0 || kk > 0));
+            mma_ts(tmem + kKvColDK, tmem + kKvColDS + kk * 8, dq_, idG, (jj > 0 || kk > 0));
           }
-          mma_commit(&s.mm_done[jj & 1]);
+          mma_commit(&s.mm_done);
           mma_commit(&s.st_empty[st]);
         }
       }
@@ -740,6 +736,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     else kl = k0 + r;
     const bool key_ok = run && kl >= 0 && kl < p.Nk;
     const int64_t m_g = key_ok ? kpos_g(G, kl) : 0;
+    if (run) {
+      // K row of key r, d columns [half D/2, (half + 1) D/2), into TMEM
+      uint32_t w[D / 4];
+      const uint8_t* src = p.k + (int64_t(b) * p.sk[0] + kl * p.sk[1] + int64_t(hk) * p.sk[2]) * 2 + half * D;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const uint4 x = key_ok ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
+        w[4 * c] = x.x;
+        w[4 * c + 1] = x.y;
+        w[4 * c + 2] = x.z;
+        w[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_st16(tl + kKvColK + half * (D / 4) + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.k_tmem);
+    }
     bool ok = true;
     for (int j = 0; run && j < U; ++j) {
       const int st = j % kBwdStages;
@@ -805,17 +820,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pk[i] = pack_bf16x2(pv[0], pv[1]);
         dk[i] = pack_bf16x2(ds[0], ds[1]);
       }
-      if (j >= 2) ok = mbar_wait(&s.mm_done[j & 1], ((j - 2) >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      if (j >= 1) ok = mbar_wait(&s.mm_done, (j - 1) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      tmem_st16(tl + kKvColP + (j & 1) * 32 + 16 * half, pk);
-      tmem_st16(tl + kKvColDS + (j & 1) * 32 + 16 * half, dk);
+      tmem_st16(tl + kKvColP + 16 * half, pk);
+      tmem_st16(tl + kKvColDS + 16 * half, dk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&s.p_full[j & 1]);
+      mbar_arrive(&s.p_full);
     }
     if (ok && run) ok = mbar_wait(&s.fin, 0, ab, VS_ERR_TIMEOUT);
     ok = __all_sync(0xffffffffu, ok);
