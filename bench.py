@@ -388,7 +388,7 @@ def striped(args, w, x, rank, world):
     do0 = vs.striped_permute(to_dev(x["dout"]), W, w.stripe, only_rank=0)
     ksh, vsh = vs.striped_permute(k, W, w.stripe), vs.striped_permute(v, W, w.stripe)
     wk = vs.StripedWorker(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, W, rank=0, stripe=w.stripe, device=dev,
-                          last_q=w.last_q, scale=w.scale)
+                          last_q=w.last_q, scale=w.scale, inner=args.inner)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
@@ -453,7 +453,9 @@ def striped(args, w, x, rank, world):
     tm = np.array([r["ms_fwd"] + r["ms_bwd"] for r in ring])
     dense_f = dense_causal_flops(w.B, w.N, w.Hq, w.d)
     cfg = _config(w)
-    cfg.update({"world": W, "stripe": w.stripe, "worker": 0, "ring": "src = -s mod world, KV shards local"})
+    cfg.update({"world": W, "stripe": w.stripe, "worker": 0,
+                "ring": ("hierarchical: nodes of %d cards, inner rings inside an outer ring" % args.inner
+                         if args.inner else "flat: src = -s mod world") + "; KV shards local"})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg, "roofline": roofline,
@@ -466,7 +468,49 @@ def striped(args, w, x, rank, world):
             "imbalance": {"flops_max_over_mean": float(fl.max() / fl.mean()),
                           "ms_max_over_mean": float(tm.max() / tm.mean())},
             "kernels": per_kernel, "step_ms_all": step_ms}
+    if args.all_workers:
+        line["workers"] = _all_workers(args, w, q, k, v, to_dev(x["dout"]), dev)
     return line, clk.summary()
+
+
+def _all_workers(args, w, q, k, v, do, dev):
+    """Every worker's ring on this GPU, one after the other: per worker and
+    ring step the executed FLOPs (from its index) and device time (one timed
+    step after one warm-up), and the imbalance across workers of their total
+    time and FLOPs."""
+    import torch
+
+    import dynamic_vertical_slash_gb300 as vs
+    from dynamic_vertical_slash_gb300.pipeline import flop_counts
+
+    W = w.world
+    ksh, vsh = vs.striped_permute(k, W, w.stripe), vs.striped_permute(v, W, w.stripe)
+    out = []
+    for r in range(W):
+        q_r = vs.striped_permute(q, W, w.stripe, only_rank=r)
+        do_r = vs.striped_permute(do, W, w.stripe, only_rank=r)
+        wk = vs.StripedWorker(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, W, rank=r, stripe=w.stripe, device=dev,
+                              last_q=w.last_q, scale=w.scale, inner=args.inner)
+        wk.select(q, k)
+        wk.build_index(q_r, ksh)
+        for _ in range(2):
+            wk.forward(q_r, ksh, vsh)
+            wk.backward(do_r)
+        torch.cuda.synchronize()
+        wk.check()
+        fl = [flop_counts(c, w.d) for c in wk.counts()]
+        ms = wk.step_times()
+        out.append({"worker": r, "src": [wk.source(s) for s in range(W)],
+                    "executed_flops": [f["fwd_executed"] + f["bwd_executed"] for f in fl],
+                    "ms": [a + b for a, b in ms]})
+        del wk, q_r, do_r
+    tot_ms = np.array([sum(o["ms"]) for o in out])
+    tot_fl = np.array([sum(o["executed_flops"]) for o in out])
+    step_ms = np.array([o["ms"] for o in out])
+    return {"per_worker": out,
+            "imbalance_ms_max_over_mean": float(tot_ms.max() / tot_ms.mean()),
+            "imbalance_flops_max_over_mean": float(tot_fl.max() / tot_fl.mean()),
+            "step_imbalance_ms_max_over_mean": float(step_ms.max() / step_ms.mean())}
 
 
 def main():
@@ -480,6 +524,10 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--inner", type=int, default=0,
+                    help="striped workloads: cards per node for the hierarchical ring order (0 = flat ring)")
+    ap.add_argument("--all-workers", action="store_true",
+                    help="striped workloads: also run every worker's ring and report the imbalance across workers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

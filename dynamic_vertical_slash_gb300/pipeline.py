@@ -128,12 +128,25 @@ class StripedWorker:
     timed with CUDA events so per-step load and its imbalance can be read
     off.  Buffers are preallocated; the selection is made once, on the
     global sequence, by ``select``.
+
+    ``inner`` > 0 selects the hierarchical order of Hierarchical Balanced
+    Sparse Ring Attention (section 4.2 (i)-(ii), Algorithm 2): workers are
+    grouped in nodes of ``inner`` cards (worker r = node n * inner + card c);
+    at outer step i the node holds the KV buffer of node n - i, and its inner
+    ring passes slices among the node's cards, so inner step j of outer step
+    i attends to the shard of worker ((n - i) mod nodes) * inner +
+    ((c - j) mod inner).  Only the order of the steps changes; the merged
+    result is the same up to the summation order.
     """
 
     def __init__(self, B: int, N_global: int, Hq: int, Hkv: int, d: int, kv: int, ks: int, world: int,
-                 rank: int = 0, stripe: int = 64, device="cuda", last_q: int = 64, scale: Optional[float] = None):
+                 rank: int = 0, stripe: int = 64, device="cuda", last_q: int = 64, scale: Optional[float] = None,
+                 inner: int = 0):
         if N_global % (world * stripe):
             raise ValueError("N_global must be a multiple of world * stripe")
+        if inner and world % inner:
+            raise ValueError("world must be a multiple of the node size")
+        self.inner = inner
         self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N_global, Hq, Hkv, d, kv, ks
         self.world, self.rank, self.stripe, self.last_q = world, rank, stripe, last_q
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -172,7 +185,12 @@ class StripedWorker:
 
     def source(self, s: int) -> int:
         """The KV shard worker ``rank`` attends to at ring step s."""
-        return (self.rank - s) % self.world
+        if not self.inner:
+            return (self.rank - s) % self.world
+        nodes = self.world // self.inner
+        n, c = divmod(self.rank, self.inner)
+        i, j = divmod(s, self.inner)
+        return ((n - i) % nodes) * self.inner + (c - j) % self.inner
 
     def select(self, q_global, k_global, stream=None):
         """Vertical / slash selection on the global sequence (Algorithm 1's
