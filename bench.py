@@ -314,46 +314,7 @@ def ours(args, w, x, rank, world):
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        hq, hk, hv, hdo = (pin(t) for t in (q, k, v, do))
-        for h, t in ((hq, q), (hk, k), (hv, v), (hdo, do)):
-            h.copy_(t)
-        ho, hdq, hdk, hdv = pin(q), pin(q), pin(k), pin(v)
-        dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(t) for t in (q, k, v, do))
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-        d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
-
-        def e2e_step():
-            dq_in.copy_(hq, non_blocking=True)
-            dk_in.copy_(hk, non_blocking=True)
-            dv_in.copy_(hv, non_blocking=True)
-            ddo_in.copy_(hdo, non_blocking=True)
-            o, _ = attn.forward(dq_in, dk_in, dv_in)
-            gq, gk, gv = attn.backward(ddo_in)
-            ho.copy_(o, non_blocking=True)
-            hdq.copy_(gq, non_blocking=True)
-            hdk.copy_(gk, non_blocking=True)
-            hdv.copy_(gv, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.steps):
-            e2e_step()
-        b.record()
-        torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b) / args.steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        attn.check()
-        e2e = {"value": world * executed / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "VSAttention.forward/backward (C ABI) with pinned host inputs and outputs"}
+        e2e = _e2e(args, w, attn, q, k, v, do, dev, world, executed)
 
     dense_f = dense_causal_flops(w.B, w.N, w.Hq, w.d)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -367,6 +328,115 @@ def ours(args, w, x, rank, world):
             "kernels": per_kernel, "attention_ms_per_step": attn_ms, "step_ms_all": step_ms}
     line.update(extra)
     return line, clk.summary()
+
+
+def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
+    """The same metric through the public API (VSAttention), with every
+    step's inputs copied in from pinned host memory and its results (O, dQ,
+    dK, dV) copied back, all inside the timed region.
+
+    Two schedules: `serial` (copy in, compute, copy out, one after the other
+    on one stream) and `pipelined` (the line's value): two VSAttention
+    instances and two input buffer sets alternate between steps, step i's
+    host->device copy runs on its own stream while step i-1 computes, and its
+    results go back on a third stream while step i+1 computes -- the usual
+    prefetching of the next batch.  Device time from CUDA events spanning
+    the first copy to the last one."""
+    import torch
+
+    import dynamic_vertical_slash_gb300 as vs
+
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    hin = [pin(t) for t in (q, k, v, do)]
+    for hbuf, t in zip(hin, (q, k, v, do)):
+        hbuf.copy_(t)
+    hout = [pin(t) for t in (q, q, k, v)]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def reduce_max(ms):
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    # ---- serial
+    din0 = [torch.empty_like(t) for t in (q, k, v, do)]
+
+    def serial_step():
+        for dst, src in zip(din0, hin):
+            dst.copy_(src, non_blocking=True)
+        o, _ = attn.forward(din0[0], din0[1], din0[2])
+        gq, gk, gv = attn.backward(din0[3])
+        for dst, src in zip(hout, (o, gq, gk, gv)):
+            dst.copy_(src, non_blocking=True)
+
+    serial_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        serial_step()
+    b.record()
+    torch.cuda.synchronize()
+    serial_ms = reduce_max(a.elapsed_time(b) / args.steps)
+    attn.check()
+
+    # ---- pipelined
+    att = [attn, vs.VSAttention(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, device=dev, last_q=w.last_q, scale=w.scale)]
+    din = [din0, [torch.empty_like(t) for t in (q, k, v, do)]]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(n):
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(s_in)
+        comp_done, out_done = [None, None], [None, None]
+        for i in range(n):
+            sl = i % 2
+            with torch.cuda.stream(s_in):
+                if comp_done[sl] is not None:  # step i - 2 has finished reading this input set
+                    s_in.wait_event(comp_done[sl])
+                for dst, src in zip(din[sl], hin):
+                    dst.copy_(src, non_blocking=True)
+                in_done = torch.cuda.Event()
+                in_done.record(s_in)
+            s_comp.wait_event(in_done)
+            if out_done[sl] is not None:  # step i - 2's results have left this instance's buffers
+                s_comp.wait_event(out_done[sl])
+            o, _ = att[sl].forward(din[sl][0], din[sl][1], din[sl][2], stream=s_comp)
+            gq, gk, gv = att[sl].backward(din[sl][3], stream=s_comp)
+            cd = torch.cuda.Event()
+            cd.record(s_comp)
+            comp_done[sl] = cd
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(cd)
+                for dst, src in zip(hout, (o, gq, gk, gv)):
+                    dst.copy_(src, non_blocking=True)
+                od = torch.cuda.Event()
+                od.record(s_out)
+                out_done[sl] = od
+        end = torch.cuda.Event(enable_timing=True)
+        end.record(s_out)
+        return start, end
+
+    run(2)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    start, end = run(args.steps)
+    torch.cuda.synchronize()
+    pipe_ms = reduce_max(start.elapsed_time(end) / args.steps)
+    for a_ in att:
+        a_.check()
+    return {"value": world * executed / (pipe_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": pipe_ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "serial": {"value": world * executed / (serial_ms * 1e-3) / 1e12, "ms_per_step": serial_ms},
+            "path": "VSAttention.forward/backward (C ABI) with pinned host inputs and outputs; pipelined: next "
+                    "step's inputs copied in and previous step's results copied out on separate streams while a "
+                    "step computes (two instances, two input sets)"}
 
 
 def striped(args, w, x, rank, world):
