@@ -1,32 +1,44 @@
-// Online Vertical-Slash estimation (Algorithm 1, first four lines).
+// Online Vertical-Slash estimation (Algorithm 1, first four lines), with the
+// last-64-row logits on the tensor cores.
 //
-//   pass 1  est_rowstats : per (b, h, key split) partial (max, sum exp) of the
-//                          last 64 query rows' causal logits
-//   pass 2  est_scores   : per (b, h, 64-key tile) A_hat = exp(S - LSE):
-//                          column sums -> v[m] (complete per tile), diagonal
-//                          sums -> 127 partial slash sums per tile
+// The g query heads of a KV head share its keys, so their last-64 query rows
+// are stacked two heads per 128-row tile (M = 128) and multiplied by
+// 128-key tiles of K (N = 128, K = d) with tcgen05.mma into TMEM:
+//   pass 1  est_rowstats : per (b, KV head, row tile, key split) partial
+//                          (max, sum exp) of every row's causal logits
+//   est_lse              : LSE of every row from its key-split partials
+//   pass 2  est_scores   : per (b, KV head, 128-key tile) A_hat = exp(S - LSE)
+//                          staged in shared memory: column sums -> v[m]
+//                          (complete per tile), diagonal sums -> 191 partial
+//                          slash sums per head and tile
 //   pass 3  est_scombine : s[o] = the (at most two) tile partials of o, added
 //                          in a fixed order (deterministic, no float atomics)
 //   pass 4  est_topk     : radix select of the k-th largest score, then an
 //                          index-ordered compaction; ties go to the lower index
+// Warp roles in passes 1 and 2: warp 0 issues TMA loads, warp 1 the MMAs
+// (one lane), warps 2-9 read the scores (one thread per TMEM lane, two warps
+// per lane quarter, each on half the columns).  Waits are bounded.
 #include "vs_internal.h"
+#include "vs_kernel_common.cuh"
 
 namespace vs {
 namespace {
 
-constexpr int kEstThreads = 256;
 constexpr int kLastQ = 64;
-constexpr int kChunk = 32;     // keys per chunk in pass 1
-constexpr int kSplits = 64;    // key splits per head in pass 1
+constexpr int kSplits = 64;        // key splits per row tile in pass 1
+constexpr int kEstKeys = 128;      // keys per tile (MMA N)
+constexpr int kEstThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 compute
+constexpr int kEstCompute = 256;
+constexpr int kEstDiag = 192;      // 191 diagonals (row - key in [-127, 63]) per head and key tile, padded
 constexpr int kTopkThreads = 1024;
 
 struct EstLayout {
-  int64_t off_part, off_vbuf, off_spart, off_sbuf, total;
+  int64_t off_part, off_lse, off_vbuf, off_spart, off_sbuf, total;
 };
 
 EstLayout est_layout(const vs_shape* s) {
   EstLayout L;
-  const int64_t BH = int64_t(s->B) * s->Hq, N = s->Nk, NT = N / 64;
+  const int64_t BH = int64_t(s->B) * s->Hq, N = s->Nk, NT = (N + kEstKeys - 1) / kEstKeys;
   int64_t off = 256;
   auto take = [&](int64_t bytes) {
     const int64_t at = off;
@@ -34,188 +46,349 @@ EstLayout est_layout(const vs_shape* s) {
     return at;
   };
   L.off_part = take(BH * kSplits * kLastQ * 8);
+  L.off_lse = take(BH * kLastQ * 4);
   L.off_vbuf = take(BH * N * 4);
-  L.off_spart = take(BH * NT * 128 * 4);
+  L.off_spart = take(BH * NT * kEstDiag * 4);
   L.off_sbuf = take(BH * N * 4);
   L.total = off;
   return L;
 }
 
-// Loads `rows` rows of d bf16 values (token stride s_tok elements) into a
-// float tile with row pitch `pitch`.
-__device__ __forceinline__ void load_rows_f32(float* dst, int pitch, const uint16_t* src, int64_t s_tok, int rows,
-                                              int d, int row0, int row_limit) {
-  for (int i = threadIdx.x; i < rows * (d / 8); i += blockDim.x) {
-    const int r = i / (d / 8), c8 = (i % (d / 8)) * 8;
-    float* o = dst + r * pitch + c8;
-    if (row0 + r < row_limit) {
-      const uint4 w = *reinterpret_cast<const uint4*>(src + int64_t(row0 + r) * s_tok + c8);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[2 * e] = __uint_as_float(ws[e] << 16);
-        o[2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = 0.f;
-    }
-  }
-}
-
 struct EstParams {
-  const uint16_t* q;
-  const uint16_t* k;
-  int64_t sq[3], sk[3];
-  int B, N, Hq, Hkv, d;
+  int B, N, Hq, Hkv, d, g, MT;  // MT: 128-row tiles per KV head = ceil(g / 2)
   float scale_log2;
   float2* part;   // [BH][kSplits][64] (max, sum) in log2 units
+  float* lse;     // [BH][64] log2 units
   float* v;       // [BH][N]
-  float* spart;   // [BH][NT][128]
+  float* spart;   // [BH][NT][kEstDiag]
   float* s;       // [BH][N]
+  int* err;
 };
 
-__global__ void __launch_bounds__(kEstThreads) est_rowstats(const EstParams p) {
-  extern __shared__ float sm[];
-  const int d = p.d, pitch = d + 4;
-  float* qs = sm;                      // [64][pitch]
-  float* ks = sm + kLastQ * pitch;     // [kChunk][pitch]
-  const int bh = blockIdx.x, sp = blockIdx.y;
-  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / (p.Hq / p.Hkv);
-  const int N = p.N;
-  const int per = ((N + kSplits - 1) / kSplits + kChunk - 1) / kChunk * kChunk;
-  const int k0 = sp * per, k1 = min(N, k0 + per);
-  const uint16_t* qb = p.q + int64_t(b) * p.sq[0] + int64_t(h) * p.sq[2];
-  const uint16_t* kb = p.k + int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2];
-  load_rows_f32(qs, pitch, qb, p.sq[1], kLastQ, d, N - kLastQ, N);
-  const int r = threadIdx.x / 4, kl = threadIdx.x % 4;
-  const int n = N - kLastQ + r;
-  float m = -INFINITY, l = 0.f;
-  for (int c0 = k0; c0 < k1; c0 += kChunk) {
-    __syncthreads();
-    load_rows_f32(ks, pitch, kb, p.sk[1], kChunk, d, c0, k1);
-    __syncthreads();
-    float acc[kChunk / 4];
-#pragma unroll
-    for (int i = 0; i < kChunk / 4; ++i) acc[i] = 0.f;
-    for (int c = 0; c < d; c += 4) {
-      const float4 qv = *reinterpret_cast<const float4*>(qs + r * pitch + c);
-#pragma unroll
-      for (int i = 0; i < kChunk / 4; ++i) {
-        const float4 kv = *reinterpret_cast<const float4*>(ks + (kl + 4 * i) * pitch + c);
-        acc[i] += qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kChunk / 4; ++i) {
-      const int key = c0 + kl + 4 * i;
-      if (key < k1 && key <= n) {
-        const float x = acc[i] * p.scale_log2;
-        if (x > m) {
-          l = l * exp2f(m - x) + 1.f;
-          m = x;
-        } else {
-          l += exp2f(x - m);
-        }
-      }
-    }
-  }
-  // merge the four key lanes of the row
-#pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-    const float lo = __shfl_xor_sync(0xffffffffu, l, off);
-    const float mn = fmaxf(m, mo);
-    if (mn == -INFINITY) continue;
-    l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + (mo == -INFINITY ? 0.f : lo * exp2f(mo - mn));
-    m = mn;
-  }
-  if (kl == 0) p.part[(int64_t(bh) * kSplits + sp) * kLastQ + r] = make_float2(m, l);
+// Shared memory of both tensor-core passes: one 128-row Q tile (two heads'
+// last 64 rows) per buffer, 128-key K tiles, the staged A_hat tile.
+template <int D>
+struct EstSmem {
+  static constexpr int NH = D / 64;
+  uint8_t q[2][NH][128 * 128];
+  uint8_t k[2][NH][kEstKeys * 128];
+  float stage[128][kEstKeys + 1];  // pass 2: A_hat of the row tile (pitch 129: conflict-free rows and columns)
+  float lse[128];
+  float red_m[128], red_l[128];    // pass 1: the second column half's (max, sum)
+  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], s_full[2], s_free[2], teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// First query head (within the group) of row tile mt's two heads; a tile's
+// second head may not exist (odd g): its rows load the first head again and
+// are ignored.
+__device__ __forceinline__ int est_tile_head(int hk, int g, int mt, int hh) {
+  return hk * g + min(2 * mt + hh, g - 1);
 }
 
-__global__ void __launch_bounds__(kEstThreads) est_scores(const EstParams p) {
-  extern __shared__ float sm[];
-  const int d = p.d, pitch = d + 4;
-  float* qs = sm;                        // [64][pitch]
-  float* ks = qs + kLastQ * pitch;       // [64][pitch]
-  float* at = ks + 64 * pitch;           // [64][65]  A_hat tile
-  float* lse = at + 64 * 65;             // [64]
-  const int bh = blockIdx.x, tile = blockIdx.y;
-  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / (p.Hq / p.Hkv);
-  const int N = p.N, m0 = tile * 64;
-  if (threadIdx.x < kLastQ) {
-    const float2* pp = p.part + int64_t(bh) * kSplits * kLastQ + threadIdx.x;
+template <int D>
+__device__ __forceinline__ void est_load_q(EstSmem<D>& s, int buf, const CUtensorMap* tmQ, int hk, int g, int mt,
+                                           int N, int b) {
+  constexpr int NH = D / 64;
+  mbar_arrive_expect_tx(&s.q_full[buf], 2 * NH * 64 * 128);
+  for (int hh = 0; hh < 2; ++hh)
+    for (int hf = 0; hf < NH; ++hf)
+      tma_load_4d(s.q[buf][hf] + hh * 64 * 128, tmQ, &s.q_full[buf], 64 * hf, est_tile_head(hk, g, mt, hh),
+                  N - kLastQ, b);
+}
+
+// S = Q K^T of one row tile and one key tile into TMEM columns [col, col + 128).
+template <int D>
+__device__ __forceinline__ void est_mma(EstSmem<D>& s, int qb, int kb, uint32_t dst) {
+  const uint32_t idS = idesc_bf16(128, kEstKeys, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t da = sdesc_sw128(smem_u32(s.q[qb][kk / 4]) + (kk % 4) * 32, 16, 1024);
+    const uint64_t db = sdesc_sw128(smem_u32(s.k[kb][kk / 4]) + (kk % 4) * 32, 16, 1024);
+    mma_ss(dst, da, db, idS, kk > 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void est_init(EstSmem<D>& s, int ncols) {
+  const int warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], 1);
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.s_free[i], kEstCompute);
+    }
+    mbar_init(&s.teardown, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+template <int D>
+__device__ __forceinline__ void est_teardown(EstSmem<D>& s, bool mma_issued, int ncols) {
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x / 32 == 1) {
+    if (threadIdx.x % 32 == 0 && mma_issued && s.abort_flag) {
+      // make sure no MMA still writes TMEM before it is released
+      mma_commit(&s.teardown);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&s.teardown, 0) && global_ns() - t0 < kWaitBudgetNs) {
+      }
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(s.tmem_base, ncols);
+  }
+}
+
+// Pass 1: grid (B * Hkv * MT, kSplits).  Keys of split sp: 128-key chunks
+// [c * 128, c * 128 + 128) with c = sp, sp + kSplits, ... (interleaved so that
+// every split sees the same share of the causal edge).
+template <int D>
+__global__ void __launch_bounds__(kEstThreads, 1)
+    est_rowstats(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const EstParams p) {
+  constexpr int NH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  EstSmem<D>& s = *reinterpret_cast<EstSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int mt = int(blockIdx.x) % p.MT, bhk = int(blockIdx.x) / p.MT;
+  const int b = bhk / p.Hkv, hk = bhk % p.Hkv, sp = blockIdx.y;
+  const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys;
+  const int nchunk = NT > sp ? (NT - sp + kSplits - 1) / kSplits : 0;
+  est_init<D>(s, 256);
+  const uint32_t tmem = s.tmem_base;
+  const Abort ab{&s.abort_flag, p.err};
+  bool mma_issued = false;
+  if (warp == 0) {
+    if (lane == 0 && nchunk > 0) {
+      est_load_q<D>(s, 0, &tmQ, hk, p.g, mt, N, b);
+      for (int c = 0; c < nchunk; ++c) {
+        const int kb = c & 1;
+        if (c >= 2 && !mbar_wait(&s.k_empty[kb], ((c >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+        mbar_arrive_expect_tx(&s.k_full[kb], NH * kEstKeys * 128);
+        for (int hf = 0; hf < NH; ++hf)
+          tma_load_4d(s.k[kb][hf], &tmK, &s.k_full[kb], 64 * hf, hk, (sp + c * kSplits) * kEstKeys, b);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nchunk > 0) {
+      bool ok = mbar_wait(&s.q_full[0], 0, ab, VS_ERR_TIMEOUT);
+      for (int c = 0; ok && c < nchunk; ++c) {
+        const int kb = c & 1;
+        if (!(ok = mbar_wait(&s.k_full[kb], (c >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (c >= 2 && !(ok = mbar_wait(&s.s_free[kb], ((c >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        tc_fence_after();
+        est_mma<D>(s, 0, kb, tmem + 128 * kb);
+        mma_commit(&s.s_full[kb]);
+        mma_commit(&s.k_empty[kb]);
+        mma_issued = true;
+      }
+    }
+  } else {
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane, i = r & 63;
+    const int64_t n_i = int64_t(N) - kLastQ + i;
+    const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
     float m = -INFINITY, l = 0.f;
-    for (int sp = 0; sp < kSplits; ++sp) {
-      const float2 x = pp[sp * kLastQ];
-      if (x.x == -INFINITY) continue;
-      const float mn = fmaxf(m, x.x);
-      l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + x.y * exp2f(x.x - mn);
-      m = mn;
+    bool ok = true;
+    for (int c = 0; c < nchunk; ++c) {
+      const int kb = c & 1;
+      ok = mbar_wait(&s.s_full[kb], (c >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t x[64];
+      tmem_ld32(tl + 128 * kb + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tl + 128 * kb + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.s_free[kb]);
+      const int64_t key0 = int64_t(sp + c * kSplits) * kEstKeys + 64 * half;
+      const int nvalid = int(max(int64_t(0), min(int64_t(64), n_i - key0 + 1)));  // keys <= n_i (N - 1 at most)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k)
+        if (k < nvalid) mx = fmaxf(mx, __uint_as_float(x[k]) * p.scale_log2);
+      if (mx == -INFINITY) continue;
+      if (mx > m) {
+        l = (m == -INFINITY) ? 0.f : l * ex2(m - mx);
+        m = mx;
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 64; ++k)
+        if (k < nvalid) acc[k & 3] += ex2(fmaf(__uint_as_float(x[k]), p.scale_log2, -m));
+      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
-    lse[threadIdx.x] = m + log2f(l);
-  }
-  const uint16_t* qb = p.q + int64_t(b) * p.sq[0] + int64_t(h) * p.sq[2];
-  const uint16_t* kb = p.k + int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2];
-  load_rows_f32(qs, pitch, qb, p.sq[1], kLastQ, d, N - kLastQ, N);
-  load_rows_f32(ks, pitch, kb, p.sk[1], 64, d, m0, N);
-  __syncthreads();
-  const int r = threadIdx.x / 4, kl = threadIdx.x % 4;
-  const int n = N - kLastQ + r;
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int c = 0; c < d; c += 4) {
-    const float4 qv = *reinterpret_cast<const float4*>(qs + r * pitch + c);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float4 kv = *reinterpret_cast<const float4*>(ks + (kl + 4 * i) * pitch + c);
-      acc[i] += qv.x * kv.x + qv.y * kv.y + qv.z * kv.z + qv.w * kv.w;
+    // merge the two column halves of each row
+    if (half == 1) {
+      s.red_m[r] = m;
+      s.red_l[r] = l;
+    }
+    bar_sync_and(1, kEstCompute, true);
+    if (half == 0 && ok) {
+      const float mo = s.red_m[r], lo = s.red_l[r];
+      const float mn = fmaxf(m, mo);
+      const float ln = (mn == -INFINITY) ? 0.f
+                                         : ((m == -INFINITY ? 0.f : l * ex2(m - mn)) +
+                                            (mo == -INFINITY ? 0.f : lo * ex2(mo - mn)));
+      const int hh = r >> 6;
+      if (2 * mt + hh < p.g) {
+        const int64_t bh = int64_t(b) * p.Hq + hk * p.g + 2 * mt + hh;
+        p.part[(bh * kSplits + sp) * kLastQ + i] = make_float2(mn, ln);
+      }
     }
   }
-  const float L = lse[r];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = kl + 4 * i, key = m0 + j;
-    at[r * 65 + j] = (key <= n) ? exp2f(acc[i] * p.scale_log2 - L) : 0.f;
+  est_teardown<D>(s, mma_issued, 256);
+}
+
+// LSE (log2 units) of every (b, h, last-64 row) from its key-split partials.
+__global__ void est_lse(const EstParams p) {
+  const int bh = blockIdx.x, i = threadIdx.x;
+  const float2* pp = p.part + int64_t(bh) * kSplits * kLastQ + i;
+  float m = -INFINITY, l = 0.f;
+  for (int sp = 0; sp < kSplits; ++sp) {  // fixed order
+    const float2 x = pp[sp * kLastQ];
+    if (x.x == -INFINITY) continue;
+    const float mn = fmaxf(m, x.x);
+    l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + x.y * exp2f(x.x - mn);
+    m = mn;
   }
-  __syncthreads();
-  // vertical: column sums (4 threads per key, 16 rows each)
-  {
-    const int j = threadIdx.x / 4, part = threadIdx.x % 4;
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sum += at[(part * 16 + i) * 65 + j];
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    if (part == 0) p.v[int64_t(bh) * N + m0 + j] = sum;
-  }
-  // slash: diagonal delta = r - j in [-63, 63] <-> offset o = N - 64 - m0 + delta
-  if (threadIdx.x < 128) {
-    const int t = threadIdx.x;
-    float sum = 0.f;
-    if (t < 127) {
-      const int delta = t - 63;
-      const int rlo = max(0, delta), rhi = min(63, 63 + delta);
-      for (int rr = rlo; rr <= rhi; ++rr) sum += at[rr * 65 + (rr - delta)];
+  p.lse[int64_t(bh) * kLastQ + i] = m + log2f(l);
+}
+
+// Pass 2: grid (B * Hkv, NT).  One key tile; its row tiles one after another.
+template <int D>
+__global__ void __launch_bounds__(kEstThreads, 1)
+    est_scores(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const EstParams p) {
+  constexpr int NH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  EstSmem<D>& s = *reinterpret_cast<EstSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bhk = blockIdx.x, tile = blockIdx.y;
+  const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
+  const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys, MT = p.MT;
+  const int64_t m0 = int64_t(tile) * kEstKeys;
+  est_init<D>(s, 256);
+  const uint32_t tmem = s.tmem_base;
+  const Abort ab{&s.abort_flag, p.err};
+  bool mma_issued = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.k_full[0], NH * kEstKeys * 128);
+      for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.k[0][hf], &tmK, &s.k_full[0], 64 * hf, hk, int(m0), b);
+      for (int mt = 0; mt < MT; ++mt) {
+        const int qb = mt & 1;
+        if (mt >= 2 && !mbar_wait(&s.q_empty[qb], ((mt >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+        est_load_q<D>(s, qb, &tmQ, hk, p.g, mt, N, b);
+      }
     }
-    p.spart[(int64_t(bh) * (N / 64) + tile) * 128 + t] = sum;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(&s.k_full[0], 0, ab, VS_ERR_TIMEOUT);
+      for (int mt = 0; ok && mt < MT; ++mt) {
+        const int qb = mt & 1;
+        if (!(ok = mbar_wait(&s.q_full[qb], (mt >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (mt >= 2 && !(ok = mbar_wait(&s.s_free[qb], ((mt >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        tc_fence_after();
+        est_mma<D>(s, qb, 0, tmem + 128 * qb);
+        mma_commit(&s.s_full[qb]);
+        mma_commit(&s.q_empty[qb]);
+        mma_issued = true;
+      }
+    }
+  } else {
+    const int t = threadIdx.x - 64;  // 0..255
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane, i = r & 63;
+    const int64_t n_i = int64_t(N) - kLastQ + i;
+    const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
+    bool ok = true;
+    for (int mt = 0; mt < MT; ++mt) {
+      const int qb = mt & 1;
+      if (half == 0) {
+        const int hh = r >> 6;
+        const int64_t bh = int64_t(b) * p.Hq + est_tile_head(hk, p.g, mt, hh);
+        s.lse[r] = p.lse[bh * kLastQ + i];
+      }
+      ok = mbar_wait(&s.s_full[qb], (mt >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      // every compute warp takes the same decision (and the tile's lse is visible)
+      ok = bar_sync_and(1, kEstCompute, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t x[64];
+      tmem_ld32(tl + 128 * qb + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(tl + 128 * qb + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.s_free[qb]);
+      const float L = s.lse[r];
+      const int64_t key0 = m0 + 64 * half;
+      const int nvalid = int(max(int64_t(0), min(int64_t(64), n_i - key0 + 1)));
+      float* row = &s.stage[r][64 * half];
+#pragma unroll
+      for (int k = 0; k < 64; ++k)
+        row[k] = (k < nvalid) ? ex2(fmaf(__uint_as_float(x[k]), p.scale_log2, -L)) : 0.f;
+      bar_sync_and(1, kEstCompute, true);  // tile staged
+      // vertical: column sums of each head's 64 rows
+      {
+        const int j = t & 127, hh = t >> 7;
+        if (2 * mt + hh < p.g && m0 + j < N) {
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+          for (int ii = 0; ii < 64; ii += 2) {
+            a0 += s.stage[64 * hh + ii][j];
+            a1 += s.stage[64 * hh + ii + 1][j];
+          }
+          const int64_t bh = int64_t(b) * p.Hq + hk * p.g + 2 * mt + hh;
+          p.v[bh * N + m0 + j] = a0 + a1;
+        }
+      }
+      // slash: diagonal delta = row - key in [-127, 63] of each head
+      for (int w = t; w < 2 * kEstDiag; w += kEstCompute) {
+        const int hh = w / kEstDiag, dgi = w % kEstDiag;
+        if (2 * mt + hh >= p.g) continue;
+        float sum = 0.f;
+        if (dgi < 191) {
+          const int delta = dgi - 127;
+          const int lo = max(0, delta), hi = min(63, 127 + delta);
+          for (int ii = lo; ii <= hi; ++ii) sum += s.stage[64 * hh + ii][ii - delta];
+        }
+        const int64_t bh = int64_t(b) * p.Hq + hk * p.g + 2 * mt + hh;
+        p.spart[(bh * NT + tile) * kEstDiag + dgi] = sum;
+      }
+      bar_sync_and(1, kEstCompute, true);  // stage and lse free for the next row tile
+    }
   }
+  est_teardown<D>(s, mma_issued, 256);
 }
 
 __global__ void est_scombine(const EstParams p) {
   const int bh = blockIdx.y;
-  const int N = p.N, NT = N / 64;
+  const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys;
   const int o = blockIdx.x * blockDim.x + threadIdx.x;
   if (o >= N) return;
-  const float* sp = p.spart + int64_t(bh) * NT * 128;
-  const int x = N - 64 - o;
-  const int Tc = (x >= 0) ? x / 64 : -1;
+  const float* sp = p.spart + int64_t(bh) * NT * kEstDiag;
+  const int x = N - kLastQ - o;  // tile T holds o at delta = 128 T - x in [-127, 63]
+  const int Thi = (x + 63 >= 0) ? (x + 63) / kEstKeys : -1;
   float sum = 0.f;
-  for (int T = Tc; T <= Tc + 1; ++T) {  // fixed order
+  for (int T = Thi - 1; T <= Thi; ++T) {  // fixed order
     if (T < 0 || T >= NT) continue;
-    const int delta = o - (N - 64 - 64 * T);
-    if (delta >= -63 && delta <= 63) sum += sp[int64_t(T) * 128 + delta + 63];
+    const int delta = kEstKeys * T - x;
+    if (delta >= -127 && delta <= 63) sum += sp[int64_t(T) * kEstDiag + delta + 127];
   }
   p.s[int64_t(bh) * N + o] = sum;
 }
@@ -311,44 +484,29 @@ __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
   }
 }
 
-}  // namespace
-
-size_t estimate_workspace_bytes(const vs_shape* s, int) { return size_t(est_layout(s).total); }
-
-vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, int kv, int ks, float scale,
-                          int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
-                          cudaStream_t st) {
-  const EstLayout L = est_layout(s);
-  uint8_t* W = static_cast<uint8_t*>(ws);
-  EstParams p;
-  p.q = static_cast<const uint16_t*>(q);
-  p.k = static_cast<const uint16_t*>(k);
-  for (int i = 0; i < 3; ++i) {
-    p.sq[i] = s->sq[i];
-    p.sk[i] = s->sk[i];
-  }
-  p.B = s->B;
-  p.N = s->Nk;
-  p.Hq = s->Hq;
-  p.Hkv = s->Hkv;
-  p.d = s->d;
-  p.scale_log2 = scale * kLog2e;
-  p.part = reinterpret_cast<float2*>(W + L.off_part);
-  p.v = v_score ? v_score : reinterpret_cast<float*>(W + L.off_vbuf);
-  p.spart = reinterpret_cast<float*>(W + L.off_spart);
-  p.s = s_score ? s_score : reinterpret_cast<float*>(W + L.off_sbuf);
-  const int BH = s->B * s->Hq;
-  const int pitch = s->d + 4;
-  const size_t sm1 = size_t(kLastQ + kChunk) * pitch * 4;
-  const size_t sm2 = (size_t(kLastQ + 64) * pitch + 64 * 65 + 64) * 4;
-  if (cudaFuncSetAttribute(est_rowstats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm1)) != cudaSuccess ||
-      cudaFuncSetAttribute(est_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm2)) != cudaSuccess)
+// The estimator's kernels on the given scratch (p.part / lse / spart and the
+// score outputs set by the caller).
+template <int D>
+vs_status launch_est_kernels(const vs_shape* s, const void* q, const void* k, EstParams& p, int kv, int ks,
+                             int32_t* v_idx, int32_t* s_idx, cudaStream_t st) {
+  CUtensorMap tq, tk;
+  vs_status rc;
+  if ((rc = make_tmap_bshd(&tq, q, s->B, s->Nq, s->Hq, D, s->sq, kLastQ)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tk, k, s->B, s->Nk, s->Hkv, D, s->sk, kEstKeys)) != VS_OK) return rc;
+  const size_t sm = sizeof(EstSmem<D>) + 1024;
+  if (cudaFuncSetAttribute(est_rowstats<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)) != cudaSuccess ||
+      cudaFuncSetAttribute(est_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)) != cudaSuccess)
     return VS_ERR_CUDA;
+  const int BH = s->B * s->Hq, BHK = s->B * s->Hkv;
+  const int NT = (s->Nk + kEstKeys - 1) / kEstKeys;
   trace_begin("est_rowstats", st);
-  est_rowstats<<<dim3(BH, kSplits), kEstThreads, sm1, st>>>(p);
+  est_rowstats<D><<<dim3(BHK * p.MT, kSplits), kEstThreads, sm, st>>>(tq, tk, p);
+  trace_end(st);
+  trace_begin("est_lse", st);
+  est_lse<<<BH, kLastQ, 0, st>>>(p);
   trace_end(st);
   trace_begin("est_scores", st);
-  est_scores<<<dim3(BH, s->Nk / 64), kEstThreads, sm2, st>>>(p);
+  est_scores<D><<<dim3(BHK, NT), kEstThreads, sm, st>>>(tq, tk, p);
   trace_end(st);
   trace_begin("est_scombine", st);
   est_scombine<<<dim3((s->Nk + 255) / 256, BH), 256, 0, st>>>(p);
@@ -364,8 +522,47 @@ vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, 
   trace_begin("est_topk", st);
   est_topk<<<dim3(BH, 2), kTopkThreads, 0, st>>>(tp);
   trace_end(st);
-  note_launch(4);
+  note_launch(5);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+EstParams est_params(const vs_shape* s, float scale, int* err) {
+  EstParams p;
+  p.B = s->B;
+  p.N = s->Nk;
+  p.Hq = s->Hq;
+  p.Hkv = s->Hkv;
+  p.d = s->d;
+  p.g = s->Hq / s->Hkv;
+  p.MT = (p.g + 1) / 2;
+  p.scale_log2 = scale * kLog2e;
+  p.err = err;
+  return p;
+}
+
+vs_status launch_est(const vs_shape* s, const void* q, const void* k, EstParams& p, int kv, int ks, int32_t* v_idx,
+                     int32_t* s_idx, cudaStream_t st) {
+  if (s->d == 128) return launch_est_kernels<128>(s, q, k, p, kv, ks, v_idx, s_idx, st);
+  if (s->d == 64) return launch_est_kernels<64>(s, q, k, p, kv, ks, v_idx, s_idx, st);
+  return VS_ERR_SHAPE;
+}
+
+}  // namespace
+
+size_t estimate_workspace_bytes(const vs_shape* s, int) { return size_t(est_layout(s).total); }
+
+vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, int kv, int ks, float scale,
+                          int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                          cudaStream_t st) {
+  const EstLayout L = est_layout(s);
+  uint8_t* W = static_cast<uint8_t*>(ws);
+  EstParams p = est_params(s, scale, static_cast<int*>(ws));
+  p.part = reinterpret_cast<float2*>(W + L.off_part);
+  p.lse = reinterpret_cast<float*>(W + L.off_lse);
+  p.v = v_score ? v_score : reinterpret_cast<float*>(W + L.off_vbuf);
+  p.spart = reinterpret_cast<float*>(W + L.off_spart);
+  p.s = s_score ? s_score : reinterpret_cast<float*>(W + L.off_sbuf);
+  return launch_est(s, q, k, p, kv, ks, v_idx, s_idx, st);
 }
 
 }  // namespace vs
@@ -398,15 +595,17 @@ void* noalloc_scratch_address(int dev) {
   return g_noalloc_ptr[dev];
 }
 
-// Scratch layout: 256-byte status header, per-split row statistics,
-// per-tile slash partials.  Returns the bytes needed.
-int64_t noalloc_layout(const vs_shape* s, int64_t* off_part, int64_t* off_spart) {
-  const int64_t BH = int64_t(s->B) * s->Hq, N = s->Nk, NT = N / 64;
+// Scratch layout: 256-byte status header, per-split row statistics, row
+// LSEs, per-tile slash partials.  Returns the bytes needed.
+int64_t noalloc_layout(const vs_shape* s, int64_t* off_part, int64_t* off_lse, int64_t* off_spart) {
+  const int64_t BH = int64_t(s->B) * s->Hq, N = s->Nk, NT = (N + vs::kEstKeys - 1) / vs::kEstKeys;
   int64_t off = 256;
   *off_part = off;
   off += (BH * vs::kSplits * vs::kLastQ * 8 + 255) / 256 * 256;
+  *off_lse = off;
+  off += (BH * vs::kLastQ * 4 + 255) / 256 * 256;
   *off_spart = off;
-  off += (BH * NT * 128 * 4 + 255) / 256 * 256;
+  off += (BH * NT * vs::kEstDiag * 4 + 255) / 256 * 256;
   return off;
 }
 
@@ -425,8 +624,8 @@ extern "C" vs_status vs_estimate_noalloc(const vs_shape* s, const void* q, const
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return VS_ERR_SHAPE;
   if (last_q != 64) return VS_ERR_ARG;
   if (kv < 1 || ks < 1 || kv > s->Nk || ks > s->Nk || !(scale > 0.f)) return VS_ERR_ARG;
-  int64_t off_part = 0, off_spart = 0;
-  if (size_t(noalloc_layout(s, &off_part, &off_spart)) > kNoAllocScratchBytes) return VS_ERR_WORKSPACE;
+  int64_t off_part = 0, off_lse = 0, off_spart = 0;
+  if (size_t(noalloc_layout(s, &off_part, &off_lse, &off_spart)) > kNoAllocScratchBytes) return VS_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return VS_ERR_CUDA;
   uint8_t* W = static_cast<uint8_t*>(noalloc_scratch_address(dev));
@@ -434,42 +633,11 @@ extern "C" vs_status vs_estimate_noalloc(const vs_shape* s, const void* q, const
   // The kernels write every scratch element they later read within the
   // call; only the status header is cleared.
   if (cudaMemsetAsync(W, 0, 256, stream) != cudaSuccess) return VS_ERR_CUDA;
-  EstParams p;
-  p.q = static_cast<const uint16_t*>(q);
-  p.k = static_cast<const uint16_t*>(k);
-  for (int i = 0; i < 3; ++i) {
-    p.sq[i] = s->sq[i];
-    p.sk[i] = s->sk[i];
-  }
-  p.B = s->B;
-  p.N = s->Nk;
-  p.Hq = s->Hq;
-  p.Hkv = s->Hkv;
-  p.d = s->d;
-  p.scale_log2 = scale * kLog2e;
+  EstParams p = est_params(s, scale, reinterpret_cast<int*>(W));
   p.part = reinterpret_cast<float2*>(W + off_part);
+  p.lse = reinterpret_cast<float*>(W + off_lse);
   p.v = v_score;
   p.spart = reinterpret_cast<float*>(W + off_spart);
   p.s = s_score;
-  const int BH = s->B * s->Hq;
-  const int pitch = s->d + 4;
-  const size_t sm1 = size_t(kLastQ + kChunk) * pitch * 4;
-  const size_t sm2 = (size_t(kLastQ + 64) * pitch + 64 * 65 + 64) * 4;
-  if (cudaFuncSetAttribute(est_rowstats, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm1)) != cudaSuccess ||
-      cudaFuncSetAttribute(est_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm2)) != cudaSuccess)
-    return VS_ERR_CUDA;
-  est_rowstats<<<dim3(BH, kSplits), kEstThreads, sm1, stream>>>(p);
-  est_scores<<<dim3(BH, s->Nk / 64), kEstThreads, sm2, stream>>>(p);
-  est_scombine<<<dim3((s->Nk + 255) / 256, BH), 256, 0, stream>>>(p);
-  TopkParams tp;
-  tp.score = p.v;
-  tp.score2 = p.s;
-  tp.out = v_idx;
-  tp.out2 = s_idx;
-  tp.N = s->Nk;
-  tp.k = kv;
-  tp.k2 = ks;
-  est_topk<<<dim3(BH, 2), kTopkThreads, 0, stream>>>(tp);
-  note_launch(4);
-  return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+  return launch_est(s, q, k, p, kv, ks, v_idx, s_idx, stream);
 }

@@ -107,16 +107,18 @@ vs_status vs_estimate(const vs_shape* shape, const void* q, const void* k, int l
  * allocation while it executes, or latency-critical loops where cudaMalloc's
  * implicit device-wide synchronisation would stall every other stream.  This
  * entry point computes exactly what vs_estimate computes, with the same
- * kernels, but keeps its scratch (row statistics and slash partials) in a
+ * kernels, but keeps its scratch (row statistics, row LSEs and slash
+ * partials) in a
  * fixed 32 MiB array of the library's static device memory, which every GPU
  * that loads the library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
  *   Arguments as for vs_estimate, except that v_score and s_score are
  *   required (the scores live in the caller's buffers, not in the scratch).
- *   Scratch needed: 256 + B*Hq*32 KiB + B*Hq*N*8 bytes (each term rounded up
- *   to 256); larger problems are rejected with VS_ERR_WORKSPACE before any
- *   launch (for example B*Hq = 16 fits N up to 257984).
+ *   Scratch needed: 256 + B*Hq*32 KiB + B*Hq*256 + B*Hq*ceil(N/128)*768
+ *   bytes (each term rounded up to 256); larger problems are rejected with
+ *   VS_ERR_WORKSPACE before any launch (for example B*Hq = 16 fits N up to
+ *   343936).
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
