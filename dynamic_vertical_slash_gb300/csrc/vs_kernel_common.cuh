@@ -32,28 +32,17 @@ __device__ __forceinline__ Geo geo_from(const ArenaHeader* h, int Hkv, int d) {
   return G;
 }
 
-// Slash-tile mask of one query row against the 64 keys starting at local key
-// c (query-major passes).  Bit k set iff offset n_g - m_g(c + k) is selected,
-// key c + k is not a selected column, and the key exists (c + k >= 0).  The
-// 64 keys are globally contiguous (unstriped, or c block-aligned).
-__device__ __forceinline__ uint64_t slash_row_mask(const Geo& G, const uint64_t* offbits, const uint64_t* colbits,
-                                                   int64_t n_g, int64_t c) {
-  const int64_t m0 = (c >= 0) ? kpos_g(G, c) : c;  // c < 0 only without striping
-  const int64_t base = n_g - m0;                    // offset of key k is base - k
-  const uint64_t x = bits64(offbits, base - 63, G.WG);
-  uint64_t m = __brevll(x);                          // bit k <-> offset base - k
-  m &= ~bits64(colbits, m0, G.WG);                   // vertical entries belong to the bars
-  if (c < 0) m &= (~0ull) << (-c);
-  return m;
-}
-
-// The same slash-tile masks for all 128 rows of query tile t at once, built by
-// one warp: the lane's rows are rr * 32 + lane (rr = 0..3), returned in m[rr].
-// Within a 64-row block the rows' global positions are contiguous, so the
-// offset windows of its 64 rows lie in three consecutive bitmap words; lanes
-// 0-5 load the words of both blocks and lanes 6-7 the two column-bitmap words
-// (one memory round trip per tile), and every row's window is cut out of the
-// shuffled words.  Equal to slash_row_mask for every row.
+// Slash-tile masks of the 128 rows of query tile t against the 64 keys
+// starting at local key c (query-major passes): bit k of row n's mask is set
+// iff offset n_g - m_g(c + k) is selected, key c + k is not a selected column
+// (vertical entries belong to the bars), and the key exists (c + k >= 0; c < 0
+// only without striping).  The 64 keys are globally contiguous (unstriped, or
+// c block-aligned).  Built by one warp: the lane's rows are rr * 32 + lane
+// (rr = 0..3), returned in m[rr].  Within a 64-row block the rows' global
+// positions are contiguous, so the offset windows of its 64 rows lie in three
+// consecutive bitmap words; lanes 0-5 load the words of both blocks and lanes
+// 6-7 the two column-bitmap words (one memory round trip per tile), and every
+// row's window is cut out of the shuffled words.
 __device__ __forceinline__ void slash_tile_masks(const Geo& G, const uint64_t* offbits, const uint64_t* colbits,
                                                  int t, int64_t c, int Nq, int lane, uint64_t (&m)[4]) {
   const int64_t m0 = (c >= 0) ? kpos_g(G, c) : c;
