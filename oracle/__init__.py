@@ -8,7 +8,8 @@ Plain, slow and fp64: the arithmetic lives in ``vs_oracle.c`` (loaded with
 ctypes) plus a few numpy helpers here that follow the pages' definitions
 directly:
 
-* ``estimate`` / ``topk`` / ``select`` -- Algorithm 1 of *MTraining:
+* ``estimate`` / ``topk`` / ``select`` / ``topp_budget`` / ``select_topp`` --
+  Algorithm 1 of *MTraining:
   Distributed Dynamic Sparse Attention for Efficient Ultra-Long Context
   Training*: the last-``last_q`` observation window, ``sum_v`` / ``sum_s`` and
   ``argtopk`` (fixed budgets; ties go to the lower index).
@@ -23,6 +24,7 @@ Inputs are converted to float64 (bf16 values widen exactly); all arithmetic is f
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import numpy as np
@@ -106,6 +108,68 @@ def select(v: np.ndarray, s: np.ndarray, kv: int, ks: int):
             iv[b, h] = topk(v[b, h], kv)
             is_[b, h] = topk(s[b, h], ks)
     return iv, is_
+
+
+# Top-p budgets decide an integer (a count) from sums of scores, so both this
+# oracle and the kernels take the decision in one exact precision: a score x
+# counts floor(x * 2^40) mass units, sums of units are exact integers, and the
+# target is t = ceil(fl(p * T)) for the list total T (one IEEE double product).
+MASS_UNIT_LOG2 = 40
+
+
+def mass_units(score: np.ndarray) -> np.ndarray:
+    """floor(x * 2^40) of each score as int64 (exact: scaling by a power of two)."""
+    x = np.asarray(score, np.float64)
+    return np.floor(x * float(2 ** MASS_UNIT_LOG2)).astype(np.int64)
+
+
+def topp_budget(units: np.ndarray, p: float) -> int:
+    """``topp`` of Algorithm 1 on integer mass units: the smallest k in [0, n]
+    whose k largest units sum to at least t = ceil(p * T), T = sum of all
+    units; n when no k reaches t.  (Which of several equal units is counted
+    does not change the sum, so ties need no rule here.)"""
+    u = np.sort(np.asarray(units, np.int64))[::-1]
+    n = u.size
+    T = int(u.sum())
+    t = math.ceil(float(p) * float(T))
+    if t <= 0:
+        return 0
+    csum = np.cumsum(u)
+    k = int(np.searchsorted(csum, t, side="left")) + 1
+    return min(k, n)
+
+
+def pool(units: np.ndarray, block: int = 64) -> np.ndarray:
+    """``Pool`` of Algorithm 1: the sum of each run of `block` consecutive
+    entries (the last run may be shorter)."""
+    u = np.asarray(units, np.int64)
+    nb = (u.size + block - 1) // block
+    padded = np.zeros(nb * block, np.int64)
+    padded[:u.size] = u
+    return padded.reshape(nb, block).sum(1)
+
+
+def select_topp(v: np.ndarray, s: np.ndarray, pv: float, ps: float, kv_max: int, ks_max: int, block: int = 64):
+    """Budgets from top-p, then token-level selection (Algorithm 1):
+    kv = min(topp(units(v), pv), kv_max); ks = min(block * topp(Pool(units(s),
+    block), ps), ks_max, N); iv = argtopk(v, kv), is = argtopk(s, ks).  The
+    slash budget pools the slash scores (the listing's ``Pool(sum_v ...)`` is
+    read as ``Pool(sum_s ...)``: the budget it sets is spent on sum_s) in
+    64-offset blocks, matching the kernel's 64 x 64 slash tiles.
+    Returns (iv [B,H,kv_max], is [B,H,ks_max], kv [B,H], ks [B,H]); each list
+    holds its budget's indices ascending, then -1."""
+    B, H, N = v.shape
+    iv = np.full((B, H, kv_max), -1, np.int32)
+    is_ = np.full((B, H, ks_max), -1, np.int32)
+    kv = np.zeros((B, H), np.int32)
+    ks = np.zeros((B, H), np.int32)
+    for b in range(B):
+        for h in range(H):
+            kv[b, h] = min(topp_budget(mass_units(v[b, h]), pv), kv_max)
+            ks[b, h] = min(block * topp_budget(pool(mass_units(s[b, h]), block), ps), ks_max, N)
+            iv[b, h, :kv[b, h]] = topk(v[b, h], int(kv[b, h]))
+            is_[b, h, :ks[b, h]] = topk(s[b, h], int(ks[b, h]))
+    return iv, is_, kv, ks
 
 
 # ------------------------------------------------------------------ attention

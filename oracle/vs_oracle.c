@@ -155,8 +155,11 @@ static void tables_build(const ora_problem* p, int b, int h, ora_tables* t) {
   for (int m = 0; m < p->Nk; ++m) t->loc[p->kpos[m]] = m;
   const int32_t* iv = p->iv + ((size_t)b * p->Hq + h) * p->kv;
   const int32_t* is = p->is + ((size_t)b * p->Hq + h) * p->ks;
-  for (int j = 0; j < p->kv; ++j) t->vsel[iv[j]] = 1;
-  for (int j = 0; j < p->ks; ++j) t->ssel[is[j]] = 1;
+  /* entries < 0 pad a list whose budget is below its capacity (top-p) */
+  for (int j = 0; j < p->kv; ++j)
+    if (iv[j] >= 0) t->vsel[iv[j]] = 1;
+  for (int j = 0; j < p->ks; ++j)
+    if (is[j] >= 0) t->ssel[is[j]] = 1;
 }
 static void tables_free(ora_tables* t) {
   free(t->vsel);
@@ -173,12 +176,14 @@ static int mask_row(const ora_problem* p, int b, int h, const ora_tables* t, int
   const int32_t* is = p->is + ((size_t)b * p->Hq + h) * p->ks;
   int cnt = 0;
   for (int j = 0; j < p->ks; ++j) { /* slash entries */
+    if (is[j] < 0) continue;
     const int64_t pm = pn - is[j];
     if (pm < 0) continue;
     const int64_t m = t->loc[pm];
     if (m >= 0) out[cnt++] = (int32_t)m;
   }
   for (int j = 0; j < p->kv; ++j) { /* vertical entries not already on a selected diagonal */
+    if (iv[j] < 0) continue;
     const int64_t pm = iv[j];
     if (pm > pn || t->ssel[pn - pm]) continue;
     const int64_t m = t->loc[pm];
