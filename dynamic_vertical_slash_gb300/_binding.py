@@ -17,7 +17,7 @@ import torch
 
 from . import _build
 
-VS_OK, VS_ERR_ARG, VS_ERR_SHAPE, VS_ERR_WORKSPACE, VS_ERR_INDEX, VS_ERR_TIMEOUT, VS_ERR_CUDA = range(7)
+VS_OK, VS_ERR_ARG, VS_ERR_SHAPE, VS_ERR_WORKSPACE, VS_ERR_INDEX, VS_ERR_TIMEOUT, VS_ERR_CUDA, VS_ERR_SCORE = range(8)
 
 
 class VSError(RuntimeError):
@@ -61,6 +61,10 @@ def lib(build_if_missing: bool = True):
     L.vs_estimate_workspace.restype = ctypes.c_size_t
     L.vs_estimate.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, _P, _P, _P,
                               _P, ctypes.c_size_t, _P]
+    L.vs_estimate_topp.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.vs_select_topp.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_double, ctypes.c_double,
+                                 ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.vs_block_index_bytes.argtypes = [_S, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vs_stripe)]
     L.vs_block_index_bytes.restype = ctypes.c_size_t
     L.vs_build_block_index.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vs_stripe), _P,
@@ -144,6 +148,46 @@ def vs_estimate(q, k, kv: int, ks: int, scale: Optional[float] = None, last_q: i
                              _ptr(v_score), _ptr(s_score), _ptr(ws), ws.numel() * ws.element_size(),
                              _stream(stream)), "vs_estimate")
     return v_idx, s_idx
+
+
+def vs_estimate_topp(q, k, pv: float, ps: float, kv_max: int, ks_max: int, scale: Optional[float] = None,
+                     last_q: int = 64, v_idx=None, s_idx=None, kv=None, ks=None, v_score=None, s_score=None, ws=None,
+                     stream=None):
+    """Vertical and slash selection with top-p budgets (Algorithm 1).  Returns
+    (v_idx [B,Hq,kv_max], s_idx [B,Hq,ks_max], kv [B,Hq], ks [B,Hq]), int32;
+    each list ascending, padded with -1 past its budget."""
+    sh = make_shape(q, k)
+    B, N, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dev = q.device
+    v_idx = torch.empty(B, Hq, kv_max, dtype=torch.int32, device=dev) if v_idx is None else v_idx
+    s_idx = torch.empty(B, Hq, ks_max, dtype=torch.int32, device=dev) if s_idx is None else s_idx
+    kv = torch.empty(B, Hq, dtype=torch.int32, device=dev) if kv is None else kv
+    ks = torch.empty(B, Hq, dtype=torch.int32, device=dev) if ks is None else ks
+    need = lib().vs_estimate_workspace(ctypes.byref(sh), last_q)
+    ws = _ws(need, dev) if ws is None else ws
+    _check(lib().vs_estimate_topp(ctypes.byref(sh), _ptr(q), _ptr(k), last_q, float(pv), float(ps), kv_max, ks_max,
+                                  scale, _ptr(v_idx), _ptr(s_idx), _ptr(kv), _ptr(ks), _ptr(v_score), _ptr(s_score),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "vs_estimate_topp")
+    return v_idx, s_idx, kv, ks
+
+
+def vs_select_topp(v_score, s_score, pv: float, ps: float, kv_max: int, ks_max: int, v_idx=None, s_idx=None,
+                   kv=None, ks=None, ws=None, stream=None):
+    """Top-p budgets and selection on given fp32 scores [B, H, N]."""
+    B, H, N = v_score.shape
+    assert v_score.dtype == torch.float32 and s_score.dtype == torch.float32
+    assert v_score.is_contiguous() and s_score.is_contiguous() and s_score.shape == v_score.shape
+    dev = v_score.device
+    v_idx = torch.empty(B, H, kv_max, dtype=torch.int32, device=dev) if v_idx is None else v_idx
+    s_idx = torch.empty(B, H, ks_max, dtype=torch.int32, device=dev) if s_idx is None else s_idx
+    kv = torch.empty(B, H, dtype=torch.int32, device=dev) if kv is None else kv
+    ks = torch.empty(B, H, dtype=torch.int32, device=dev) if ks is None else ks
+    ws = _ws(256, dev) if ws is None else ws
+    _check(lib().vs_select_topp(B, H, N, _ptr(v_score), _ptr(s_score), float(pv), float(ps), kv_max, ks_max,
+                                _ptr(v_idx), _ptr(s_idx), _ptr(kv), _ptr(ks), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)), "vs_select_topp")
+    return v_idx, s_idx, kv, ks
 
 
 def make_stripe(world: int, q_rank: int, kv_rank: int, N_global: int, stripe: int = 64) -> vs_stripe:

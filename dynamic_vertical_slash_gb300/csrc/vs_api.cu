@@ -106,6 +106,7 @@ const char* vs_status_string(vs_status st) {
     case VS_ERR_INDEX: return "VS_ERR_INDEX: index list out of range, unsorted or duplicated";
     case VS_ERR_TIMEOUT: return "VS_ERR_TIMEOUT: a bounded device wait ran out";
     case VS_ERR_CUDA: return "VS_ERR_CUDA: CUDA runtime error";
+    case VS_ERR_SCORE: return "VS_ERR_SCORE: a score is negative or not finite, or a list's total is too large";
   }
   return "unknown vs_status";
 }
@@ -187,6 +188,38 @@ vs_status vs_estimate(const vs_shape* s, const void* q, const void* k, int last_
   if (!aligned16(q) || !aligned16(k)) return VS_ERR_SHAPE;
   if (ws_bytes < estimate_workspace_bytes(s, last_q)) return VS_ERR_WORKSPACE;
   return launch_estimate(s, q, k, last_q, kv, ks, scale, v_idx, s_idx, v_score, s_score, ws, stream);
+}
+
+vs_status vs_estimate_topp(const vs_shape* s, const void* q, const void* k, int last_q, double pv, double ps,
+                           int kv_max, int ks_max, float scale, int32_t* v_idx, int32_t* s_idx, int32_t* kv,
+                           int32_t* ks, float* v_score, float* s_score, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  vs_status rc = check_shape(s);
+  if (rc != VS_OK) return rc;
+  if (!q || !k || !v_idx || !s_idx || !kv || !ks || !ws) return VS_ERR_ARG;
+  if (s->Nq != s->Nk || size_t(s->Nk) > topp_max_n()) return VS_ERR_SHAPE;
+  if (last_q != 64) return VS_ERR_ARG;
+  if (!(pv >= 0.0 && pv <= 1.0) || !(ps >= 0.0 && ps <= 1.0)) return VS_ERR_ARG;
+  if (kv_max < 1 || ks_max < 1 || kv_max > s->Nk || ks_max > s->Nk) return VS_ERR_ARG;
+  if (!(scale > 0.f)) return VS_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k)) return VS_ERR_SHAPE;
+  if (ws_bytes < estimate_workspace_bytes(s, last_q)) return VS_ERR_WORKSPACE;
+  return launch_estimate_topp(s, q, k, pv, ps, kv_max, ks_max, scale, v_idx, s_idx, kv, ks, v_score, s_score, ws,
+                              stream);
+}
+
+vs_status vs_select_topp(int B, int H, int N, const float* v_score, const float* s_score, double pv, double ps,
+                         int kv_max, int ks_max, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks, void* ws,
+                         size_t ws_bytes, cudaStream_t stream) {
+  if (!v_score || !s_score || !v_idx || !s_idx || !kv || !ks || !ws) return VS_ERR_ARG;
+  if (B < 1 || H < 1 || N < 64 || N % 64 || size_t(N) > topp_max_n()) return VS_ERR_SHAPE;
+  if (int64_t(B) * H > (int64_t(1) << 31) - 1 || int64_t(B) * H > 65535 * 1024) return VS_ERR_SHAPE;
+  if (!(pv >= 0.0 && pv <= 1.0) || !(ps >= 0.0 && ps <= 1.0)) return VS_ERR_ARG;
+  if (kv_max < 1 || ks_max < 1 || kv_max > N || ks_max > N) return VS_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(v_score) | reinterpret_cast<uintptr_t>(s_score)) & 3u) return VS_ERR_SHAPE;
+  if (ws_bytes < 256) return VS_ERR_WORKSPACE;
+  return launch_select_topp(B, H, N, v_score, s_score, pv, ps, kv_max, ks_max, v_idx, s_idx, kv, ks,
+                            static_cast<int*>(ws), stream);
 }
 
 // --------------------------------------------------------------------- index

@@ -31,6 +31,7 @@ constexpr int kEstThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 compute
 constexpr int kEstCompute = 256;
 constexpr int kEstDiag = 192;      // 191 diagonals (row - key in [-127, 63]) per head and key tile, padded
 constexpr int kTopkThreads = 1024;
+constexpr size_t kToppMaxSmem = size_t(192) << 10;  // pooled slash units: N <= 1,572,864
 
 struct EstLayout {
   int64_t off_part, off_lse, off_vbuf, off_spart, off_sbuf, total;
@@ -421,23 +422,17 @@ __device__ __forceinline__ int block_scan(int x, int* wsum, int* total) {
   return res;
 }
 
-struct TopkParams {
-  const float* score;  // [BH][N] for v, then s
-  const float* score2;
-  int32_t* out;        // [BH][k]
-  int32_t* out2;
-  int N, k, k2;
-};
-
-__global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
-  const int bh = blockIdx.x, which = blockIdx.y;
-  const uint32_t* x = reinterpret_cast<const uint32_t*>(which == 0 ? p.score : p.score2) + int64_t(bh) * p.N;
-  const int k = which == 0 ? p.k : p.k2;
-  int32_t* out = (which == 0 ? p.out : p.out2) + int64_t(bh) * k;
+// Radix select of the k-th largest of N fp32 scores (the bit patterns of
+// nonnegative floats order like their values), then an index-ordered
+// compaction: out[0, k) = the k largest scores' indices, ties to the lower
+// index, ascending; out[k, cap) = -1.  Called by all threads of the block.
+__device__ void topk_block(const uint32_t* x, int N, int k, int32_t* out, int cap) {
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_want;
   __shared__ int wsum[32];
+  for (int i = k + threadIdx.x; i < cap; i += blockDim.x) out[i] = -1;
+  if (k <= 0) return;
   if (threadIdx.x == 0) {
     s_prefix = 0;
     s_want = k;
@@ -447,7 +442,7 @@ __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
     __syncthreads();
     const uint32_t prefix = s_prefix;
     const uint32_t hi_mask = (shift == 24) ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int i = threadIdx.x; i < p.N; i += blockDim.x) {
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
       const uint32_t v = x[i];
       if ((v & hi_mask) == prefix) atomicAdd(&hist[(v >> shift) & 255], 1);
     }
@@ -469,13 +464,13 @@ __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
   const uint32_t kth = s_prefix;
   const int take_eq = s_want;
   int eq_base = 0, out_base = 0;
-  for (int i0 = 0; i0 < p.N; i0 += blockDim.x) {
+  for (int i0 = 0; i0 < N; i0 += blockDim.x) {
     const int i = i0 + threadIdx.x;
-    const uint32_t v = (i < p.N) ? x[i] : 0u;
-    const int is_eq = (i < p.N && v == kth) ? 1 : 0;
+    const uint32_t v = (i < N) ? x[i] : 0u;
+    const int is_eq = (i < N && v == kth) ? 1 : 0;
     int tot;
     const int eq_incl = block_scan(is_eq, wsum, &tot);
-    const int sel = (i < p.N) && (v > kth || (is_eq && eq_base + eq_incl - 1 < take_eq));
+    const int sel = (i < N) && (v > kth || (is_eq && eq_base + eq_incl - 1 < take_eq));
     eq_base += tot;
     int tot2;
     const int pos = block_scan(sel, wsum, &tot2);
@@ -484,11 +479,201 @@ __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
   }
 }
 
+struct TopkParams {
+  const float* score;  // [BH][N] for v, then s
+  const float* score2;
+  int32_t* out;        // [BH][k]
+  int32_t* out2;
+  int N, k, k2;
+};
+
+__global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
+  const int bh = blockIdx.x, which = blockIdx.y;
+  const uint32_t* x = reinterpret_cast<const uint32_t*>(which == 0 ? p.score : p.score2) + int64_t(bh) * p.N;
+  const int k = which == 0 ? p.k : p.k2;
+  topk_block(x, p.N, k, (which == 0 ? p.out : p.out2) + int64_t(bh) * k, k);
+}
+
+// ---------------------------------------------------------------- top-p
+// Top-p budgets (Algorithm 1, `topp` and `Pool`): the budget is the smallest
+// k whose k largest scores carry at least a fraction p of the list's mass.
+// The decision is taken exactly: a score x counts floor(x * 2^40) mass units
+// (integers; their sums do not depend on the order of addition), the target
+// is t = ceil(p * T) for the total T (one rounded double product), and the
+// k-th largest is found by a radix select that tracks unit sums per digit.
+// Scores must be finite and nonnegative with a total below 2^13 (the
+// estimator's total is last_q); otherwise VS_ERR_SCORE and empty lists.
+constexpr double kUnitScale = 1099511627776.0;   // 2^40
+constexpr uint64_t kUnitTotalMax = 1ull << 53;  // totals stay exact as doubles
+constexpr uint64_t kSat = 1ull << 62;
+
+__device__ __forceinline__ uint64_t mass_unit(float x) { return __double2ull_rz(double(x) * kUnitScale); }
+__device__ __forceinline__ uint64_t sat_add(uint64_t a, uint64_t b) {
+  const uint64_t c = a + b;  // a, b <= 2^62: no wrap
+  return c > kSat ? kSat : c;
+}
+
+struct ToppParams {
+  const float* v;  // [BH][N]
+  const float* s;
+  int32_t* v_idx;  // [BH][kv_max]
+  int32_t* s_idx;  // [BH][ks_max]
+  int32_t* kv;     // [BH] budgets (out)
+  int32_t* ks;
+  int* err;
+  int N, kv_max, ks_max;
+  double pv, ps;
+};
+
+struct ToppShared {
+  int cnt[256];
+  uint64_t sum[256];
+  uint64_t red[32];
+  uint64_t prefix, want;
+  int above, bad, k;
+};
+
+// Saturating block sum of one value per thread (values <= 2^62).
+__device__ uint64_t block_sum_sat(uint64_t x, ToppShared& S) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = sat_add(x, __shfl_xor_sync(0xffffffffu, x, off));
+  if (lane == 0) S.red[w] = x;
+  __syncthreads();
+  uint64_t t = 0;
+  for (int i = 0; i < int(blockDim.x >> 5); ++i) t = sat_add(t, S.red[i]);
+  __syncthreads();
+  return t;
+}
+
+// Smallest k in [0, n] with (sum of the k largest units) >= t, for t >= 1 and
+// t <= total.  Keys order the elements like their units: POOLED keys are the
+// units (< 2^53) themselves, otherwise fp32 score bits.
+template <bool POOLED>
+__device__ int topp_count(const uint32_t* x, const uint64_t* pooled, int n, uint64_t t, ToppShared& S) {
+  if (threadIdx.x == 0) {
+    S.prefix = 0;
+    S.want = t;
+    S.above = 0;
+  }
+  for (int shift = POOLED ? 48 : 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+      S.cnt[i] = 0;
+      S.sum[i] = 0;
+    }
+    __syncthreads();
+    const uint64_t hi = S.prefix >> (shift + 8);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t key = POOLED ? pooled[i] : uint64_t(x[i]);
+      if ((key >> (shift + 8)) == hi) {
+        const int dgt = int((key >> shift) & 255);
+        atomicAdd(&S.cnt[dgt], 1);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&S.sum[dgt]),
+                  static_cast<unsigned long long>(POOLED ? key : mass_unit(__uint_as_float(uint32_t(key)))));
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint64_t want = S.want;
+      uint64_t cum = 0;
+      int above = 0, sel = 0;
+      for (int bin = 255; bin >= 0; --bin) {
+        if (cum + S.sum[bin] >= want) {
+          sel = bin;
+          break;
+        }
+        cum += S.sum[bin];
+        above += S.cnt[bin];
+      }
+      S.want = want - cum;  // > 0: the bins above sum to less than want
+      S.above += above;
+      S.prefix |= uint64_t(sel) << shift;
+    }
+    __syncthreads();
+  }
+  // the k-th largest has key S.prefix; the smallest j with j * u >= want of
+  // its copies completes the budget
+  const uint64_t u = POOLED ? S.prefix : mass_unit(__uint_as_float(uint32_t(S.prefix)));
+  const int k = S.above + (u ? int((S.want + u - 1) / u) : 0);
+  __syncthreads();
+  return k < n ? k : n;
+}
+
+// Grid (BH, 2): y = 0 the vertical list, y = 1 the slash list.  Dynamic
+// shared memory: the pooled slash units, one per 64-offset block.
+__global__ void __launch_bounds__(kTopkThreads) est_topp(const ToppParams p) {
+  extern __shared__ __align__(16) uint64_t pooled[];
+  __shared__ ToppShared S;
+  const int bh = blockIdx.x, which = blockIdx.y;
+  const int N = p.N;
+  const float* xf = (which == 0 ? p.v : p.s) + int64_t(bh) * N;
+  const uint32_t* x = reinterpret_cast<const uint32_t*>(xf);
+  if (threadIdx.x == 0) S.bad = 0;
+  __syncthreads();
+  // 1. validate, total mass; the slash list is pooled per 64-offset block
+  uint64_t mine = 0;
+  int bad = 0;
+  if (which == 0) {
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+      const float f = xf[i];
+      if (!(f >= 0.f && f < 8192.f)) bad = 1;
+      else mine = sat_add(mine, mass_unit(f));
+    }
+  } else {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int b = w; b < N / 64; b += nw) {
+      uint64_t u = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float f = xf[64 * b + 32 * h + lane];
+        if (!(f >= 0.f && f < 8192.f)) bad = 1;
+        else u += mass_unit(f);  // < 2^54 for two scores below 2^13
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) u = sat_add(u, __shfl_xor_sync(0xffffffffu, u, off));
+      if (lane == 0) pooled[b] = u;
+      mine = sat_add(mine, lane == 0 ? u : 0ull);
+    }
+  }
+  if (bad) S.bad = 1;
+  const uint64_t T = block_sum_sat(mine, S);  // its syncs also publish S.bad and pooled[]
+  const bool ok = !S.bad && T < kUnitTotalMax;
+  // 2. budget
+  int k = 0;
+  if (ok) {
+    const double prod = (which == 0 ? p.pv : p.ps) * double(T);
+    const uint64_t t = uint64_t(ceil(prod));
+    if (t > 0) k = which == 0 ? topp_count<false>(x, nullptr, N, t, S) : topp_count<true>(nullptr, pooled, N / 64, t, S);
+  } else if (threadIdx.x == 0) {
+    raise_error(p.err, VS_ERR_SCORE);
+  }
+  const int cap = which == 0 ? p.kv_max : p.ks_max;
+  if (which == 1) k = min(64 * k, N);
+  k = min(k, cap);
+  if (threadIdx.x == 0) (which == 0 ? p.kv : p.ks)[bh] = k;
+  // 3. the k largest at token level, padded to the list capacity
+  topk_block(x, N, k, (which == 0 ? p.v_idx : p.s_idx) + int64_t(bh) * cap, cap);
+}
+
+size_t topp_smem_bytes(int N) { return size_t(N / 64) * sizeof(uint64_t); }
+
+vs_status launch_topp(const ToppParams& tp, int BH, cudaStream_t st) {
+  const size_t sm = topp_smem_bytes(tp.N);
+  if (sm > kToppMaxSmem) return VS_ERR_SHAPE;
+  if (cudaFuncSetAttribute(est_topp, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)) != cudaSuccess)
+    return VS_ERR_CUDA;
+  trace_begin("est_topp", st);
+  est_topp<<<dim3(BH, 2), kTopkThreads, sm, st>>>(tp);
+  trace_end(st);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
 // The estimator's kernels on the given scratch (p.part / lse / spart and the
 // score outputs set by the caller).
 template <int D>
 vs_status launch_est_kernels(const vs_shape* s, const void* q, const void* k, EstParams& p, int kv, int ks,
-                             int32_t* v_idx, int32_t* s_idx, cudaStream_t st) {
+                             int32_t* v_idx, int32_t* s_idx, ToppParams* topp, cudaStream_t st) {
   CUtensorMap tq, tk;
   vs_status rc;
   if ((rc = make_tmap_bshd(&tq, q, s->B, s->Nq, s->Hq, D, s->sq, kLastQ)) != VS_OK) return rc;
@@ -511,6 +696,13 @@ vs_status launch_est_kernels(const vs_shape* s, const void* q, const void* k, Es
   trace_begin("est_scombine", st);
   est_scombine<<<dim3((s->Nk + 255) / 256, BH), 256, 0, st>>>(p);
   trace_end(st);
+  if (topp) {
+    topp->v = p.v;
+    topp->s = p.s;
+    topp->err = p.err;
+    note_launch(4);
+    return launch_topp(*topp, BH, st);
+  }
   TopkParams tp;
   tp.score = p.v;
   tp.score2 = p.s;
@@ -541,15 +733,61 @@ EstParams est_params(const vs_shape* s, float scale, int* err) {
 }
 
 vs_status launch_est(const vs_shape* s, const void* q, const void* k, EstParams& p, int kv, int ks, int32_t* v_idx,
-                     int32_t* s_idx, cudaStream_t st) {
-  if (s->d == 128) return launch_est_kernels<128>(s, q, k, p, kv, ks, v_idx, s_idx, st);
-  if (s->d == 64) return launch_est_kernels<64>(s, q, k, p, kv, ks, v_idx, s_idx, st);
+                     int32_t* s_idx, cudaStream_t st, ToppParams* topp = nullptr) {
+  if (topp && topp_smem_bytes(s->Nk) > kToppMaxSmem) return VS_ERR_SHAPE;
+  if (s->d == 128) return launch_est_kernels<128>(s, q, k, p, kv, ks, v_idx, s_idx, topp, st);
+  if (s->d == 64) return launch_est_kernels<64>(s, q, k, p, kv, ks, v_idx, s_idx, topp, st);
   return VS_ERR_SHAPE;
 }
 
 }  // namespace
 
 size_t estimate_workspace_bytes(const vs_shape* s, int) { return size_t(est_layout(s).total); }
+
+size_t topp_max_n() { return kToppMaxSmem / sizeof(uint64_t) * 64; }
+
+vs_status launch_estimate_topp(const vs_shape* s, const void* q, const void* k, double pv, double ps, int kv_max,
+                               int ks_max, float scale, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks,
+                               float* v_score, float* s_score, void* ws, cudaStream_t st) {
+  const EstLayout L = est_layout(s);
+  uint8_t* W = static_cast<uint8_t*>(ws);
+  EstParams p = est_params(s, scale, static_cast<int*>(ws));
+  p.part = reinterpret_cast<float2*>(W + L.off_part);
+  p.lse = reinterpret_cast<float*>(W + L.off_lse);
+  p.v = v_score ? v_score : reinterpret_cast<float*>(W + L.off_vbuf);
+  p.spart = reinterpret_cast<float*>(W + L.off_spart);
+  p.s = s_score ? s_score : reinterpret_cast<float*>(W + L.off_sbuf);
+  ToppParams tp{};
+  tp.v_idx = v_idx;
+  tp.s_idx = s_idx;
+  tp.kv = kv;
+  tp.ks = ks;
+  tp.N = s->Nk;
+  tp.kv_max = kv_max;
+  tp.ks_max = ks_max;
+  tp.pv = pv;
+  tp.ps = ps;
+  return launch_est(s, q, k, p, kv_max, ks_max, v_idx, s_idx, st, &tp);
+}
+
+vs_status launch_select_topp(int B, int H, int N, const float* v_score, const float* s_score, double pv, double ps,
+                             int kv_max, int ks_max, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks,
+                             int* err, cudaStream_t st) {
+  ToppParams tp{};
+  tp.v = v_score;
+  tp.s = s_score;
+  tp.v_idx = v_idx;
+  tp.s_idx = s_idx;
+  tp.kv = kv;
+  tp.ks = ks;
+  tp.err = err;
+  tp.N = N;
+  tp.kv_max = kv_max;
+  tp.ks_max = ks_max;
+  tp.pv = pv;
+  tp.ps = ps;
+  return launch_topp(tp, B * H, st);
+}
 
 vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, int kv, int ks, float scale,
                           int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,

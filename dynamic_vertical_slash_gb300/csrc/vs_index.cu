@@ -68,18 +68,20 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   const int64_t NG = H.N_global;
   const int W = H.world;
 
-  __shared__ int bad;
+  __shared__ int bad, nks;
   __shared__ int part[kIdxThreads + 1];
-  if (tid == 0) bad = 0;
+  if (tid == 0) bad = nks = 0;
   __syncthreads();
-  // 1. validate: strictly ascending, inside [0, N_global)
+  // 1. validate: strictly ascending inside [0, N_global), then only -1 (a
+  // budget below the list's capacity); nks = the slash entries in use
   for (int i = tid; i < H.kv; i += kIdxThreads) {
     const int x = iv[i];
-    if (x < 0 || x >= NG || (i > 0 && iv[i - 1] >= x)) bad = 1;
+    if (x < -1 || x >= NG || (x >= 0 && i > 0 && !(iv[i - 1] >= 0 && iv[i - 1] < x))) bad = 1;
   }
   for (int i = tid; i < H.ks; i += kIdxThreads) {
     const int x = is[i];
-    if (x < 0 || x >= NG || (i > 0 && is[i - 1] >= x)) bad = 1;
+    if (x < -1 || x >= NG || (x >= 0 && i > 0 && !(is[i - 1] >= 0 && is[i - 1] < x))) bad = 1;
+    if (x >= 0) atomicAdd(&nks, 1);
   }
   // 2. clear bitmaps
   for (int w = tid; w < H.WG; w += kIdxThreads) offbits[w] = colbits[w] = 0ull;
@@ -100,10 +102,11 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   // 3. bitmaps
   for (int i = tid; i < H.ks; i += kIdxThreads) {
     const int x = is[i];
-    atomicOr(reinterpret_cast<unsigned long long*>(offbits + (x >> 6)), 1ull << (x & 63));
+    if (x >= 0) atomicOr(reinterpret_cast<unsigned long long*>(offbits + (x >> 6)), 1ull << (x & 63));
   }
   for (int i = tid; i < H.kv; i += kIdxThreads) {
     const int x = iv[i];
+    if (x < 0) continue;
     atomicOr(reinterpret_cast<unsigned long long*>(colbits + (x >> 6)), 1ull << (x & 63));
     const int blk = x >> 6;
     if (blk % W == H.kv_rank) {
@@ -153,8 +156,8 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
       int64_t cur = 0;
       int j = 0;
       while (true) {
-        while (j < H.ks && is[j] < cur - 127) ++j;
-        if (j == H.ks) break;
+        while (j < nks && is[j] < cur - 127) ++j;
+        if (j == nks) break;
         const int64_t u = max(cur, int64_t(is[j]));
         if (u > int64_t(H.Nq) + 126 || ne >= H.EMAX) break;
         elist[ne] = int32_t(u);

@@ -33,6 +33,13 @@ vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int l
                           int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
                           cudaStream_t st);
 size_t estimate_workspace_bytes(const vs_shape* s, int last_q);
+vs_status launch_estimate_topp(const vs_shape* s, const void* q, const void* k, double pv, double ps, int kv_max,
+                               int ks_max, float scale, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks,
+                               float* v_score, float* s_score, void* ws, cudaStream_t st);
+vs_status launch_select_topp(int B, int H, int N, const float* v_score, const float* s_score, double pv, double ps,
+                             int kv_max, int ks_max, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks,
+                             int* err, cudaStream_t st);
+size_t topp_max_n();
 vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                        const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t st);
 size_t index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* stripe, ArenaHeader* hdr_out);

@@ -50,7 +50,8 @@ typedef enum {
   VS_ERR_WORKSPACE = 3, /* workspace or index arena too small */
   VS_ERR_INDEX = 4,     /* (device) index list out of range, unsorted or duplicated */
   VS_ERR_TIMEOUT = 5,   /* (device) a bounded wait ran out */
-  VS_ERR_CUDA = 6       /* CUDA runtime error while encoding or launching */
+  VS_ERR_CUDA = 6,      /* CUDA runtime error while encoding or launching */
+  VS_ERR_SCORE = 7      /* (device) a score is negative, not finite, or the list's total is >= 2^13 */
 } vs_status;
 
 /* Problem shape.  Nq / Nk are the local query / key lengths (equal unless a
@@ -99,6 +100,45 @@ vs_status vs_estimate(const vs_shape* shape, const void* q, const void* k, int l
                       cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * vs_estimate_topp / vs_select_topp -- top-p budgets (Algorithm 1, the
+ * `topp` and `Pool` lines; section 4.1 (i) online budget approximation and
+ * (ii) kernel-aware granularity).
+ *
+ * Instead of fixed kv / ks, each (b, h) gets the smallest budgets that
+ * recall a fraction of its observed attention mass:
+ *   kv = min(topp(v, pv), kv_max)
+ *   ks = min(64 * topp(Pool(s, 64), ps), ks_max, N)
+ * where topp(x, p) is the smallest k whose k largest entries of x sum to at
+ * least p * sum(x), and Pool sums 64 consecutive slash offsets (the slash
+ * tiles are 64 x 64 blocks).  Then v_idx = argtopk(v, kv) and s_idx =
+ * argtopk(s, ks) as in vs_estimate.  The decision is exact and reproducible:
+ * a score x counts floor(x * 2^40) integer mass units, the target is
+ * ceil(p * T) for the unit total T (one double product), and the budget is
+ * the smallest k whose k largest unit counts reach it.
+ *
+ *   pv, ps        fractions in [0, 1]
+ *   kv_max/ks_max list capacities, 1..N
+ *   v_idx         int32 [B][Hq][kv_max] (out): the kv selected columns,
+ *                 ascending, then -1
+ *   s_idx         int32 [B][Hq][ks_max] (out): the ks selected offsets,
+ *                 ascending, then -1
+ *   kv, ks        int32 [B][Hq] device (out): the budgets
+ * vs_estimate_topp takes the remaining arguments of vs_estimate (same
+ * workspace).  vs_select_topp runs the budget and selection step alone on
+ * given scores (fp32 [B][H][N], device): ws is a device buffer of at least
+ * 256 bytes whose first word is the status word.
+ * Limits: N <= 1,572,864.  Device errors: VS_ERR_SCORE (that head's lists
+ * are then empty and its budgets 0).
+ * ------------------------------------------------------------------------- */
+vs_status vs_estimate_topp(const vs_shape* shape, const void* q, const void* k, int last_q, double pv, double ps,
+                           int kv_max, int ks_max, float scale, int32_t* v_idx, int32_t* s_idx, int32_t* kv,
+                           int32_t* ks, float* v_score, float* s_score, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+vs_status vs_select_topp(int B, int H, int N, const float* v_score, const float* s_score, double pv, double ps,
+                         int kv_max, int ks_max, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks, void* ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * vs_estimate_noalloc -- vs_estimate without a caller workspace.  (The paper
  * has no counterpart: this is a deployment convenience of this library.)
  *
@@ -137,6 +177,8 @@ vs_status vs_estimate_noalloc(const vs_shape* shape, const void* q, const void* 
  *
  * Turns the selected columns (v_idx, global, sorted) and diagonals (s_idx,
  * global offsets n - m, sorted) into the arena the attention kernels read.
+ * A list may end in entries equal to -1 (a top-p budget below the list's
+ * capacity); they select nothing, and a list of only -1 is empty.
  * The mask it encodes is exact at token level:
  *     M[n, m] = (m <= n) and (m in v_idx or n - m in s_idx)
  * on global positions.  It is covered by
@@ -153,8 +195,9 @@ vs_status vs_estimate_noalloc(const vs_shape* shape, const void* q, const void* 
  *   v_idx  int32 [B][Hq][kv]; s_idx int32 [B][Hq][ks] (device)
  *   arena  device buffer of at least vs_block_index_bytes() bytes; fully
  *          rewritten by this call
- * Device errors: VS_ERR_INDEX when a list is out of range, unsorted or has
- * duplicates (the arena then describes an empty mask).
+ * Device errors: VS_ERR_INDEX when a list is out of range, unsorted, has
+ * duplicates, or has an entry after a -1 (the arena then describes an empty
+ * mask).
  * ------------------------------------------------------------------------- */
 size_t vs_block_index_bytes(const vs_shape* shape, int kv, int ks, const vs_stripe* stripe);
 vs_status vs_build_block_index(const vs_shape* shape, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,

@@ -236,3 +236,27 @@ def small_workload(N: int, Hq: int, Hkv: int, d: int, kv: int, ks: int, seed: in
     return Workload(f"N{N}-H{Hq}x{Hkv}-d{d}", N=N, Hq=Hq, Hkv=Hkv, d=d, kv=kv, ks=ks,
                     seqs=[SeqSpec(seed=seed + i, n_out=n_out, n_slash=n_slash, band=band) for i in range(B)],
                     last_q=last_q, world=world)
+
+
+def score_lists(B: int, H: int, N: int, seed: int, total: float = 64.0):
+    """Seeded synthetic vertical / slash score lists, float32 [B, H, N] each,
+    shaped like an observation window's column and diagonal sums (each list
+    sums to about ``total``, the window length): vertical scores are a
+    heavy (Pareto) tail with a sink at column 0 and a few outlier columns;
+    slash scores decay with the offset (a local band) plus a few planted
+    diagonals and a tail.  A draw of inputs for the selection step, no part
+    of the method."""
+    rng = np.random.default_rng(seed)
+    v = rng.pareto(1.2, (B, H, N)) + 1e-3
+    v[:, :, 0] += 0.2 * N
+    for b in range(B):
+        for h in range(H):
+            v[b, h, rng.choice(N, 8, replace=False)] += rng.uniform(0.01, 0.05) * N
+    o = np.arange(N, dtype=np.float64)
+    s = rng.pareto(1.5, (B, H, N)) * 0.05 + 50.0 / (1.0 + o / 16.0) ** 2
+    for b in range(B):
+        for h in range(H):
+            s[b, h, rng.choice(N, 6, replace=False)] += rng.uniform(0.5, 3.0) * s[b, h].mean() * 20
+    v *= total / v.sum(-1, keepdims=True)
+    s *= total / s.sum(-1, keepdims=True)
+    return v.astype(np.float32), s.astype(np.float32)

@@ -47,7 +47,7 @@ def _shape(B=1, N=1024, Hq=2, Hkv=1, d=64):
 
 
 def test_status_strings(L):
-    for code in range(7):
+    for code in range(8):
         assert L.vs_status_string(code)
     assert b"VS_ERR_SHAPE" in L.vs_status_string(2)
 
