@@ -3,7 +3,7 @@
 //   bwd_prep     D_n = rowsum(dO_n * O_n) and LSE in log2 units, per row.
 //   dq kernel    query-major, one CTA per (b, h, 128-row tile), same units as
 //                the forward: S = Q K^T, dP = dO V^T, dS = P (dP - D),
-//                dQ += dS K (A operand dS read from TMEM).
+//                dQ += dS K; Q, dO and dS are A operands read from TMEM.
 //   bar kernel   key-major over gathered selected columns, one CTA per
 //                (b, h, 128-column chunk, row split): S^T = K Q^T,
 //                dP^T = V dO^T, dV += P^T dO, dK += dS^T Q over 64-row units
@@ -134,20 +134,23 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
 }
 
 // ---------------------------------------------------------------- dQ kernel
-// TMEM: dQ [0, 128), S and dP double-buffered [128, 256) / [256, 384), dS
-// (bf16, double-buffered) [384, 448), dO (bf16, the A operand of dP, loaded
-// once per tile) [448, 512).
-constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColDS = 384, kDqColDO = 448;
+// TMEM: dQ [0, 128), S and dP double-buffered [128, 256) / [256, 384), Q
+// (bf16, the A operand of S) [384, 448), dO (bf16, the A operand of dP)
+// [448, 512); Q and dO are loaded once per tile.  dS (bf16) is written over
+// its unit's S buffer: the warp that read S columns [32h, 32h + 32) writes
+// dS columns [32h, 32h + 16).  MMAs run in issue order, so S of unit j + 2
+// (same buffer) is issued after dQ of unit j has read dS, and no extra
+// barrier guards the reuse.
+constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColQ = 384, kDqColDO = 448;
 
 template <int D>
 struct DqSmem {
   static constexpr int NH = D / 64;
-  uint8_t q[NH][kQTile * 128];
   uint8_t k[kBwdStages][NH][kKTile * 128];
   uint8_t v[kBwdStages][NH][kKTile * 128];
-  uint64_t q_full, do_full;
+  uint64_t qdo_full;
   uint64_t kv_full[kBwdStages], kv_empty[kBwdStages];
-  uint64_t s_full[2], s_free[2], ds_full[2], ds_done[2];
+  uint64_t s_full[2], ds_full[2];
   uint64_t fin, teardown;
   uint64_t mask[kBwdStages][kQTile];  // per-stage row masks, written by the producer
   int64_t bar_keys[kKTile];           // producer: a bar chunk's key positions
@@ -191,8 +194,8 @@ __device__ __forceinline__ void unit_row_masks(uint64_t* out, int64_t* scratch, 
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
+    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const BwdParams p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,17 +226,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int U = nslash + nbar;
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
-    mbar_init(&s.q_full, 1);
-    mbar_init(&s.do_full, kBwdCompute);
+    mbar_init(&s.qdo_full, kBwdCompute);
     for (int i = 0; i < kBwdStages; ++i) {
       mbar_init(&s.kv_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], kBwdCompute);
       mbar_init(&s.ds_full[i], kBwdCompute);
-      mbar_init(&s.ds_done[i], 1);
     }
     mbar_init(&s.fin, 1);
     mbar_init(&s.teardown, 1);
@@ -254,10 +254,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int issued[kBwdStages];
     for (int i = 0; i < kBwdStages; ++i) issued[i] = -1;
     if (U > 0) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
-        for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
-      }
       const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
       const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
       for (int j = 0; j < U; ++j) {
@@ -301,20 +297,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && U > 0) {
       const uint32_t idS = idesc_bf16(128, 64, 0, 0);
       const uint32_t idQ = idesc_bf16(128, D, 0, 1);
-      bool ok = mbar_wait(&s.q_full, 0, ab, VS_ERR_TIMEOUT) && mbar_wait(&s.do_full, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait(&s.qdo_full, 0, ab, VS_ERR_TIMEOUT);
+      // Order: S_0 dP_0, then per j: S_j dP_j, dQ += dS_{j-1} K.  S_j reuses
+      // the buffer of unit j - 2, whose dS the dQ MMA issued before it reads.
       for (int j = 0; ok && j <= U; ++j) {
         if (j < U) {
           const int st = j % kBwdStages;
           if (!(ok = mbar_wait(&s.kv_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
           if (j >= nslash) fence_proxy_async_smem();
-          if (j >= 2 && !(ok = mbar_wait(&s.s_free[j & 1], ((j - 2) >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ss(tmem + kDqColS + (j & 1) * 64, dq_, dk_, idS, kk > 0);
+            mma_ts(tmem + kDqColS + (j & 1) * 64, tmem + kDqColQ + kk * 8, dk_, idS, kk > 0);
             mma_ts(tmem + kDqColDP + (j & 1) * 64, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
           }
           mma_issued = true;
@@ -327,9 +323,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kKTile / 16; ++kk) {
             const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][0]) + kk * 2048, kKTile * 128, 1024);
-            mma_ts(tmem + kDqColAcc, tmem + kDqColDS + (jj & 1) * 32 + kk * 8, dk_, idQ, (jj > 0 || kk > 0));
+            const uint32_t a_ds = tmem + kDqColS + (jj & 1) * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+            mma_ts(tmem + kDqColAcc, a_ds, dk_, idQ, (jj > 0 || kk > 0));
           }
-          mma_commit(&s.ds_done[jj & 1]);
           mma_commit(&s.kv_empty[st]);
         }
       }
@@ -348,10 +344,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       Lr = reinterpret_cast<const float*>(p.ws + L.off_l2)[int64_t(bh) * p.Nq + n_loc];
       Dr = reinterpret_cast<const float*>(p.ws + L.off_d)[int64_t(bh) * p.Nq + n_loc];
     }
-    {
-      // dO row r, d columns [half D/2, (half + 1) D/2), into TMEM as bf16 pairs
+    // Q row r and dO row r, d columns [half D/2, (half + 1) D/2), into TMEM
+    // as bf16 pairs
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
       uint32_t w[D / 4];
-      const uint8_t* src = p.dO + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(h) * p.so[2]) * 2 + half * D;
+      const uint8_t* src =
+          which ? p.dO + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(h) * p.so[2]) * 2 + half * D
+                : p.q + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(h) * p.sq[2]) * 2 + half * D;
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
         const uint4 x = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
@@ -360,13 +360,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         w[4 * c + 2] = x.z;
         w[4 * c + 3] = x.w;
       }
+      const uint32_t col = (which ? kDqColDO : kDqColQ) + half * (D / 4);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
-        tmem_st16(tl + kDqColDO + half * (D / 4) + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&s.do_full);
+        tmem_st16(tl + col + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c]));
     }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&s.qdo_full);
     bool ok = true;
     for (int j = 0; j < U; ++j) {
       ok = mbar_wait(&s.s_full[j & 1], (j >> 1) & 1, ab, VS_ERR_TIMEOUT);
@@ -379,8 +380,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32(tl + kDqColS + (j & 1) * 64 + 32 * half, sr);
       tmem_ld32(tl + kDqColDP + (j & 1) * 64 + 32 * half, pr);
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&s.s_free[j & 1]);
       // masks written by the producer before it released the stage
       const int st = j % kBwdStages;
       ok = mbar_wait(&s.kv_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT);
@@ -402,13 +401,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         pk[i] = pack_bf16x2(ds[0], ds[1]);
       }
-      if (j >= 2) ok = mbar_wait(&s.ds_done[j & 1], ((j - 2) >> 1) & 1, ab, VS_ERR_TIMEOUT);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st16(tl + kDqColDS + (j & 1) * 32 + 16 * half, pk);
+      // over this warp's own S columns (read above): dQ of unit j - 2, the
+      // last reader of this buffer's previous dS, completed before S_j did
+      tmem_st16(tl + kDqColS + (j & 1) * 64 + 32 * half, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ds_full[j & 1]);
@@ -989,10 +984,8 @@ BwdParams make_params(const vs_shape* sh, const void* q, const void* k, const vo
 
 template <int D>
 vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, cudaStream_t st) {
-  CUtensorMap tq128, tg128, tk64, tv64, tk128, tv128, tq64, tg64;
+  CUtensorMap tk64, tv64, tk128, tv128, tq64, tg64;
   vs_status rc;
-  if ((rc = make_tmap_bshd(&tq128, p.q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile)) != VS_OK) return rc;
-  if ((rc = make_tmap_bshd(&tg128, p.dO, sh->B, sh->Nq, sh->Hq, D, sh->so, kQTile)) != VS_OK) return rc;
   if ((rc = make_tmap_bshd(&tk64, p.k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kKTile)) != VS_OK) return rc;
   if ((rc = make_tmap_bshd(&tv64, p.v, sh->B, sh->Nk, sh->Hkv, D, sh->sv, kKTile)) != VS_OK) return rc;
   if ((rc = make_tmap_bshd(&tk128, p.k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kBarK)) != VS_OK) return rc;
@@ -1028,7 +1021,7 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   trace_begin("bwd_dq", st);
-  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tq128, tk64, tv64, p);
+  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tk64, tv64, p);
   trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;

@@ -52,12 +52,19 @@ class VSAttention:
 
     forward(q, k, v) -> (o, lse) and backward(dO) -> (dq, dk, dv) run the
     estimator, the index build and the sparse kernels with fixed budgets
-    kv / ks.  All tensors are BSHD bf16 on the device.
+    kv / ks, or, when ``pv`` and ``ps`` are given, with per-head top-p
+    budgets (Algorithm 1) of at most kv / ks entries (``budgets`` then holds
+    the [B, Hq] budgets of the last forward).  All tensors are BSHD bf16 on
+    the device.
     """
 
     def __init__(self, B: int, N: int, Hq: int, Hkv: int, d: int, kv: int, ks: int,
-                 device="cuda", last_q: int = 64, scale: Optional[float] = None):
+                 device="cuda", last_q: int = 64, scale: Optional[float] = None,
+                 pv: Optional[float] = None, ps: Optional[float] = None):
         self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N, Hq, Hkv, d, kv, ks
+        if (pv is None) != (ps is None):
+            raise ValueError("top-p mode needs both pv and ps")
+        self.pv, self.ps = pv, ps
         self.last_q = last_q
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         dev = torch.device(device)
@@ -81,13 +88,20 @@ class VSAttention:
         self.dk = torch.empty_like(k0)
         self.dv = torch.empty_like(k0)
         self.ws_bwd = torch.zeros(L.vs_attn_bwd_workspace(ctypes.byref(sh), kv), dtype=torch.uint8, device=dev)
+        self.budgets = (torch.zeros(B, Hq, dtype=torch.int32, device=dev),
+                        torch.zeros(B, Hq, dtype=torch.int32, device=dev)) if pv is not None else None
         self._qkv = None
 
     def forward(self, q, k, v, stream=None, selection=None):
         """Estimate, index, sparse forward.  ``selection`` = (v_idx, s_idx)
-        int32 device tensors [B, Hq, kv] / [B, Hq, ks] (sorted ascending)
-        replaces the estimator, e.g. to reuse one layer's selection."""
-        if selection is None:
+        int32 device tensors [B, Hq, kv] / [B, Hq, ks] (sorted ascending,
+        optionally ending in -1) replaces the estimator, e.g. to reuse one
+        layer's selection."""
+        if selection is None and self.pv is not None:
+            B_.vs_estimate_topp(q, k, self.pv, self.ps, self.kv, self.ks, self.scale, self.last_q, self.v_idx,
+                                self.s_idx, self.budgets[0], self.budgets[1], self.v_score, self.s_score, self.ws_est,
+                                stream)
+        elif selection is None:
             B_.vs_estimate(q, k, self.kv, self.ks, self.scale, self.last_q, self.v_idx, self.s_idx, self.v_score,
                            self.s_score, self.ws_est, stream)
         else:

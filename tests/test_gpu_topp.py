@@ -198,3 +198,30 @@ def test_index_padding_rules(vs):
         arena = vs.vs_build_block_index(q, k, torch.tensor([[bad, bad]], dtype=torch.int32, device="cuda"), is_)
         torch.cuda.synchronize()
         assert vs.vs_check_status(arena) == VS_ERR_INDEX
+
+
+def test_vsattention_topp_mode(vs):
+    """The layer object in top-p mode: its budgets and lists replay through
+    the oracle's selection on its own scores, and a forward / backward on
+    the oracle's selection (passed in) matches the oracle."""
+    w, x = make_inputs(1, 2048, 4, 2, 128, seed=35, n_out=5, n_slash=4)
+    layer = vs.VSAttention(1, 2048, 4, 2, 128, 600, 1024, pv=0.85, ps=0.7)
+    q, k, v = dev_bf16(x["q"]), dev_bf16(x["k"]), dev_bf16(x["v"])
+    layer.forward(q, k, v)
+    layer.backward(dev_bf16(x["dout"]))
+    torch.cuda.synchronize()
+    layer.check()
+    got = [layer.v_idx.cpu().numpy(), layer.s_idx.cpu().numpy(), layer.budgets[0].cpu().numpy(),
+           layer.budgets[1].cpu().numpy()]
+    _assert_same(got, oracle.select_topp(layer.v_score.cpu().numpy(), layer.s_score.cpu().numpy(), 0.85, 0.7, 600,
+                                         1024))
+    v_ref, s_ref = oracle.estimate(host_f64(x["q"]), host_f64(x["k"]), 64, w.scale)
+    iv, is_, _, _ = oracle.select_topp(v_ref, s_ref, 0.85, 0.7, 600, 1024)
+    o, lse = layer.forward(q, k, v, selection=(torch.from_numpy(iv).cuda(), torch.from_numpy(is_).cuda()))
+    dq, dk, dv = layer.backward(dev_bf16(x["dout"]))
+    torch.cuda.synchronize()
+    layer.check()
+    ref = oracle.attention(oracle.Problem(host_f64(x["q"]), host_f64(x["k"]), host_f64(x["v"]), iv, is_, w.scale,
+                                          dout=host_f64(x["dout"])))
+    for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert rel_l2(host_f64(t), ref[name]) <= 1e-2, name
