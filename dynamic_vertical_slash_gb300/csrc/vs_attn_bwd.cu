@@ -1,9 +1,9 @@
 // Sparse attention backward on the Vertical-Slash mask (tcgen05 / TMEM / TMA).
 //
 //   bwd_prep     D_n = rowsum(dO_n * O_n) and LSE in log2 units, per row.
-//   dq kernel    query-major, one CTA per (b, h, 128-row tile), same units as
-//                the forward: S = Q K^T, dP = dO V^T, dS = P (dP - D),
-//                dQ += dS K; Q, dO and dS are A operands read from TMEM.
+//   dq kernel    query-major, one CTA per (b, h, 128-row tile), the forward's
+//                units two at a time: S = Q K^T, dP = dO V^T (N = 128),
+//                dS = P (dP - D), dQ += dS K.
 //   bar kernel   key-major over gathered selected columns, one CTA per
 //                (b, h, 128-column chunk, row split): S^T = K Q^T,
 //                dP^T = V dO^T, dV += P^T dO, dK += dS^T Q over 64-row units
@@ -134,69 +134,60 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
 }
 
 // ---------------------------------------------------------------- dQ kernel
-// TMEM: dQ [0, 128), S and dP double-buffered [128, 256) / [256, 384), Q
-// (bf16, the A operand of S) [384, 448), dO (bf16, the A operand of dP)
-// [448, 512); Q and dO are loaded once per tile.  dS (bf16) is written over
-// its unit's S buffer: the warp that read S columns [32h, 32h + 32) writes
-// dS columns [32h, 32h + 16).  MMAs run in issue order, so S of unit j + 2
-// (same buffer) is issued after dQ of unit j has read dS, and no extra
-// barrier guards the reuse.
+// One CTA per (b, h, 128-row query tile) walks the forward's units two at a
+// time (a pair: 128 keys, the two units' 64-key blocks stacked):
+//   S = Q K^T and dP = dO V^T as M=128, N=128 MMA chains, A (Q, dO) in TMEM;
+//   dS = P (dP - D) on the exact mask, written to shared memory (bf16);
+//   dQ += dS K over the pair's 128 keys (A = dS, B = K, both in shared memory).
+// The compute warps copy S and dP of a pair into registers and release the
+// TMEM at once, so the next pair's S / dP run while they compute dS.  Each
+// compute thread builds its own row's mask of its unit (slash: a window of
+// the offset bitmap; bar: a count of the unit's keys at or before the row).
+// TMEM: dQ [0, 128), S [128, 256), dP [256, 384), Q [384, 448), dO [448, 512).
 constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColQ = 384, kDqColDO = 448;
+constexpr int kDqPairKeys = 2 * kKTile;
+constexpr int kDqKSlots = 3, kDqVSlots = 2;
 
 template <int D>
 struct DqSmem {
   static constexpr int NH = D / 64;
-  uint8_t k[kBwdStages][NH][kKTile * 128];
-  uint8_t v[kBwdStages][NH][kKTile * 128];
+  uint8_t k[kDqKSlots][NH][kDqPairKeys * 128];  // K of a pair, 128B-swizzled, per d-half
+  uint8_t v[kDqVSlots][NH][kDqPairKeys * 128];
+  uint8_t ds[2][kQTile * 128];                   // dS of a pair, keys [0, 64) and [64, 128), K-major SW128
+  int64_t bar_pos[kDqKSlots][2][kKTile];         // bar units: global key positions (INT64_MAX = none)
+  int64_t unit_c[kDqKSlots][2];                  // slash: first local key; bar: kUnitBar; none: kUnitNone
   uint64_t qdo_full;
-  uint64_t kv_full[kBwdStages], kv_empty[kBwdStages];
-  uint64_t s_full[2], ds_full[2];
+  uint64_t k_full[kDqKSlots], k_empty[kDqKSlots], v_full[kDqVSlots], v_empty[kDqVSlots];
+  uint64_t s_full, s_free, ds_full, ds_done;
   uint64_t fin, teardown;
-  uint64_t mask[kBwdStages][kQTile];  // per-stage row masks, written by the producer
-  int64_t bar_keys[kKTile];           // producer: a bar chunk's key positions
   uint32_t tmem_base;
   int abort_flag;
 };
+constexpr int64_t kUnitBar = INT64_MIN, kUnitNone = INT64_MIN + 1;
 
-// Row masks of one query-major unit (128 rows), written by the producer warp:
-// slash tiles cut from the offset / column bitmaps (one memory round trip per
-// unit), bar chunks as the prefix of the chunk's ascending keys at or before
-// each row (binary search over the keys' positions in `scratch`).
-__device__ __forceinline__ void unit_row_masks(uint64_t* out, int64_t* scratch, const Geo& G, const ArenaView& av,
-                                               int64_t bh, int t, int Nq, bool slash, int64_t c,
-                                               const int32_t* keys, int lane) {
-  uint64_t m[kQTile / 32];
-  if (slash) {
-    slash_tile_masks(G, av.offbits + bh * G.WG, av.colbits + bh * G.WG, t, c, Nq, lane, m);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = __ldg(keys + e * 32 + lane);
-      scratch[e * 32 + lane] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
-    }
-    __syncwarp();
-#pragma unroll
-    for (int rr = 0; rr < kQTile / 32; ++rr) {
-      const int64_t nl = int64_t(t) * kQTile + rr * 32 + lane;
-      const int64_t ng = qpos_g(G, nl);
-      int pos = 0;
-#pragma unroll
-      for (int step = 32; step > 0; step >>= 1)
-        if (scratch[pos + step - 1] <= ng) pos += step;
-      const int cnt = (scratch[kKTile - 1] <= ng) ? kKTile : pos;
-      m[rr] = nl < Nq ? (cnt == kKTile ? ~0ull : ((1ull << cnt) - 1)) : 0ull;
-    }
-    __syncwarp();
+// Loads the K (which = 0) or V rows of unit u into half `hf` of a pair slot
+// (TMA for slash units, a cp.async gather for bar units); returns the bytes the
+// TMA will deliver.  All 32 lanes call it; lane 0 issues the TMA.
+template <int D>
+__device__ __forceinline__ int dq_load_unit(uint8_t (*slot)[kDqPairKeys * 128], int hf, uint64_t* bar,
+                                            const CUtensorMap* tm, const uint8_t* base, int64_t s_tok,
+                                            const int32_t* vlist, int u, int nslash, int64_t c, int hk, int b,
+                                            int lane) {
+  constexpr int NH = D / 64;
+  if (u < nslash) {
+    if (lane == 0)
+      for (int h = 0; h < NH; ++h) tma_load_4d(slot[h] + hf * kKTile * 128, tm, bar, 64 * h, hk, int(c), b);
+    return NH * kKTile * 128;
   }
-#pragma unroll
-  for (int rr = 0; rr < kQTile / 32; ++rr) out[rr * 32 + lane] = m[rr];
+  gather_rows<D>(smem_u32(slot[0]) + hf * kKTile * 128, kDqPairKeys, base, s_tok, vlist + (u - nslash) * kKTile,
+                 kKTile, lane);
+  return 0;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const BwdParams p) {
-  constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -224,17 +215,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     nbar = lo;
   }
   const int U = nslash + nbar;
+  const int P = (U + 1) / 2;  // pairs
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(&s.qdo_full, kBwdCompute);
-    for (int i = 0; i < kBwdStages; ++i) {
-      mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_empty[i], 1);
+    for (int i = 0; i < kDqKSlots; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.ds_full[i], kBwdCompute);
+    for (int i = 0; i < kDqVSlots; ++i) {
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);
     }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.s_free, kBwdCompute);
+    mbar_init(&s.ds_full, kBwdCompute);
+    mbar_init(&s.ds_done, 1);
     mbar_init(&s.fin, 1);
     mbar_init(&s.teardown, 1);
     fence_mbar_init();
@@ -249,95 +245,139 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = s.tmem_base;
   const Abort ab{&s.abort_flag, p.err};
   bool mma_issued = false;
+  auto gathered = [&](int i) { return 2 * i + 1 >= nslash; };  // pair i holds a bar unit
 
   if (warp == 0) {
-    int issued[kBwdStages];
-    for (int i = 0; i < kBwdStages; ++i) issued[i] = -1;
-    if (U > 0) {
-      const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
-      const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
-      for (int j = 0; j < U; ++j) {
-        const int st = j % kBwdStages;
-        if (j >= kBwdStages && !mbar_wait(&s.kv_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
-        // row masks computed ahead of the compute warps (hides the bitmap reads)
-        unit_row_masks(s.mask[st], s.bar_keys, G, av, bh, t, p.Nq, j < nslash,
-                       j < nslash ? int64_t(t) * kQTile + 64 - __ldg(elist + j) : 0,
-                       vlist + (j < nslash ? 0 : (j - nslash) * kKTile), lane);
-        __syncwarp();
-        if (j < nslash) {
-          if (lane == 0) {
-            const int c = t * kQTile + 64 - __ldg(elist + j);
-            mbar_arrive_expect_tx(&s.kv_full[st], 2 * NH * kKTile * 128);
-            for (int hf = 0; hf < NH; ++hf) {
-              tma_load_4d(s.k[st][hf], &tmK, &s.kv_full[st], 64 * hf, hk, c, b);
-              tma_load_4d(s.v[st][hf], &tmV, &s.kv_full[st], 64 * hf, hk, c, b);
-            }
-          }
+    // ------------------------------------------------------------ producer
+    // Per pair: the units' descriptions and K into a K slot (kept until the
+    // dQ chain of the pair has read it), then V into a V slot.
+    int issued_k[kDqKSlots], issued_v[kDqVSlots];
+    for (int i = 0; i < kDqKSlots; ++i) issued_k[i] = -1;
+    for (int i = 0; i < kDqVSlots; ++i) issued_v[i] = -1;
+    const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
+    const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
+    for (int i = 0; i < P; ++i) {
+      const int ks = i % kDqKSlots, vsl = i % kDqVSlots;
+      if (i >= kDqKSlots && !mbar_wait(&s.k_empty[ks], ((i / kDqKSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+      int64_t c[2];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int u = 2 * i + hf;
+        if (u >= U) {
+          c[hf] = kUnitNone;
+        } else if (u < nslash) {
+          c[hf] = int64_t(t) * kQTile + 64 - __ldg(elist + u);
         } else {
-          const int32_t* keys = vlist + (j - nslash) * kKTile;
-          gather_rows<D>(smem_u32(s.k[st][0]), kKTile, kb, p.sk[1], keys, kKTile, lane);
-          gather_rows<D>(smem_u32(s.v[st][0]), kKTile, vb, p.sv[1], keys, kKTile, lane);
-          asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.kv_full[st])) : "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s.kv_full[st]);
+          c[hf] = kUnitBar;
+          const int32_t* keys = vlist + (u - nslash) * kKTile;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = __ldg(keys + e * 32 + lane);
+            s.bar_pos[ks][hf][e * 32 + lane] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
+          }
         }
-        issued[st] = j;
-        __syncwarp();
+        if (lane == 0) s.unit_c[ks][hf] = c[hf];
       }
+      // gathers (and their arrivals) first, then the one plain arrival with
+      // the TMA byte count, so the phase cannot complete before the gathers
+      int bytes = 0;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        if (2 * i + hf < U)
+          bytes += dq_load_unit<D>(s.k[ks], hf, &s.k_full[ks], &tmK, kb, p.sk[1], vlist, 2 * i + hf, nslash,
+                                   c[hf], hk, b, lane);
+      if (gathered(i))
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.k_full[ks])) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&s.k_full[ks], uint32_t(bytes));
+      issued_k[ks] = i;
+      if (i >= kDqVSlots && !mbar_wait(&s.v_empty[vsl], ((i / kDqVSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+      bytes = 0;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        if (2 * i + hf < U)
+          bytes += dq_load_unit<D>(s.v[vsl], hf, &s.v_full[vsl], &tmV, vb, p.sv[1], vlist, 2 * i + hf, nslash,
+                                   c[hf], hk, b, lane);
+      if (gathered(i))
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.v_full[vsl])) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&s.v_full[vsl], uint32_t(bytes));
+      issued_v[vsl] = i;
     }
     if (lane == 0 && s.abort_flag) {
-      for (int i = 0; i < kBwdStages; ++i)
-        if (issued[i] >= 0) {
+      // drain loads still in flight before the CTA's shared memory is released
+      for (int i = 0; i < kDqKSlots; ++i)
+        if (issued_k[i] >= 0) {
           const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(&s.kv_full[i], (issued[i] / kBwdStages) & 1) && global_ns() - t0 < kWaitBudgetNs) {
+          while (!mbar_try_wait(&s.k_full[i], (issued_k[i] / kDqKSlots) & 1) && global_ns() - t0 < kWaitBudgetNs) {
+          }
+        }
+      for (int i = 0; i < kDqVSlots; ++i)
+        if (issued_v[i] >= 0) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(&s.v_full[i], (issued_v[i] / kDqVSlots) & 1) && global_ns() - t0 < kWaitBudgetNs) {
           }
         }
     }
   } else if (warp == 1) {
-    if (lane == 0 && U > 0) {
-      const uint32_t idS = idesc_bf16(128, 64, 0, 0);
+    // ------------------------------------------------------------ MMA issuer
+    // Per pair i: S_i, dP_i (once the compute warps hold S / dP of pair i - 1
+    // in registers), then dQ += dS K of pair i - 1.
+    if (lane == 0 && P > 0) {
+      const uint32_t idS = idesc_bf16(128, kDqPairKeys, 0, 0);
       const uint32_t idQ = idesc_bf16(128, D, 0, 1);
       bool ok = mbar_wait(&s.qdo_full, 0, ab, VS_ERR_TIMEOUT);
-      // Order: S_0 dP_0, then per j: S_j dP_j, dQ += dS_{j-1} K.  S_j reuses
-      // the buffer of unit j - 2, whose dS the dQ MMA issued before it reads.
-      for (int j = 0; ok && j <= U; ++j) {
-        if (j < U) {
-          const int st = j % kBwdStages;
-          if (!(ok = mbar_wait(&s.kv_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
-          if (j >= nslash) fence_proxy_async_smem();
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ts(tmem + kDqColS + (j & 1) * 64, tmem + kDqColQ + kk * 8, dk_, idS, kk > 0);
-            mma_ts(tmem + kDqColDP + (j & 1) * 64, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
-          }
-          mma_issued = true;
-          mma_commit(&s.s_full[j & 1]);
+      auto issue_dq = [&](int i) {
+        if (!(ok = mbar_wait(&s.ds_full, i & 1, ab, VS_ERR_TIMEOUT))) return;
+        tc_fence_after();
+        const int ks = i % kDqKSlots;
+        const int nk = (2 * i + 1 < U) ? kDqPairKeys / 16 : kKTile / 16;
+        for (int kk = 0; kk < nk; ++kk) {
+          const uint64_t da = sdesc_sw128(smem_u32(s.ds[kk / 4]) + (kk % 4) * 32, 16, 1024);
+          const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][0]) + kk * 2048, kDqPairKeys * 128, 1024);
+          mma_ss(tmem + kDqColAcc, da, dk_, idQ, (i > 0 || kk > 0));
         }
-        if (j >= 1) {
-          const int jj = j - 1, st = jj % kBwdStages;
-          if (!(ok = mbar_wait(&s.ds_full[jj & 1], (jj >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
-          tc_fence_after();
+        mma_commit(&s.ds_done);
+        mma_commit(&s.k_empty[ks]);
+      };
+      for (int i = 0; ok && i < P; ++i) {
+        const int ks = i % kDqKSlots, vsl = i % kDqVSlots;
+        if (!(ok = mbar_wait(&s.k_full[ks], (i / kDqKSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait(&s.v_full[vsl], (i / kDqVSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (i >= 1 && !(ok = mbar_wait(&s.s_free, (i - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (gathered(i)) fence_proxy_async_smem();
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kKTile / 16; ++kk) {
-            const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[st][0]) + kk * 2048, kKTile * 128, 1024);
-            const uint32_t a_ds = tmem + kDqColS + (jj & 1) * 64 + (kk >> 1) * 32 + (kk & 1) * 8;
-            mma_ts(tmem + kDqColAcc, a_ds, dk_, idQ, (jj > 0 || kk > 0));
-          }
-          mma_commit(&s.kv_empty[st]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][kk / 4]) + (kk % 4) * 32, 16, 1024);
+          mma_ts(tmem + kDqColS, tmem + kDqColQ + kk * 8, dk_, idS, kk > 0);
         }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[vsl][kk / 4]) + (kk % 4) * 32, 16, 1024);
+          mma_ts(tmem + kDqColDP, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
+        }
+        mma_commit(&s.s_full);
+        mma_commit(&s.v_empty[vsl]);
+        mma_issued = true;
+        if (i >= 1) issue_dq(i - 1);
       }
+      if (ok) issue_dq(P - 1);
       mma_commit(&s.fin);
     }
   } else {
+    // ------------------------------------------------------------ compute
+    // Warp (quarter, half): row quarter * 32 + lane, unit 2 i + half of each
+    // pair i (the pair's key columns [64 half, 64 half + 64)).
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;  // which 32 of the 64 key columns
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
     const int64_t n_loc = int64_t(t) * kQTile + r;
     const bool row_ok = n_loc < p.Nq && inputs_ok;
+    const int64_t n_g = qpos_g(G, n_loc);
+    const uint64_t* offbits = av.offbits + int64_t(bh) * G.WG;
+    const uint64_t* colbits = av.colbits + int64_t(bh) * G.WG;
     float Lr = 0.f, Dr = 0.f;
     if (row_ok) {
       const BwdLayout L = bwd_layout_dev(av.hdr, D);
@@ -368,47 +408,77 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&s.qdo_full);
+    uint8_t* ds_row = s.ds[half] + r * 128;
     bool ok = true;
-    for (int j = 0; j < U; ++j) {
-      ok = mbar_wait(&s.s_full[j & 1], (j >> 1) & 1, ab, VS_ERR_TIMEOUT);
+    for (int i = 0; i < P; ++i) {
+      const int ks = i % kDqKSlots;
+      // the unit's description (written by the producer before K landed)
+      ok = mbar_wait(&s.k_full[ks], (i / kDqKSlots) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const int64_t c = s.unit_c[ks][half];
+      uint64_t mask = 0;
+      if (row_ok && c != kUnitNone) {
+        if (c == kUnitBar) {
+          const int64_t* pos = s.bar_pos[ks][half];
+          int cnt = 0;
+#pragma unroll
+          for (int step = 32; step > 0; step >>= 1)
+            if (pos[cnt + step - 1] <= n_g) cnt += step;
+          if (pos[kKTile - 1] <= n_g) cnt = kKTile;
+          mask = cnt == kKTile ? ~0ull : ((1ull << cnt) - 1);
+        } else {
+          // bit k: offset n_g - m_g(c + k) selected, key c + k exists and is
+          // not a selected column (the 64 keys are globally contiguous)
+          const int64_t m0 = c >= 0 ? kpos_g(G, c) : c;
+          const uint64_t x = bits64(offbits, n_g - m0 - 63, G.WG);
+          const uint64_t keep = ~bits64(colbits, m0, G.WG) & (c < 0 ? ((~0ull) << (-c)) : ~0ull);
+          mask = __brevll(x) & keep;
+        }
+      }
+      ok = mbar_wait(&s.s_full, i & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[32], pr[32];
-      tmem_ld32(tl + kDqColS + (j & 1) * 64 + 32 * half, sr);
-      tmem_ld32(tl + kDqColDP + (j & 1) * 64 + 32 * half, pr);
+      uint32_t sr[64], pr[64];
+      tmem_ld32(tl + kDqColS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tl + kDqColS + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tl + kDqColDP + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+      tmem_ld32(tl + kDqColDP + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
       tmem_ld_wait();
-      // masks written by the producer before it released the stage
-      const int st = j % kBwdStages;
-      ok = mbar_wait(&s.kv_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT);
+      tc_fence_before();
+      mbar_arrive(&s.s_free);
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        float ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = 2 * k + e;
+          const float pv = ex2(fmaf(__uint_as_float(sr[col]), p.scale_log2, -Lr));
+          const float x = pv * (__uint_as_float(pr[col]) - Dr);
+          ds[e] = ((mask >> col) & 1ull) ? x : 0.f;  // after the product: masked scores may be garbage
+        }
+        pk[k] = pack_bf16x2(ds[0], ds[1]);
+      }
+      if (i >= 1) ok = mbar_wait(&s.ds_done, (i - 1) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      const uint32_t mask = row_ok ? uint32_t(s.mask[st][r] >> (32 * half)) : 0u;
-      uint32_t pk[16];
+      // row r of the unit's 64 keys: eight 16-byte chunks, 128B-swizzled
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float ds[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * i + e;
-          float pv = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -Lr));
-          pv = ((mask >> c) & 1u) ? pv : 0.f;  // one select: dS inherits the zero
-          ds[e] = pv * (__uint_as_float(pr[c]) - Dr);
-        }
-        pk[i] = pack_bf16x2(ds[0], ds[1]);
-      }
-      // over this warp's own S columns (read above): dQ of unit j - 2, the
-      // last reader of this buffer's previous dS, completed before S_j did
-      tmem_st16(tl + kDqColS + (j & 1) * 64 + 32 * half, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&s.ds_full[j & 1]);
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(ds_row + ((j ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(&s.ds_full);
     }
-    if (ok && U > 0) ok = mbar_wait(&s.fin, 0, ab, VS_ERR_TIMEOUT);
+    if (ok && P > 0) ok = mbar_wait(&s.fin, 0, ab, VS_ERR_TIMEOUT);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok && inputs_ok) {
@@ -420,14 +490,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
       for (int cc = (D / 2) * half; cc < (D / 2) * (half + 1); cc += 16) {
         uint32_t gv[16];
-        if (U > 0) {
+        if (P > 0) {
           tmem_ld16(tl + kDqColAcc + cc, gv);
           tmem_ld_wait();
         }
         if (!store) continue;
         float y[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = U > 0 ? __uint_as_float(gv[i]) * p.scale : 0.f;
+        for (int i = 0; i < 16; ++i) y[i] = P > 0 ? __uint_as_float(gv[i]) * p.scale : 0.f;
         if (acc) {
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
