@@ -22,6 +22,7 @@ namespace vs {
 namespace {
 
 constexpr int kBwdThreads = 320;
+constexpr int kDqThreads = 352;   // + warp 10: issues the dQ MMAs
 constexpr int kBwdCompute = 256;  // two warps per TMEM lane quarter, each owning half the columns
 constexpr int kBwdStages = 4;
 constexpr int kMaxGroup = 64;  // query heads per KV head supported by the key-major kernel
@@ -143,6 +144,9 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
 // TMEM at once, so the next pair's S / dP run while they compute dS.  Each
 // compute thread builds its own row's mask of its unit (slash: a window of
 // the offset bitmap; bar: a count of the unit's keys at or before the row).
+// Two warps issue MMAs: warp 1 the S / dP chains, warp 10 the dQ chains (the
+// two streams touch disjoint TMEM and are ordered by barriers only), so the
+// waits of one stream do not leave the tensor pipe idle.
 // TMEM: dQ [0, 128), S [128, 256), dP [256, 384), Q [384, 448), dO [448, 512).
 constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColQ = 384, kDqColDO = 448;
 constexpr int kDqPairKeys = 2 * kKTile;
@@ -159,7 +163,7 @@ struct DqSmem {
   uint64_t qdo_full;
   uint64_t k_full[kDqKSlots], k_empty[kDqKSlots], v_full[kDqVSlots], v_empty[kDqVSlots];
   uint64_t s_full, s_free, ds_full, ds_done;
-  uint64_t fin, teardown;
+  uint64_t fin, teardown, teardown_dq;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -185,7 +189,7 @@ __device__ __forceinline__ int dq_load_unit(uint8_t (*slot)[kDqPairKeys * 128], 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&s.ds_done, 1);
     mbar_init(&s.fin, 1);
     mbar_init(&s.teardown, 1);
+    mbar_init(&s.teardown_dq, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -256,8 +261,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < kDqVSlots; ++i) issued_v[i] = -1;
     const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
     const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
+    // e-list entries of the pair, loaded one pair ahead
+    int e_cur[2], e_nxt[2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) e_cur[hf] = hf < nslash ? __ldg(elist + hf) : 0;
     for (int i = 0; i < P; ++i) {
       const int ks = i % kDqKSlots, vsl = i % kDqVSlots;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) e_nxt[hf] = 2 * i + 2 + hf < nslash ? __ldg(elist + 2 * i + 2 + hf) : 0;
       if (i >= kDqKSlots && !mbar_wait(&s.k_empty[ks], ((i / kDqKSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
       int64_t c[2];
 #pragma unroll
@@ -266,7 +277,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (u >= U) {
           c[hf] = kUnitNone;
         } else if (u < nslash) {
-          c[hf] = int64_t(t) * kQTile + 64 - __ldg(elist + u);
+          c[hf] = int64_t(t) * kQTile + 64 - e_cur[hf];
         } else {
           c[hf] = kUnitBar;
           const int32_t* keys = vlist + (u - nslash) * kKTile;
@@ -303,6 +314,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&s.v_full[vsl], uint32_t(bytes));
       issued_v[vsl] = i;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) e_cur[hf] = e_nxt[hf];
     }
     if (lane == 0 && s.abort_flag) {
       // drain loads still in flight before the CTA's shared memory is released
@@ -320,26 +333,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per pair i: S_i, dP_i (once the compute warps hold S / dP of pair i - 1
-    // in registers), then dQ += dS K of pair i - 1.
+    // ------------------------------------------------------- S / dP issuer
+    // Per pair i: S_i, dP_i once the compute warps hold S / dP of pair i - 1
+    // in registers.
     if (lane == 0 && P > 0) {
       const uint32_t idS = idesc_bf16(128, kDqPairKeys, 0, 0);
-      const uint32_t idQ = idesc_bf16(128, D, 0, 1);
       bool ok = mbar_wait(&s.qdo_full, 0, ab, VS_ERR_TIMEOUT);
-      auto issue_dq = [&](int i) {
-        if (!(ok = mbar_wait(&s.ds_full, i & 1, ab, VS_ERR_TIMEOUT))) return;
-        tc_fence_after();
-        const int ks = i % kDqKSlots;
-        const int nk = (2 * i + 1 < U) ? kDqPairKeys / 16 : kKTile / 16;
-        for (int kk = 0; kk < nk; ++kk) {
-          const uint64_t da = sdesc_sw128(smem_u32(s.ds[kk / 4]) + (kk % 4) * 32, 16, 1024);
-          const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][0]) + kk * 2048, kDqPairKeys * 128, 1024);
-          mma_ss(tmem + kDqColAcc, da, dk_, idQ, (i > 0 || kk > 0));
-        }
-        mma_commit(&s.ds_done);
-        mma_commit(&s.k_empty[ks]);
-      };
       for (int i = 0; ok && i < P; ++i) {
         const int ks = i % kDqKSlots, vsl = i % kDqVSlots;
         if (!(ok = mbar_wait(&s.k_full[ks], (i / kDqKSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
@@ -360,9 +359,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(&s.s_full);
         mma_commit(&s.v_empty[vsl]);
         mma_issued = true;
-        if (i >= 1) issue_dq(i - 1);
       }
-      if (ok) issue_dq(P - 1);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dQ issuer
+    // Per pair i, once its dS is in shared memory: dQ += dS K over the pair's
+    // keys (K stays in its slot until then).
+    if (lane == 0 && P > 0) {
+      const uint32_t idQ = idesc_bf16(128, D, 0, 1);
+      bool ok = true;
+      for (int i = 0; ok && i < P; ++i) {
+        if (!(ok = mbar_wait(&s.ds_full, i & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (gathered(i)) fence_proxy_async_smem();
+        tc_fence_after();
+        const int ks = i % kDqKSlots;
+        const int nk = (2 * i + 1 < U) ? kDqPairKeys / 16 : kKTile / 16;
+        for (int kk = 0; kk < nk; ++kk) {
+          const uint64_t da = sdesc_sw128(smem_u32(s.ds[kk / 4]) + (kk % 4) * 32, 16, 1024);
+          const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][0]) + kk * 2048, kDqPairKeys * 128, 1024);
+          mma_ss(tmem + kDqColAcc, da, dk_, idQ, (i > 0 || kk > 0));
+        }
+        mma_commit(&s.ds_done);
+        mma_commit(&s.k_empty[ks]);
+        mma_issued = true;
+      }
       mma_commit(&s.fin);
     }
   } else {
@@ -419,25 +439,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       const int64_t c = s.unit_c[ks][half];
-      uint64_t mask = 0;
-      if (row_ok && c != kUnitNone) {
-        if (c == kUnitBar) {
-          const int64_t* pos = s.bar_pos[ks][half];
-          int cnt = 0;
-#pragma unroll
-          for (int step = 32; step > 0; step >>= 1)
-            if (pos[cnt + step - 1] <= n_g) cnt += step;
-          if (pos[kKTile - 1] <= n_g) cnt = kKTile;
-          mask = cnt == kKTile ? ~0ull : ((1ull << cnt) - 1);
-        } else {
-          // bit k: offset n_g - m_g(c + k) selected, key c + k exists and is
-          // not a selected column (the 64 keys are globally contiguous)
-          const int64_t m0 = c >= 0 ? kpos_g(G, c) : c;
-          const uint64_t x = bits64(offbits, n_g - m0 - 63, G.WG);
-          const uint64_t keep = ~bits64(colbits, m0, G.WG) & (c < 0 ? ((~0ull) << (-c)) : ~0ull);
-          mask = __brevll(x) & keep;
-        }
-      }
+      const bool slash = row_ok && c != kUnitNone && c != kUnitBar;
+      // slash: bit k of the mask is set iff offset n_g - m_g(c + k) is
+      // selected, key c + k exists and is not a selected column (the 64 keys
+      // are globally contiguous).  The bitmap words are loaded here and used
+      // after the scores arrive.
+      const int64_t m0 = slash ? (c >= 0 ? kpos_g(G, c) : c) : 0;
+      const int64_t lo = n_g - m0 - 63;
+      const int64_t wo = lo >> 6, wc = m0 >> 6;
+      const uint64_t oa = (slash && wo >= 0 && wo < G.WG) ? __ldg(offbits + wo) : 0ull;
+      const uint64_t ob = (slash && wo + 1 >= 0 && wo + 1 < G.WG) ? __ldg(offbits + wo + 1) : 0ull;
+      const uint64_t ca = (slash && wc >= 0 && wc < G.WG) ? __ldg(colbits + wc) : 0ull;
+      const uint64_t cb = (slash && wc + 1 >= 0 && wc + 1 < G.WG) ? __ldg(colbits + wc + 1) : 0ull;
       ok = mbar_wait(&s.s_full, i & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -452,6 +465,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.s_free);
+      uint64_t mask = 0;
+      if (slash) {
+        const int so = int(lo & 63), sc = int(m0 & 63);
+        const uint64_t x = so ? ((oa >> so) | (ob << (64 - so))) : oa;
+        const uint64_t cw = sc ? ((ca >> sc) | (cb << (64 - sc))) : ca;
+        mask = __brevll(x) & ~cw & (c < 0 ? ((~0ull) << (-c)) : ~0ull);
+      } else if (row_ok && c == kUnitBar) {
+        const int64_t* pos = s.bar_pos[ks][half];
+        int cnt = 0;
+#pragma unroll
+        for (int step = 32; step > 0; step >>= 1)
+          if (pos[cnt + step - 1] <= n_g) cnt += step;
+        if (pos[kKTile - 1] <= n_g) cnt = kKTile;
+        mask = cnt == kKTile ? ~0ull : ((1ull << cnt) - 1);
+      }
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
@@ -527,16 +555,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   }
+  // an issuer that gave up waits (bounded) for its own MMAs in flight
+  if ((warp == 1 || warp == 10) && lane == 0 && mma_issued && s.abort_flag) {
+    uint64_t* tb = warp == 1 ? &s.teardown : &s.teardown_dq;
+    mma_commit(tb);
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(tb, 0) && global_ns() - t0 < kWaitBudgetNs) {
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    if (lane == 0 && mma_issued && s.abort_flag) {
-      mma_commit(&s.teardown);
-      const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(&s.teardown, 0) && global_ns() - t0 < kWaitBudgetNs) {
-      }
-    }
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1091,7 +1120,7 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   trace_begin("bwd_dq", st);
-  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kBwdThreads, sm_dq, st>>>(tk64, tv64, p);
+  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kDqThreads, sm_dq, st>>>(tk64, tv64, p);
   trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
