@@ -21,8 +21,7 @@
 namespace vs {
 namespace {
 
-constexpr int kBwdThreads = 320;
-constexpr int kDqThreads = 352;   // + warp 10: issues the dQ MMAs
+constexpr int kIssue2Threads = 352;  // + warp 10, the second MMA-issuing warp
 constexpr int kBwdCompute = 256;  // two warps per TMEM lane quarter, each owning half the columns
 constexpr int kBwdStages = 4;
 constexpr int kMaxGroup = 64;  // query heads per KV head supported by the key-major kernel
@@ -189,7 +188,7 @@ __device__ __forceinline__ int dq_load_unit(uint8_t (*slot)[kDqPairKeys * 128], 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kDqThreads, 1)
+__global__ void __launch_bounds__(kIssue2Threads, 1)
     vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -594,7 +593,7 @@ struct KvSmem {
   uint64_t kv_full, k_tmem;
   uint64_t st_full[kBwdStages], st_empty[kBwdStages];
   uint64_t s_full, s_free, p_full, mm_done;
-  uint64_t fin, teardown;
+  uint64_t fin, teardown, teardown_g;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -613,7 +612,7 @@ struct KvWork {
 };
 
 template <int D, bool BAR>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kIssue2Threads, 1)
     vs_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
                      const BwdParams p) {
@@ -690,6 +689,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&s.mm_done, 1);
     mbar_init(&s.fin, 1);
     mbar_init(&s.teardown, 1);
+    mbar_init(&s.teardown_g, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -779,43 +779,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ---------------------------------------------------- S^T / dP^T issuer
+    // Unit j once the compute warps hold S^T / dP^T of unit j - 1.
     if (lane == 0 && run) {
       const uint32_t idS = idesc_bf16(128, kRowTile, 0, 0);
-      const uint32_t idG = idesc_bf16(128, D, 0, 1);
       bool ok = mbar_wait(&s.kv_full, 0, ab, VS_ERR_TIMEOUT) && mbar_wait(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT);
       if (ok && BAR) fence_proxy_async_smem();
-      for (int j = 0; ok && j <= U; ++j) {
-        if (j < U) {
-          const int st = j % kBwdStages;
-          if (!(ok = mbar_wait(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
-          if (j >= 1 && !(ok = mbar_wait(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
-          tc_fence_after();
+      for (int j = 0; ok && j < U; ++j) {
+        const int st = j % kBwdStages;
+        if (!(ok = mbar_wait(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (j >= 1 && !(ok = mbar_wait(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
-            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ts(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
-            mma_ss(tmem + kKvColDP, dva, dg_, idS, kk > 0);
-          }
-          mma_issued = true;
-          mma_commit(&s.s_full);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
+          const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+          const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+          mma_ts(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
+          mma_ss(tmem + kKvColDP, dva, dg_, idS, kk > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1, st = jj % kBwdStages;
-          if (!(ok = mbar_wait(&s.p_full, jj & 1, ab, VS_ERR_TIMEOUT))) break;
-          tc_fence_after();
+        mma_issued = true;
+        mma_commit(&s.s_full);
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------- dV / dK issuer
+    // Unit j once its P^T / dS^T are in TMEM; the unit's stage is released
+    // after these MMAs (the S^T / dP^T MMAs that read it completed before the
+    // compute warps saw the scores).
+    if (lane == 0 && run) {
+      const uint32_t idG = idesc_bf16(128, D, 0, 1);
+      bool ok = true;
+      for (int j = 0; ok && j < U; ++j) {
+        const int st = j % kBwdStages;
+        if (!(ok = mbar_wait(&s.p_full, j & 1, ab, VS_ERR_TIMEOUT))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kRowTile / 16; ++kk) {
-            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][0]) + kk * 2048, kRowTile * 128, 1024);
-            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][0]) + kk * 2048, kRowTile * 128, 1024);
-            mma_ts(tmem + kKvColDV, tmem + kKvColP + kk * 8, dg_, idG, (jj > 0 || kk > 0));
-            mma_ts(tmem + kKvColDK, tmem + kKvColDS + kk * 8, dq_, idG, (jj > 0 || kk > 0));
-          }
-          mma_commit(&s.mm_done);
-          mma_commit(&s.st_empty[st]);
+        for (int kk = 0; kk < kRowTile / 16; ++kk) {
+          const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][0]) + kk * 2048, kRowTile * 128, 1024);
+          const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][0]) + kk * 2048, kRowTile * 128, 1024);
+          mma_ts(tmem + kKvColDV, tmem + kKvColP + kk * 8, dg_, idG, (j > 0 || kk > 0));
+          mma_ts(tmem + kKvColDK, tmem + kKvColDS + kk * 8, dq_, idG, (j > 0 || kk > 0));
         }
+        mma_issued = true;
+        mma_commit(&s.mm_done);
+        mma_commit(&s.st_empty[st]);
       }
       mma_commit(&s.fin);
     }
@@ -1032,16 +1040,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   }
+  // an issuer that gave up waits (bounded) for its own MMAs in flight
+  if ((warp == 1 || warp == 10) && lane == 0 && mma_issued && s.abort_flag) {
+    uint64_t* tb = warp == 1 ? &s.teardown : &s.teardown_g;
+    mma_commit(tb);
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(tb, 0) && global_ns() - t0 < kWaitBudgetNs) {
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    if (lane == 0 && mma_issued && s.abort_flag) {
-      mma_commit(&s.teardown);
-      const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(&s.teardown, 0) && global_ns() - t0 < kWaitBudgetNs) {
-      }
-    }
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1110,17 +1119,17 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   trace_end(st);
   // bar partials first: the slash kernel's epilogue reads them
   trace_begin("bwd_dkv_bar", st);
-  vs_bwd_kv_kernel<D, true><<<unsigned(int64_t(sh->B) * sh->Hq * grid_per_bh), kBwdThreads, sm_kv, st>>>(
+  vs_bwd_kv_kernel<D, true><<<unsigned(int64_t(sh->B) * sh->Hq * grid_per_bh), kIssue2Threads, sm_kv, st>>>(
       tk128, tv128, tq64, tg64, p);
   trace_end(st);
   const int TK = (sh->Nk + kBarK - 1) / kBarK;
   trace_begin("bwd_dkv_slash", st);
-  vs_bwd_kv_kernel<D, false><<<unsigned(int64_t(sh->B) * sh->Hkv * TK), kBwdThreads, sm_kv, st>>>(
+  vs_bwd_kv_kernel<D, false><<<unsigned(int64_t(sh->B) * sh->Hkv * TK), kIssue2Threads, sm_kv, st>>>(
       tk128, tv128, tq64, tg64, p);
   trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   trace_begin("bwd_dq", st);
-  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kDqThreads, sm_dq, st>>>(tk64, tv64, p);
+  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kIssue2Threads, sm_dq, st>>>(tk64, tv64, p);
   trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
