@@ -18,6 +18,8 @@ directly:
 * ``merge`` -- ``merge_out_and_lse`` of Algorithm 2.
 * ``stripe_positions`` / ``striped_permute`` -- 64-token block-level
   striping (section 4.2 (ii)).
+* ``ring_owners`` / ``ring_work`` -- per (query worker, key worker) mask
+  entries under the striped and ZigZag ring layouts (sections 2, 3.3, 4.2).
 
 Inputs are converted to float64 (bf16 values widen exactly); all arithmetic is fp64.
 """
@@ -300,6 +302,43 @@ def striped_permute(x: np.ndarray, W: int, stripe: int, inverse: bool = False) -
     out = np.empty((B, N) + x.shape[3:], x.dtype)
     for j in range(N // stripe):
         out[:, j * stripe:(j + 1) * stripe] = x[j % W_, :, (j // W_) * stripe:(j // W_ + 1) * stripe]
+    return out
+
+
+def ring_owners(N: int, W: int, layout: str, stripe: int = 64) -> np.ndarray:
+    """Worker that holds each global token of a context-parallel ring.
+
+    striped: block j = n // stripe lives on worker j mod W (Block-level
+      Striped Sparse Ring Attention, section 4.2 (ii));
+    zigzag: the sequence is cut into 2W chunks of N / (2W) tokens and worker
+      r holds chunks r and 2W - 1 - r (the folded, mirrored layout of ZigZag
+      Ring Attention, section 2 and Figure 1)."""
+    n = np.arange(N, dtype=np.int64)
+    if layout == "striped":
+        return (n // stripe) % W
+    if layout == "zigzag":
+        c = n // (N // (2 * W))
+        return np.where(c < W, c, 2 * W - 1 - c)
+    raise ValueError(layout)
+
+
+def ring_work(iv, is_, N: int, W: int, layout: str, stripe: int = 64) -> np.ndarray:
+    """Effective work of every (query worker, key worker) pair: the number of
+    entries of the VS mask on the global sequence whose query token lives on
+    worker r and whose key token lives on worker q, summed over (b, h);
+    int64 [W, W].  At ring step s worker r attends to the keys of worker
+    (r - s) mod W, so its work at that step is out[r, (r - s) % W]."""
+    iv = np.asarray(iv, np.int32)
+    is_ = np.asarray(is_, np.int32)
+    B, H = iv.shape[:2]
+    own = ring_owners(N, W, layout, stripe)
+    z = np.zeros((B, N, H, 1))
+    p = Problem(z, np.zeros((B, N, 1, 1)), np.zeros((B, N, 1, 1)), iv, is_, 1.0)
+    out = np.zeros((W, W), np.int64)
+    for b in range(B):
+        for h in range(H):
+            n, m = np.nonzero(mask_dense(p, b, h))
+            np.add.at(out, (own[n], own[m]), 1)
     return out
 
 
