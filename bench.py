@@ -538,9 +538,33 @@ def striped(args, w, x, rank, world):
             "imbalance": {"flops_max_over_mean": float(fl.max() / fl.mean()),
                           "ms_max_over_mean": float(tm.max() / tm.mean())},
             "kernels": per_kernel, "step_ms_all": step_ms}
+    line["layouts"] = _layout_work(wk.v_idx, wk.s_idx, w.N, W)
     if args.all_workers:
         line["workers"] = _all_workers(args, w, q, k, v, to_dev(x["dout"]), dev)
     return line, clk.summary()
+
+
+def _layout_work(iv, is_, N, W):
+    """Effective work (mask entries) of every worker and ring step under the
+    striped and the ZigZag layout of the same global selection (computed on
+    the GPU, outside the timed region), and its imbalance: worker-level =
+    max / mean over the workers at one ring step, step-level = max / mean over
+    the ring steps of one worker, each reported as mean and max; plus the
+    imbalance of the workers' totals."""
+    import dynamic_vertical_slash_gb300 as vs
+
+    out = {}
+    for layout in ("striped", "zigzag"):
+        M = vs.vs_ring_work(iv, is_, N, W, layout).cpu().numpy().astype(np.float64)
+        st = np.array([[M[r, (r - s) % W] for r in range(W)] for s in range(W)])  # [step][worker]
+        wl = st.max(1) / st.mean(1)
+        sl = st.max(0) / st.mean(0)
+        tot = M.sum(1)
+        out[layout] = {"entries_per_step_worker": st.astype(np.int64).tolist(),
+                       "worker_level_mean": float(wl.mean()), "worker_level_max": float(wl.max()),
+                       "step_level_mean": float(sl.mean()), "step_level_max": float(sl.max()),
+                       "worker_totals_max_over_mean": float(tot.max() / tot.mean())}
+    return out
 
 
 def _all_workers(args, w, q, k, v, do, dev):

@@ -78,6 +78,8 @@ def lib(build_if_missing: bool = True):
     L.vs_attn_bwd.argtypes = [_S, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.striped_permute.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    L.vs_ring_work.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _P, ctypes.c_int, _P, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]
     L.vs_check_status.argtypes = [_P, _P]
     L.vs_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, _P]
     L.vs_status_string.argtypes = [ctypes.c_int]
@@ -188,6 +190,22 @@ def vs_select_topp(v_score, s_score, pv: float, ps: float, kv_max: int, ks_max: 
                                 _ptr(v_idx), _ptr(s_idx), _ptr(kv), _ptr(ks), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)), "vs_select_topp")
     return v_idx, s_idx, kv, ks
+
+
+VS_LAYOUT_STRIPED, VS_LAYOUT_ZIGZAG = 0, 1
+
+
+def vs_ring_work(v_idx, s_idx, N: int, world: int, layout: str = "striped", out=None, ws=None, stream=None):
+    """Mask entries per (query worker, key worker) of a ring over the global
+    lists: int64 device tensor [world, world] (see include/vs.h)."""
+    B, H, kv = v_idx.shape
+    ks = s_idx.shape[-1]
+    lay = {"striped": VS_LAYOUT_STRIPED, "zigzag": VS_LAYOUT_ZIGZAG}[layout]
+    out = torch.empty(world, world, dtype=torch.int64, device=v_idx.device) if out is None else out
+    ws = _ws(256, v_idx.device) if ws is None else ws
+    _check(lib().vs_ring_work(B, H, int(N), _ptr(v_idx), kv, _ptr(s_idx), ks, world, lay, _ptr(out), _ptr(ws),
+                              ws.numel() * ws.element_size(), _stream(stream)), "vs_ring_work")
+    return out
 
 
 def make_stripe(world: int, q_rank: int, kv_rank: int, N_global: int, stripe: int = 64) -> vs_stripe:

@@ -302,6 +302,20 @@ vs_status vs_attn_bwd(const vs_shape* s, const void* q, const void* k, const voi
   return launch_bwd(s, G, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, ws, ws_bytes, stream);
 }
 
+vs_status vs_ring_work(int B, int H, int64_t N, const int32_t* v_idx, int kv, const int32_t* s_idx, int ks,
+                       int world, int layout, int64_t* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!v_idx || !s_idx || !out || !ws) return VS_ERR_ARG;
+  if (B < 1 || H < 1 || N < 1 || N > (int64_t(1) << 31) - 1 || world < 1 || world > 64) return VS_ERR_SHAPE;
+  if (layout != VS_LAYOUT_STRIPED && layout != VS_LAYOUT_ZIGZAG) return VS_ERR_ARG;
+  if (layout == VS_LAYOUT_STRIPED && N % (int64_t(kBlk) * world)) return VS_ERR_SHAPE;
+  if (layout == VS_LAYOUT_ZIGZAG && N % (2 * int64_t(world))) return VS_ERR_SHAPE;
+  if (kv < 1 || ks < 1) return VS_ERR_ARG;
+  if (int64_t(B) * H > 65535) return VS_ERR_SHAPE;
+  if (ring_work_smem(N, world) > size_t(200) << 10) return VS_ERR_SHAPE;
+  if (ws_bytes < 256) return VS_ERR_WORKSPACE;
+  return launch_ring_work(B, H, N, v_idx, kv, s_idx, ks, world, layout, out, static_cast<int*>(ws), stream);
+}
+
 vs_status striped_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int stripe, int inverse,
                           int only_rank, cudaStream_t stream) {
   if (!x || !y) return VS_ERR_ARG;

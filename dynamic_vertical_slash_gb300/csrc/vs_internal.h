@@ -40,6 +40,9 @@ vs_status launch_select_topp(int B, int H, int N, const float* v_score, const fl
                              int kv_max, int ks_max, int32_t* v_idx, int32_t* s_idx, int32_t* kv, int32_t* ks,
                              int* err, cudaStream_t st);
 size_t topp_max_n();
+size_t ring_work_smem(int64_t N, int W);
+vs_status launch_ring_work(int B, int H, int64_t N, const int32_t* v_idx, int kv, const int32_t* s_idx, int ks,
+                           int world, int layout, int64_t* out, int* err, cudaStream_t st);
 vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                        const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t st);
 size_t index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* stripe, ArenaHeader* hdr_out);

@@ -266,6 +266,32 @@ vs_status vs_attn_bwd(const vs_shape* shape, const void* q, const void* k, const
 vs_status striped_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int stripe, int inverse,
                           int only_rank, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * vs_ring_work -- work of a context-parallel ring under the VS mask (section
+ * 3.3, worker- and step-level imbalance; section 4.2, Balanced Sparse Ring
+ * Attention; section 2, Striped vs ZigZag Ring Attention).
+ *
+ * out[r][q] = number of entries of the mask on the global sequence,
+ *     M[n, m] = (m <= n) and (m in v_idx or n - m in s_idx),
+ * whose query n lives on worker r and key m on worker q, summed over (b, h).
+ * At ring step s worker r attends to the keys of worker (r - s) mod world, so
+ * its effective work at that step is out[r][(r - s) mod world].
+ *   layout  VS_LAYOUT_STRIPED: 64-token block j on worker j mod world
+ *           (N a multiple of 64 world); VS_LAYOUT_ZIGZAG: 2 world chunks of
+ *           N / (2 world) tokens, worker r holds chunks r and 2 world - 1 - r
+ *           (N a multiple of 2 world)
+ *   v_idx   int32 [B][H][kv], s_idx int32 [B][H][ks]: global lists as for
+ *           vs_build_block_index (ascending, optionally ending in -1)
+ *   out     int64 [world][world] device (out; overwritten)
+ *   ws      device buffer of at least 256 bytes; its first word is the status
+ *           word (VS_ERR_INDEX for a bad list)
+ * Limits: 1 <= world <= 64, N < 2^31 and about N <= 1.2M at world 64 (the
+ * column bitmap and its prefix counts live in shared memory).
+ * ------------------------------------------------------------------------- */
+enum { VS_LAYOUT_STRIPED = 0, VS_LAYOUT_ZIGZAG = 1 };
+vs_status vs_ring_work(int B, int H, int64_t N, const int32_t* v_idx, int kv, const int32_t* s_idx, int ks,
+                       int world, int layout, int64_t* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Reads the device status word at the start of a workspace or index arena,
  * resets it to VS_OK, and returns the code it held.  Synchronises `stream`. */
 vs_status vs_check_status(void* ws_or_arena, cudaStream_t stream);
