@@ -133,6 +133,10 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
 
 // 16-byte asynchronous global->shared copy (L2 only), zero-filled when
 // `src_bytes` is 0.
+// 4-byte asynchronous global->shared copy, zero-filled when `src_bytes` is 0.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }

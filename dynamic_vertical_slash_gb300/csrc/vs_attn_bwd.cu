@@ -725,7 +725,20 @@ __global__ void __launch_bounds__(kIssue2Threads, 1)
       kv_issued = true;
       const float* l2g = reinterpret_cast<const float*>(p.ws + L.off_l2);
       const float* ddg = reinterpret_cast<const float*>(p.ws + L.off_d);
-      int cur_h = 0, cur_j = 0;  // slash: head of the group and its entry for unit j
+      // slash: the group's head of a unit and its f-list entry, read one unit
+      // ahead so that the load overlaps the previous unit's issue
+      int cur_h = 0, cur_j = 0, h_nxt = 0;
+      int32_t f_nxt = 0;
+      auto next_unit = [&]() {
+        while (cur_h < w.heads - 1 && cur_j >= s.head_units[cur_h]) {
+          cur_j = 0;
+          ++cur_h;
+        }
+        h_nxt = hk * G.g + cur_h;
+        f_nxt = __ldg(av.flist + (int64_t(b) * G.Hq + h_nxt) * G.EMAX + cur_j);
+        ++cur_j;
+      };
+      if (!BAR && U > 0) next_unit();
       for (int j = 0; j < U; ++j) {
         const int st = j % kBwdStages;
         if (j >= kBwdStages && !mbar_wait(&s.st_empty[st], ((j / kBwdStages) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
@@ -735,21 +748,21 @@ __global__ void __launch_bounds__(kIssue2Threads, 1)
           h = h_bar;
           r0 = w.row0 + int64_t(j) * kRowTile;
         } else {
-          while (cur_h < w.heads - 1 && cur_j >= s.head_units[cur_h]) {
-            cur_j = 0;
-            ++cur_h;
-          }
-          h = hk * G.g + cur_h;
-          r0 = k0 + __ldg(av.flist + (int64_t(b) * G.Hq + h) * G.EMAX + cur_j);
-          ++cur_j;
+          h = h_nxt;
+          r0 = k0 + f_nxt;
+          if (j + 1 < U) next_unit();
         }
-        const int64_t bh = int64_t(b) * p.Hq + h;
+        // the rows' LSE and D by asynchronous copies (zero past the end),
+        // tracked by the stage's barrier like the TMA loads
+        const float* l2r = l2g + (int64_t(b) * p.Hq + h) * p.Nq;
+        const float* ddr = ddg + (int64_t(b) * p.Hq + h) * p.Nq;
         for (int i = lane; i < kRowTile; i += 32) {
           const int64_t n = r0 + i;
           const bool in = n < p.Nq;
-          s.l2[st][i] = in ? l2g[bh * p.Nq + n] : 0.f;
-          s.dd[st][i] = in ? ddg[bh * p.Nq + n] : 0.f;
+          cp_async_4(smem_u32(&s.l2[st][i]), in ? l2r + n : l2r, in ? 4u : 0u);
+          cp_async_4(smem_u32(&s.dd[st][i]), in ? ddr + n : ddr, in ? 4u : 0u);
         }
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.st_full[st])) : "memory");
         if (lane == 0) {
           s.unit_head[st] = h;
           s.unit_row[st] = int32_t(r0);
