@@ -22,6 +22,8 @@ namespace vs {
 namespace {
 
 constexpr int kIssue2Threads = 352;  // + warp 10, the second MMA-issuing warp
+constexpr int kDqThreads = 384;      // + warp 11, the dQ kernel's V loader
+constexpr int kDqVWarp = 11;
 constexpr int kBwdCompute = 256;  // two warps per TMEM lane quarter, each owning half the columns
 constexpr int kBwdStages = 4;
 constexpr int kMaxGroup = 64;  // query heads per KV head supported by the key-major kernel
@@ -145,7 +147,8 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
 // the offset bitmap; bar: a count of the unit's keys at or before the row).
 // Two warps issue MMAs: warp 1 the S / dP chains, warp 10 the dQ chains (the
 // two streams touch disjoint TMEM and are ordered by barriers only), so the
-// waits of one stream do not leave the tensor pipe idle.
+// waits of one stream do not leave the tensor pipe idle; two warps load K
+// (warp 0) and V (warp 11).
 // TMEM: dQ [0, 128), S [128, 256), dP [256, 384), Q [384, 448), dO [448, 512).
 constexpr uint32_t kDqColAcc = 0, kDqColS = 128, kDqColDP = 256, kDqColQ = 384, kDqColDO = 448;
 constexpr int kDqPairKeys = 2 * kKTile;
@@ -188,7 +191,7 @@ __device__ __forceinline__ int dq_load_unit(uint8_t (*slot)[kDqPairKeys * 128], 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kIssue2Threads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -251,83 +254,69 @@ __global__ void __launch_bounds__(kIssue2Threads, 1)
   bool mma_issued = false;
   auto gathered = [&](int i) { return 2 * i + 1 >= nslash; };  // pair i holds a bar unit
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Per pair: the units' descriptions and K into a K slot (kept until the
-    // dQ chain of the pair has read it), then V into a V slot.
-    int issued_k[kDqKSlots], issued_v[kDqVSlots];
-    for (int i = 0; i < kDqKSlots; ++i) issued_k[i] = -1;
-    for (int i = 0; i < kDqVSlots; ++i) issued_v[i] = -1;
-    const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
-    const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
-    // e-list entries of the pair, loaded one pair ahead
+  if (warp == 0 || warp == kDqVWarp) {
+    // ----------------------------------------------------------- producers
+    // Warp 0: per pair the units' descriptions and K into a K slot (kept
+    // until the dQ chain of the pair has read it); warp kDqVWarp: V into a V
+    // slot.  Both walk the e-list one pair ahead.
+    const bool isv = warp == kDqVWarp;
+    const int nslot = isv ? kDqVSlots : kDqKSlots;
+    uint64_t* full = isv ? s.v_full : s.k_full;
+    uint64_t* empty = isv ? s.v_empty : s.k_empty;
+    const CUtensorMap* tm = isv ? &tmV : &tmK;
+    const uint8_t* base = isv ? p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2
+                              : p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
+    const int64_t stok = isv ? p.sv[1] : p.sk[1];
+    int issued[kDqKSlots];
+    for (int i = 0; i < kDqKSlots; ++i) issued[i] = -1;
     int e_cur[2], e_nxt[2];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) e_cur[hf] = hf < nslash ? __ldg(elist + hf) : 0;
     for (int i = 0; i < P; ++i) {
-      const int ks = i % kDqKSlots, vsl = i % kDqVSlots;
+      const int sl = i % nslot;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) e_nxt[hf] = 2 * i + 2 + hf < nslash ? __ldg(elist + 2 * i + 2 + hf) : 0;
-      if (i >= kDqKSlots && !mbar_wait(&s.k_empty[ks], ((i / kDqKSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
+      if (i >= nslot && !mbar_wait(&empty[sl], ((i / nslot) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
       int64_t c[2];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int u = 2 * i + hf;
-        if (u >= U) {
-          c[hf] = kUnitNone;
-        } else if (u < nslash) {
-          c[hf] = int64_t(t) * kQTile + 64 - e_cur[hf];
-        } else {
-          c[hf] = kUnitBar;
-          const int32_t* keys = vlist + (u - nslash) * kKTile;
+        c[hf] = u >= U ? kUnitNone : (u < nslash ? int64_t(t) * kQTile + 64 - e_cur[hf] : kUnitBar);
+        if (!isv) {
+          if (c[hf] == kUnitBar) {
+            const int32_t* keys = vlist + (u - nslash) * kKTile;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = __ldg(keys + e * 32 + lane);
-            s.bar_pos[ks][hf][e * 32 + lane] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
+            for (int e = 0; e < 2; ++e) {
+              const int key = __ldg(keys + e * 32 + lane);
+              s.bar_pos[sl][hf][e * 32 + lane] = key >= 0 ? kpos_g(G, key) : INT64_MAX;
+            }
           }
+          if (lane == 0) s.unit_c[sl][hf] = c[hf];
         }
-        if (lane == 0) s.unit_c[ks][hf] = c[hf];
       }
       // gathers (and their arrivals) first, then the one plain arrival with
       // the TMA byte count, so the phase cannot complete before the gathers
       int bytes = 0;
+      uint8_t (*slot)[kDqPairKeys * 128] = isv ? s.v[sl] : s.k[sl];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
         if (2 * i + hf < U)
-          bytes += dq_load_unit<D>(s.k[ks], hf, &s.k_full[ks], &tmK, kb, p.sk[1], vlist, 2 * i + hf, nslash,
-                                   c[hf], hk, b, lane);
+          bytes += dq_load_unit<D>(slot, hf, &full[sl], tm, base, stok, vlist, 2 * i + hf, nslash, c[hf], hk, b,
+                                   lane);
       if (gathered(i))
-        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.k_full[ks])) : "memory");
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&full[sl])) : "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&s.k_full[ks], uint32_t(bytes));
-      issued_k[ks] = i;
-      if (i >= kDqVSlots && !mbar_wait(&s.v_empty[vsl], ((i / kDqVSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)) break;
-      bytes = 0;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-        if (2 * i + hf < U)
-          bytes += dq_load_unit<D>(s.v[vsl], hf, &s.v_full[vsl], &tmV, vb, p.sv[1], vlist, 2 * i + hf, nslash,
-                                   c[hf], hk, b, lane);
-      if (gathered(i))
-        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(&s.v_full[vsl])) : "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&s.v_full[vsl], uint32_t(bytes));
-      issued_v[vsl] = i;
+      if (lane == 0) mbar_arrive_expect_tx(&full[sl], uint32_t(bytes));
+      issued[sl] = i;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) e_cur[hf] = e_nxt[hf];
     }
     if (lane == 0 && s.abort_flag) {
       // drain loads still in flight before the CTA's shared memory is released
-      for (int i = 0; i < kDqKSlots; ++i)
-        if (issued_k[i] >= 0) {
+      for (int i = 0; i < nslot; ++i)
+        if (issued[i] >= 0) {
           const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(&s.k_full[i], (issued_k[i] / kDqKSlots) & 1) && global_ns() - t0 < kWaitBudgetNs) {
-          }
-        }
-      for (int i = 0; i < kDqVSlots; ++i)
-        if (issued_v[i] >= 0) {
-          const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(&s.v_full[i], (issued_v[i] / kDqVSlots) & 1) && global_ns() - t0 < kWaitBudgetNs) {
+          while (!mbar_try_wait(&full[i], (issued[i] / nslot) & 1) && global_ns() - t0 < kWaitBudgetNs) {
           }
         }
     }
@@ -1142,7 +1131,7 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   trace_begin("bwd_dq", st);
-  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kIssue2Threads, sm_dq, st>>>(tk64, tv64, p);
+  vs_bwd_dq_kernel<D><<<unsigned(int64_t(T) * sh->B * sh->Hq), kDqThreads, sm_dq, st>>>(tk64, tv64, p);
   trace_end(st);
   note_launch(4);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
