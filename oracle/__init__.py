@@ -180,7 +180,8 @@ class _Problem(ctypes.Structure):
                 ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("n_global", ctypes.c_int64),
                 ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dout", ctypes.c_void_p),
                 ("qpos", ctypes.c_void_p), ("kpos", ctypes.c_void_p), ("iv", ctypes.c_void_p),
-                ("is_", ctypes.c_void_p), ("kv", ctypes.c_int), ("ks", ctypes.c_int), ("scale", ctypes.c_double)]
+                ("is_", ctypes.c_void_p), ("kv", ctypes.c_int), ("ks", ctypes.c_int), ("scale", ctypes.c_double),
+                ("block", ctypes.c_int)]
 
 
 class Problem:
@@ -189,10 +190,13 @@ class Problem:
     q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d], dout [B, Nq, Hq, d] or None;
     iv [B, Hq, kv] and is_ [B, Hq, ks] index the global sequence of length
     ``n_global``; qpos / kpos give each local row's / key's global position
-    (identity when None).
+    (identity when None).  block=True selects the block-cover reading of the
+    slashes (section 4.1 (ii): slashes aggregated over 64 x 64 blocks): every
+    causal entry of a 64 x 64 block (on global positions) that a selected
+    slash passes through is in the mask, besides the selected columns.
     """
 
-    def __init__(self, q, k, v, iv, is_, scale, dout=None, qpos=None, kpos=None, n_global=None):
+    def __init__(self, q, k, v, iv, is_, scale, dout=None, qpos=None, kpos=None, n_global=None, block=False):
         self.q, self.k, self.v = _f64(q), _f64(k), _f64(v)
         self.dout = None if dout is None else _f64(dout)
         B, Nq, Hq, d = self.q.shape
@@ -209,7 +213,7 @@ class Problem:
         self._c = _Problem(B, Nq, Nk, Hq, Hkv, d, self.n_global, self.q.ctypes.data, self.k.ctypes.data,
                            self.v.ctypes.data, None if self.dout is None else self.dout.ctypes.data,
                            self.qpos.ctypes.data, self.kpos.ctypes.data, self.iv.ctypes.data, self.is_.ctypes.data,
-                           self.iv.shape[2], self.is_.shape[2], self.scale)
+                           self.iv.shape[2], self.is_.shape[2], self.scale, int(bool(block)))
 
     def ref(self):
         return ctypes.byref(self._c)

@@ -53,9 +53,10 @@ typedef struct {
   const int32_t* is;     /* [B][Hq][ks] selected offsets n-m */
   int kv, ks;
   double scale;
+  int block; /* 0: the exact token mask; 1: block-cover slashes (see mask_row) */
 } ora_problem;
 
-int ora_version(void) { return 3; }
+int ora_version(void) { return 4; }
 
 int ora_num_threads(void) {
 #ifdef _OPENMP
@@ -143,6 +144,7 @@ void ora_estimate(int B, int N, int Hq, int Hkv, int d, const double* q, const d
 typedef struct {
   unsigned char* vsel; /* vsel[c] = 1 iff c in iv */
   unsigned char* ssel; /* ssel[o] = 1 iff o in is */
+  unsigned char* bact; /* block mode: bact[D] = 1 iff a selected slash passes through a 64x64 block of block diagonal D */
   int64_t* loc;        /* global key position -> local key index, or -1 */
 } ora_tables;
 
@@ -160,11 +162,30 @@ static void tables_build(const ora_problem* p, int b, int h, ora_tables* t) {
     if (iv[j] >= 0) t->vsel[iv[j]] = 1;
   for (int j = 0; j < p->ks; ++j)
     if (is[j] >= 0) t->ssel[is[j]] = 1;
+  /* block diagonal D holds the blocks (I, I - D); the slash at offset o
+   * passes through one of them iff some n - m = o with n, m in blocks I and
+   * I - D, i.e. iff |o - 64 D| <= 63 */
+  const int64_t nd = G / 64 + 1;
+  t->bact = (unsigned char*)calloc((size_t)nd, 1);
+  for (int64_t D = 0; D < nd; ++D)
+    for (int64_t o = 64 * D - 63; o <= 64 * D + 63; ++o)
+      if (o >= 0 && o < G && t->ssel[o]) {
+        t->bact[D] = 1;
+        break;
+      }
 }
 static void tables_free(ora_tables* t) {
   free(t->vsel);
   free(t->ssel);
+  free(t->bact);
   free(t->loc);
+}
+
+/* Capacity of a row's key list: distinct keys, at most one per list entry
+ * (exact mask) or any key (block cover). */
+static size_t row_cap(const ora_problem* p) {
+  const int64_t lists = (int64_t)p->kv + p->ks;
+  return (size_t)((p->block || lists > p->Nk ? p->Nk : lists) + 1);
 }
 
 /* Enumerates M(n) for local query row n: local key indices m with
@@ -175,6 +196,16 @@ static int mask_row(const ora_problem* p, int b, int h, const ora_tables* t, int
   const int32_t* iv = p->iv + ((size_t)b * p->Hq + h) * p->kv;
   const int32_t* is = p->is + ((size_t)b * p->Hq + h) * p->ks;
   int cnt = 0;
+  if (p->block) {
+    /* block cover: every causal entry of a 64x64 block that a selected slash
+     * passes through, plus the selected columns */
+    for (int m = 0; m < p->Nk; ++m) {
+      const int64_t pm = p->kpos[m];
+      if (pm > pn) continue;
+      if (t->vsel[pm] || t->bact[(pn >> 6) - (pm >> 6)]) out[cnt++] = m;
+    }
+    return cnt;
+  }
   for (int j = 0; j < p->ks; ++j) { /* slash entries */
     if (is[j] < 0) continue;
     const int64_t pm = pn - is[j];
@@ -203,7 +234,7 @@ int64_t ora_mask_count(const ora_problem* p) {
       int64_t part = 0;
 #pragma omp parallel
       {
-        int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->kv + p->ks + 1));
+        int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * row_cap(p));
 #pragma omp for reduction(+ : part) schedule(static)
         for (int n = 0; n < p->Nq; ++n) part += mask_row(p, b, h, &t, n, keys);
         free(keys);
@@ -218,7 +249,7 @@ int64_t ora_mask_count(const ora_problem* p) {
 void ora_mask_dense(const ora_problem* p, int b, int h, unsigned char* out) {
   ora_tables t;
   tables_build(p, b, h, &t);
-  int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->kv + p->ks + 1));
+  int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * row_cap(p));
   memset(out, 0, (size_t)p->Nq * p->Nk);
   for (int n = 0; n < p->Nq; ++n) {
     int c = mask_row(p, b, h, &t, n, keys);
@@ -274,8 +305,8 @@ void ora_row_stats(const ora_problem* p, int nrows, const int32_t* rows, double*
     const int b = rows[3 * r], h = rows[3 * r + 1], n = rows[3 * r + 2];
     ora_tables t;
     tables_build(p, b, h, &t);
-    int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->kv + p->ks + 1));
-    double* logit = (double*)malloc(sizeof(double) * (size_t)(p->kv + p->ks + 1));
+    int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * row_cap(p));
+    double* logit = (double*)malloc(sizeof(double) * row_cap(p));
     row_stats(p, b, h, &t, n, keys, logit, &lse[r], p->dout ? &D[r] : NULL);
     free(keys);
     free(logit);
@@ -301,8 +332,8 @@ void ora_rows(const ora_problem* p, int nrows, const int32_t* rows, double* o, d
       const int hk = h / (p->Hq / p->Hkv);
 #pragma omp parallel
       {
-        int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->kv + p->ks + 1));
-        double* logit = (double*)malloc(sizeof(double) * (size_t)(p->kv + p->ks + 1));
+        int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * row_cap(p));
+        double* logit = (double*)malloc(sizeof(double) * row_cap(p));
 #pragma omp for schedule(dynamic, 16)
         for (int r = 0; r < nrows; ++r) {
           if (rows[3 * r] != b || rows[3 * r + 1] != h) continue;
@@ -357,8 +388,8 @@ void ora_keys(const ora_problem* p, int nkeys, const int32_t* keys_in, double* d
         tables_build(p, b, h, &t);
 #pragma omp parallel
         {
-          int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->kv + p->ks + 1));
-          double* logit = (double*)malloc(sizeof(double) * (size_t)(p->kv + p->ks + 1));
+          int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * row_cap(p));
+          double* logit = (double*)malloc(sizeof(double) * row_cap(p));
 #pragma omp for schedule(dynamic, 64)
           for (int n = 0; n < p->Nq; ++n) row_stats(p, b, h, &t, n, keys, logit, &L[n], &D[n]);
           free(keys);
