@@ -181,6 +181,14 @@ static void tables_free(ora_tables* t) {
   free(t->loc);
 }
 
+/* Membership of the key at global position pm in the mask row of the query
+ * at global position pn (the same rule mask_row enumerates). */
+static int in_mask(const ora_problem* p, const ora_tables* t, int64_t pn, int64_t pm) {
+  if (pm > pn) return 0;
+  if (t->vsel[pm]) return 1;
+  return p->block ? t->bact[(pn >> 6) - (pm >> 6)] : t->ssel[pn - pm];
+}
+
 /* Capacity of a row's key list: distinct keys, at most one per list entry
  * (exact mask) or any key (block cover). */
 static size_t row_cap(const ora_problem* p) {
@@ -395,8 +403,7 @@ void ora_keys(const ora_problem* p, int nkeys, const int32_t* keys_in, double* d
           free(keys);
           free(logit);
         }
-        /* membership of key m in row n's mask: kpos[m] <= qpos[n] and
-         * (kpos[m] in iv or qpos[n]-kpos[m] in is) */
+        /* membership of key m in row n's mask (in_mask) */
 #pragma omp parallel for schedule(dynamic, 1)
         for (int r = 0; r < nkeys; ++r) {
           if (keys_in[3 * r] != b || keys_in[3 * r + 1] != hk) continue;
@@ -406,8 +413,7 @@ void ora_keys(const ora_problem* p, int nkeys, const int32_t* keys_in, double* d
           const double* vm = p->v + (((size_t)b * p->Nk + m) * p->Hkv + hk) * d;
           for (int n = 0; n < p->Nq; ++n) {
             const int64_t pn = p->qpos[n];
-            if (pm > pn) continue;
-            if (!(t.vsel[pm] || t.ssel[pn - pm])) continue;
+            if (!in_mask(p, &t, pn, pm)) continue;
             const double* qn = p->q + (((size_t)b * p->Nq + n) * p->Hq + h) * d;
             const double* don = p->dout + (((size_t)b * p->Nq + n) * p->Hq + h) * d;
             const double A = exp(p->scale * dotd(qn, km, d) - L[n]);

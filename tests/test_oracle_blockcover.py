@@ -60,3 +60,19 @@ def test_every_offset_is_full_causal():
     iv = np.full((1, 1, 1), -1, np.int32)
     is_ = np.arange(0, N, 64, dtype=np.int32).reshape(1, 1, -1)  # one slash per block diagonal
     assert oracle.mask_count(_p(N, iv, is_)) == N * (N + 1) // 2
+
+
+def test_block_attention_equals_full_causal_when_every_diagonal_is_active():
+    # one slash per block diagonal activates every block: the block mask is
+    # the full causal mask, so every output (dK / dV included) equals the
+    # exact computation with every offset selected
+    rng = np.random.default_rng(4)
+    N, d = 256, 8
+    q, k, v, do = (rng.standard_normal((1, N, 1, d)) for _ in range(4))
+    iv = np.full((1, 1, 1), -1, np.int32)
+    blk = oracle.attention(oracle.Problem(q, k, v, iv, np.arange(0, N, 64, dtype=np.int32).reshape(1, 1, -1), 0.3,
+                                          dout=do, block=True))
+    full = oracle.attention(oracle.Problem(q, k, v, iv, np.arange(N, dtype=np.int32).reshape(1, 1, -1), 0.3,
+                                           dout=do))
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_allclose(blk[key], full[key], rtol=1e-12, atol=1e-12)
