@@ -69,6 +69,8 @@ def lib(build_if_missing: bool = True):
     L.vs_block_index_bytes.restype = ctypes.c_size_t
     L.vs_build_block_index.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vs_stripe), _P,
                                        ctypes.c_size_t, _P]
+    L.vs_build_block_index_ex.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vs_stripe),
+                                          ctypes.c_int, _P, ctypes.c_size_t, _P]
     L.vs_index_counts.argtypes = [_P, _P, _P]
     L.vs_attn_fwd_workspace.argtypes = [_S]
     L.vs_attn_fwd_workspace.restype = ctypes.c_size_t
@@ -212,8 +214,13 @@ def make_stripe(world: int, q_rank: int, kv_rank: int, N_global: int, stripe: in
     return vs_stripe(world, stripe, q_rank, kv_rank, N_global)
 
 
-def vs_build_block_index(q, k, v_idx, s_idx, stripe: Optional[vs_stripe] = None, arena=None, stream=None):
-    """Sparse index arena (uint8 device tensor) for the shape of q / k."""
+VS_INDEX_BLOCK_COVER = 1
+
+
+def vs_build_block_index(q, k, v_idx, s_idx, stripe: Optional[vs_stripe] = None, arena=None, stream=None,
+                         block_cover: bool = False):
+    """Sparse index arena (uint8 device tensor) for the shape of q / k;
+    block_cover selects the block-cover reading of the slashes."""
     sh = make_shape(q, k)
     kv, ks = v_idx.shape[-1], s_idx.shape[-1]
     sp = ctypes.byref(stripe) if stripe is not None else None
@@ -221,8 +228,9 @@ def vs_build_block_index(q, k, v_idx, s_idx, stripe: Optional[vs_stripe] = None,
     if need == 0:
         raise VSError(VS_ERR_SHAPE, "vs_block_index_bytes")
     arena = torch.empty(need, dtype=torch.uint8, device=q.device) if arena is None else arena
-    _check(lib().vs_build_block_index(ctypes.byref(sh), _ptr(v_idx), _ptr(s_idx), kv, ks, sp, _ptr(arena),
-                                      arena.numel(), _stream(stream)), "vs_build_block_index")
+    _check(lib().vs_build_block_index_ex(ctypes.byref(sh), _ptr(v_idx), _ptr(s_idx), kv, ks, sp,
+                                         VS_INDEX_BLOCK_COVER if block_cover else 0, _ptr(arena), arena.numel(),
+                                         _stream(stream)), "vs_build_block_index")
     return arena
 
 

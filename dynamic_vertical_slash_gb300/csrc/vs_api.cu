@@ -230,6 +230,13 @@ size_t vs_block_index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* 
 
 vs_status vs_build_block_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                                const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t stream) {
+  return vs_build_block_index_ex(s, v_idx, s_idx, kv, ks, stripe, 0, arena, arena_bytes, stream);
+}
+
+vs_status vs_build_block_index_ex(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
+                                  const vs_stripe* stripe, int flags, void* arena, size_t arena_bytes,
+                                  cudaStream_t stream) {
+  if (flags & ~int(VS_INDEX_BLOCK_COVER)) return VS_ERR_ARG;
   vs_status rc = check_shape(s);
   if (rc != VS_OK) return rc;
   if (!v_idx || !s_idx || !arena) return VS_ERR_ARG;
@@ -246,7 +253,7 @@ vs_status vs_build_block_index(const vs_shape* s, const int32_t* v_idx, const in
   if (kv < 1 || ks < 1 || kv > NG || ks > NG) return VS_ERR_ARG;
   if (!aligned16(arena)) return VS_ERR_ARG;
   if (arena_bytes < index_bytes(s, kv, ks, stripe, nullptr)) return VS_ERR_WORKSPACE;
-  return launch_index(s, v_idx, s_idx, kv, ks, stripe, arena, arena_bytes, stream);
+  return launch_index(s, v_idx, s_idx, kv, ks, stripe, flags, arena, arena_bytes, stream);
 }
 
 vs_status vs_index_counts(const void* arena, int64_t* out, cudaStream_t stream) {

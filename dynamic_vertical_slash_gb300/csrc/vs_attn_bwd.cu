@@ -190,10 +190,9 @@ __device__ __forceinline__ int dq_load_unit(uint8_t (*slot)[kDqPairKeys * 128], 
   return 0;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kDqThreads, 1)
-    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const BwdParams p) {
+// Kernel body, compiled once per mask reading (BLOCK: block-cover slashes).
+template <int D, bool BLOCK>
+__device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMap& tmV, const BwdParams& p) {
   extern __shared__ uint8_t smem_raw[];
   DqSmem<D>& s = *reinterpret_cast<DqSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -386,6 +385,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int64_t n_g = qpos_g(G, n_loc);
     const uint64_t* offbits = av.offbits + int64_t(bh) * G.WG;
     const uint64_t* colbits = av.colbits + int64_t(bh) * G.WG;
+    // block cover: the row's two candidate block diagonals instead of its
+    // offset window
+    constexpr bool block_cover = BLOCK;
+    const uint64_t* diagbits = block_cover ? av.bdbits + int64_t(bh) * G.WG : offbits;
     float Lr = 0.f, Dr = 0.f;
     if (row_ok) {
       const BwdLayout L = bwd_layout_dev(av.hdr, D);
@@ -433,10 +436,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       // are globally contiguous).  The bitmap words are loaded here and used
       // after the scores arrive.
       const int64_t m0 = slash ? (c >= 0 ? kpos_g(G, c) : c) : 0;
-      const int64_t lo = n_g - m0 - 63;
+      const int64_t lo = block_cover ? (n_g >> 6) - (m0 >> 6) - 1 : n_g - m0 - 63;
       const int64_t wo = lo >> 6, wc = m0 >> 6;
-      const uint64_t oa = (slash && wo >= 0 && wo < G.WG) ? __ldg(offbits + wo) : 0ull;
-      const uint64_t ob = (slash && wo + 1 >= 0 && wo + 1 < G.WG) ? __ldg(offbits + wo + 1) : 0ull;
+      const uint64_t oa = (slash && wo >= 0 && wo < G.WG) ? __ldg(diagbits + wo) : 0ull;
+      const uint64_t ob = (slash && wo + 1 >= 0 && wo + 1 < G.WG) ? __ldg(diagbits + wo + 1) : 0ull;
       const uint64_t ca = (slash && wc >= 0 && wc < G.WG) ? __ldg(colbits + wc) : 0ull;
       const uint64_t cb = (slash && wc + 1 >= 0 && wc + 1 < G.WG) ? __ldg(colbits + wc + 1) : 0ull;
       ok = mbar_wait(&s.s_full, i & 1, ab, VS_ERR_TIMEOUT);
@@ -458,7 +461,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int so = int(lo & 63), sc = int(m0 & 63);
         const uint64_t x = so ? ((oa >> so) | (ob << (64 - so))) : oa;
         const uint64_t cw = sc ? ((ca >> sc) | (cb << (64 - sc))) : ca;
-        mask = __brevll(x) & ~cw & (c < 0 ? ((~0ull) << (-c)) : ~0ull);
+        const uint64_t keep = ~cw & (c < 0 ? ((~0ull) << (-c)) : ~0ull);
+        if (block_cover) {
+          // keys below the split are in the first key block (diagonal bit 1),
+          // the rest in the next one (bit 0); causal keys only
+          const uint64_t lo_keys = low_bits(64 - (m0 & 63));
+          mask = (((x & 2ull) ? lo_keys : 0ull) | ((x & 1ull) ? ~lo_keys : 0ull)) & low_bits(n_g - m0 + 1) & keep;
+        } else {
+          mask = __brevll(x) & keep;
+        }
       } else if (row_ok && c == kUnitBar) {
         const int64_t* pos = s.bar_pos[ks][half];
         int cnt = 0;
@@ -559,6 +570,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   }
 }
 
+template <int D>
+__global__ void __launch_bounds__(kDqThreads, 1)
+    vs_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const BwdParams p) {
+  if (arena_view(p.arena).hdr->block_cover) dq_body<D, true>(tmK, tmV, p);
+  else dq_body<D, false>(tmK, tmV, p);
+}
+
 // ------------------------------------------------------ key-major dK / dV
 // TMEM: dK [0, 128), dV [128, 256), S^T [256, 320), dP^T [320, 384),
 //       P^T x2 [384, 448), dS^T x2 [448, 512)
@@ -600,11 +619,9 @@ struct KvWork {
   int64_t row0;      // bar: first row of the split
 };
 
-template <int D, bool BAR>
-__global__ void __launch_bounds__(kIssue2Threads, 1)
-    vs_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
-                     const BwdParams p) {
+template <int D, bool BAR, bool BLOCK>
+__device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
+                                        const CUtensorMap& tmG, const BwdParams& p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   KvSmem<D>& s = *reinterpret_cast<KvSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -840,6 +857,7 @@ __global__ void __launch_bounds__(kIssue2Threads, 1)
     else kl = k0 + r;
     const bool key_ok = run && kl >= 0 && kl < p.Nk;
     const int64_t m_g = key_ok ? kpos_g(G, kl) : 0;
+    constexpr bool block_cover = BLOCK;
     if (run) {
       // K row of key r, d columns [half D/2, (half + 1) D/2), into TMEM
       uint32_t w[D / 4];
@@ -890,7 +908,9 @@ __global__ void __launch_bounds__(kIssue2Threads, 1)
           mask = valid;
         } else {
           const uint64_t vw = __ldg(av.vlocbits + bh * G.WL + (kl >> 6));
-          if (!((vw >> (kl & 63)) & 1ull)) mask = slash_col_mask(G, av.offbits + bh * G.WG, kl, r0);
+          if (!((vw >> (kl & 63)) & 1ull))
+            mask = block_cover ? block_col_mask(G, av.bdbits + bh * G.WG, kl, r0)
+                               : slash_col_mask(G, av.offbits + bh * G.WG, kl, r0);
         }
       }
       const uint32_t hm = uint32_t(mask >> (32 * half));
@@ -1056,6 +1076,16 @@ __global__ void __launch_bounds__(kIssue2Threads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Bars hold whole columns: only the slash kernel depends on the reading.
+template <int D, bool BAR>
+__global__ void __launch_bounds__(kIssue2Threads, 1)
+    vs_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                     const BwdParams p) {
+  if (!BAR && arena_view(p.arena).hdr->block_cover) kv_body<D, BAR, true>(tmK, tmV, tmQ, tmG, p);
+  else kv_body<D, BAR, false>(tmK, tmV, tmQ, tmG, p);
 }
 
 BwdParams make_params(const vs_shape* sh, const void* q, const void* k, const void* v, const void* o,

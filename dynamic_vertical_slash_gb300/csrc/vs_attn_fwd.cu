@@ -53,13 +53,15 @@ constexpr float kRefSlack = 18446744073709551616.0f;  // 2^64: largest masked pa
 //     row's mask is the prefix of keys at or before it.
 struct MaskRec {
   int kind;  // 0: no unit (odd last pair), 1: slash tile, 2: bar chunk
-  int lo6[2];
-  uint64_t W[6];
-  uint64_t keep;
+  int lo6[2];         // bit offsets of the row blocks' windows in W
+  uint64_t W[6];      // per row block, three words of the offset bitmap around its window
+  uint64_t keep[2];   // per row block: keys that may be set (not a selected column, existing, and
+                      // in block-cover mode on an active block diagonal of that row block)
   int64_t kg[kKTile];
 };
 
 // Row r's mask (bit k: key k of the unit) from its unit's record.
+template <bool BLOCK>
 __device__ __forceinline__ uint64_t rec_row_mask(const MaskRec& rc, int kind, int r, int64_t ng) {
   if (kind == 1) {
     const int blk = r >> 6;
@@ -67,7 +69,7 @@ __device__ __forceinline__ uint64_t rec_row_mask(const MaskRec& rc, int kind, in
     const uint64_t a = rc.W[3 * blk + (o >> 6)], b = rc.W[3 * blk + (o >> 6) + 1];
     const int sh = o & 63;
     const uint64_t x = sh ? ((a >> sh) | (b << (64 - sh))) : a;
-    return __brevll(x) & rc.keep;
+    return __brevll(x) & rc.keep[BLOCK ? blk : 0];
   }
   if (kind == 2) {
     int pos = 0;
@@ -272,10 +274,11 @@ __device__ __noinline__ RowRef fwd_rebase_second(uint32_t tl, uint32_t colS, uin
   return RowRef{m_run, l_run};
 }
 
-template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
-    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+// The kernel body, compiled once per mask reading (BLOCK: block-cover
+// slashes) so that neither reading carries the other's code.
+template <int D, bool BLOCK>
+__device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                         const FwdParams& p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -440,6 +443,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // trip; runs as far ahead as the record ring allows.
     const uint64_t* offbits_p = av.offbits + int64_t(bh) * G.WG;
     const uint64_t* colbits_p = av.colbits + int64_t(bh) * G.WG;
+    constexpr bool block_cover = BLOCK;
+    const uint64_t* bdbits_p = av.bdbits + int64_t(bh) * G.WG;
     int e_win = -1, e_pref = 0;  // elist[32 e_win + lane]
     for (int i = 0; i < P; ++i) {
       const int ri = i % kRecRing;
@@ -472,8 +477,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (hh < 2 && kh == 1) {
           const int64_t la = sec ? L0a[1] : L0a[0], lb = sec ? L0b[1] : L0b[0], mm = sec ? m0[1] : m0[0];
           const int64_t w = j < 6 ? (((j < 3 ? la : lb) >> 6) + j % 3) : ((mm >> 6) + (j - 6));
-          const uint64_t* bm = j < 6 ? offbits_p : colbits_p;
-          wv = (w >= 0 && w < G.WG) ? __ldg(bm + w) : 0ull;
+          if (block_cover && j < 6) {
+            // block cover: the words of "offset >= 0" (the causal entries);
+            // the active block diagonals go into the row blocks' keep masks
+            const int64_t base = 64 * w;
+            wv = base >= 0 ? ~0ull : ~low_bits(-base);
+          } else {
+            const uint64_t* bm = j < 6 ? offbits_p : colbits_p;
+            wv = (w >= 0 && w < G.WG) ? __ldg(bm + w) : 0ull;
+          }
+        } else if (block_cover && lane >= 16 && lane < 20) {
+          // lanes 16 + 2 u + b: unit u, row block b: the diagonals through
+          // the unit's two key blocks (bits D2 = I - J - 1 and D2 + 1)
+          const int u = (lane - 16) >> 1, rb = lane & 1;
+          if (kind[u] == 1) {
+            const int64_t D2 = (qpos_g(G, int64_t(t) * kQTile + 64 * rb) >> 6) - (m0[u] >> 6) - 1;
+            wv = bits64(bdbits_p, D2, G.WG) & 3ull;
+          }
         }
       }
       int key[2][2];
@@ -488,13 +508,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         MaskRec& rc = s.rec[ri][hh];
         if (kind[hh] == 1) {
           const uint64_t c1 = __shfl_sync(0xffffffffu, wv, 8 * hh + 7);
+          const uint64_t a0 = __shfl_sync(0xffffffffu, wv, 16 + 2 * hh), a1 = __shfl_sync(0xffffffffu, wv, 17 + 2 * hh);
           if ((lane >> 3) == hh) {
             const int j = lane & 7;
             if (j < 6) rc.W[j] = wv;
             if (j == 6) {
               const int shc = int(m0[hh] & 63);
               const uint64_t colw = shc ? ((wv >> shc) | (c1 << (64 - shc))) : wv;
-              rc.keep = ~colw & ((cc[hh] < 0) ? ((~0ull) << (-cc[hh])) : ~0ull);
+              const uint64_t keep = ~colw & ((cc[hh] < 0) ? ((~0ull) << (-cc[hh])) : ~0ull);
+              if (block_cover) {
+                // keys below the split lie in the first key block (diagonal
+                // D2 + 1, bit 1), the rest in the next (D2, bit 0)
+                const uint64_t lo_keys = low_bits(64 - (m0[hh] & 63));
+                rc.keep[0] = keep & (((a0 & 2ull) ? lo_keys : 0ull) | ((a0 & 1ull) ? ~lo_keys : 0ull));
+                rc.keep[1] = keep & (((a1 & 2ull) ? lo_keys : 0ull) | ((a1 & 1ull) ? ~lo_keys : 0ull));
+              } else {
+                rc.keep[0] = rc.keep[1] = keep;
+              }
             }
           }
           if (lane == 0) {
@@ -574,8 +604,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const MaskRec& rc0 = s.rec[ri][0];
       const MaskRec& rc1 = s.rec[ri][1];
-      const uint64_t mask0 = row_ok ? rec_row_mask(rc0, rc0.kind, r, n_g) : 0ull;
-      const uint64_t mask1 = row_ok ? rec_row_mask(rc1, rc1.kind, r, n_g) : 0ull;
+      const uint64_t mask0 = row_ok ? rec_row_mask<BLOCK>(rc0, rc0.kind, r, n_g) : 0ull;
+      const uint64_t mask1 = row_ok ? rec_row_mask<BLOCK>(rc1, rc1.kind, r, n_g) : 0ull;
       mbar_arrive(&s.rec_empty[ri]);
       // P against the row's reference maximum m_run (log2 units), one unit at
       // a time.  The reference is lazy: it only moves when a unit's masked sum
@@ -740,6 +770,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmQ, tmK, tmV, p);
+  else fwd_body<D, false>(tmQ, tmK, tmV, p);
 }
 
 template <int D>

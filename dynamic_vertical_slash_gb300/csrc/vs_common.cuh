@@ -30,10 +30,11 @@ struct ArenaHeader {
   int32_t EMAX;     // capacity of the e / f lists
   int32_t KVP;      // capacity of the vertical list (kv rounded up to 128)
   int32_t sheared;  // 1: unstriped sheared cover; 0: block-aligned striped cover
-  int32_t pad0;
+  int32_t block_cover;  // 1: slashes cover whole 64 x 64 blocks (bdbits); 0: the exact token mask
   int64_t off_offbits, off_colbits, off_elist, off_ecount, off_flist, off_fcount;
   int64_t off_vlist, off_vcount, off_vlocbits, off_vlocpre, off_counts;
   int64_t total_bytes;
+  int64_t off_bdbits;
 };
 static_assert(sizeof(ArenaHeader) <= 256, "arena header exceeds 256 bytes");
 
@@ -50,6 +51,7 @@ struct ArenaView {
   const int32_t* vcount;     // [BH]
   const uint64_t* vlocbits;  // [BH][WL]   bit k: local key k is a selected column
   const int32_t* vlocpre;    // [BH][WL]   selected columns in words before w
+  const uint64_t* bdbits;    // [BH][WG]   block mode: bit D: a selected slash passes through block diagonal D
 };
 
 __host__ __device__ inline ArenaView arena_view(const void* base) {
@@ -67,7 +69,13 @@ __host__ __device__ inline ArenaView arena_view(const void* base) {
   v.vcount = reinterpret_cast<const int32_t*>(p + h->off_vcount);
   v.vlocbits = reinterpret_cast<const uint64_t*>(p + h->off_vlocbits);
   v.vlocpre = reinterpret_cast<const int32_t*>(p + h->off_vlocpre);
+  v.bdbits = reinterpret_cast<const uint64_t*>(p + h->off_bdbits);
   return v;
+}
+
+// The low n bits set (n clipped to [0, 64]).
+__host__ __device__ __forceinline__ uint64_t low_bits(int64_t n) {
+  return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1));
 }
 
 // Plain (host-side) copy of the geometry the kernels need, passed by value.

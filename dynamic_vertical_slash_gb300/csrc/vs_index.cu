@@ -17,7 +17,11 @@
 //   vlist              selected columns that live in this key shard, as local
 //                      key indices, ascending, padded with -1;
 //   vlocbits/vlocpre   the same as a bitmap with word prefix counts;
-//   counts             work units of the four attention passes.
+//   counts             work units of the four attention passes;
+//   bdbits             block-cover mode: bit D set iff a selected offset o has
+//                      |o - 64 D| <= 63, i.e. a selected slash passes through
+//                      the 64 x 64 blocks of block diagonal D; the sheared cover
+//                      is then built over the offsets of those blocks.
 #include "vs_internal.h"
 
 namespace vs {
@@ -63,6 +67,7 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   uint64_t* vloc = reinterpret_cast<uint64_t*>(A + H.off_vlocbits) + int64_t(bh) * H.WL;
   int32_t* vpre = reinterpret_cast<int32_t*>(A + H.off_vlocpre) + int64_t(bh) * H.WL;
   int64_t* counts = reinterpret_cast<int64_t*>(A + H.off_counts) + int64_t(bh) * 4;
+  uint64_t* bdbits = reinterpret_cast<uint64_t*>(A + H.off_bdbits) + int64_t(bh) * H.WG;
   const int32_t* iv = P.v_idx + int64_t(bh) * H.kv;
   const int32_t* is = P.s_idx + int64_t(bh) * H.ks;
   const int64_t NG = H.N_global;
@@ -86,6 +91,7 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   // 2. clear bitmaps
   for (int w = tid; w < H.WG; w += kIdxThreads) offbits[w] = colbits[w] = 0ull;
   for (int w = tid; w < H.WL; w += kIdxThreads) vloc[w] = 0ull;
+  for (int w = tid; w < H.WG; w += kIdxThreads) bdbits[w] = 0ull;
   __syncthreads();
   if (bad) {
     if (tid == 0) {
@@ -116,6 +122,17 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   }
   __threadfence_block();
   __syncthreads();
+  // 3b. block cover: the active block diagonals
+  const int64_t ndiag = NG / kBlk + 1;
+  if (H.block_cover) {
+    for (int64_t w = tid; w * 64 < ndiag; w += kIdxThreads) {
+      uint64_t word = 0;
+      for (int k = 0; k < 64 && w * 64 + k < ndiag; ++k)
+        if (block_diag_active(offbits, H.WG, w * 64 + k)) word |= 1ull << k;
+      bdbits[w] = word;
+    }
+    __syncthreads();
+  }
   // 4. local vertical list from the local bitmap (ascending by construction)
   const int per = (H.WL + kIdxThreads - 1) / kIdxThreads;
   const int w0 = tid * per, w1 = min(H.WL, w0 + per);
@@ -152,13 +169,34 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   // 5. slash cover and 6. work counts (sequential; lists are short)
   if (tid == 0) {
     int ne = 0, nf = 0;
+    // block cover: the smallest offset >= x inside an active block diagonal's
+    // offsets [64 D - 63, 64 D + 63], or -1
+    auto next_eff = [&](int64_t x) -> int64_t {
+      int64_t D = x <= 0 ? 0 : x / kBlk;  // the first D with 64 D + 63 >= x
+      while (D < ndiag) {
+        const uint64_t wrd = bdbits[D >> 6] & ((~0ull) << (D & 63));
+        if (wrd) {
+          const int64_t Da = (D >> 6) * 64 + __ffsll(wrd) - 1;  // first active diagonal >= D
+          return Da < ndiag ? max(max(x, int64_t(0)), Da * kBlk - 63) : -1;
+        }
+        D = ((D >> 6) + 1) * 64;
+      }
+      return -1;
+    };
     if (H.sheared) {
       int64_t cur = 0;
       int j = 0;
       while (true) {
-        while (j < nks && is[j] < cur - 127) ++j;
-        if (j == nks) break;
-        const int64_t u = max(cur, int64_t(is[j]));
+        int64_t o;
+        if (H.block_cover) {
+          o = next_eff(cur - 127);
+          if (o < 0) break;
+        } else {
+          while (j < nks && is[j] < cur - 127) ++j;
+          if (j == nks) break;
+          o = is[j];
+        }
+        const int64_t u = max(cur, o);
         if (u > int64_t(H.Nq) + 126 || ne >= H.EMAX) break;
         elist[ne] = int32_t(u);
         flist[ne] = int32_t(u);
@@ -249,15 +287,17 @@ size_t index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* stripe, A
   h.off_vlocbits = take(BH * h.WL * 8);
   h.off_vlocpre = take(BH * h.WL * 4);
   h.off_counts = take(BH * 4 * 8);
+  h.off_bdbits = take(BH * h.WG * 8);
   h.total_bytes = off;
   if (out) *out = h;
   return size_t(off);
 }
 
 vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
-                       const vs_stripe* stripe, void* arena, size_t, cudaStream_t st) {
+                       const vs_stripe* stripe, int flags, void* arena, size_t, cudaStream_t st) {
   IndexParams P;
   index_bytes(s, kv, ks, stripe, &P.hdr);
+  P.hdr.block_cover = (flags & VS_INDEX_BLOCK_COVER) ? 1 : 0;
   P.arena = static_cast<uint8_t*>(arena);
   P.v_idx = v_idx;
   P.s_idx = s_idx;

@@ -44,7 +44,7 @@ size_t ring_work_smem(int64_t N, int W);
 vs_status launch_ring_work(int B, int H, int64_t N, const int32_t* v_idx, int kv, const int32_t* s_idx, int ks,
                            int world, int layout, int64_t* out, int* err, cudaStream_t st);
 vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
-                       const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t st);
+                       const vs_stripe* stripe, int flags, void* arena, size_t arena_bytes, cudaStream_t st);
 size_t index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* stripe, ArenaHeader* hdr_out);
 vs_status launch_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int stripe,
                          int inverse, int only_rank, cudaStream_t st);

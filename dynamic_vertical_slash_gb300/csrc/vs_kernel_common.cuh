@@ -89,6 +89,19 @@ __device__ __forceinline__ uint64_t slash_col_mask(const Geo& G, const uint64_t*
   return m;
 }
 
+// Block-cover counterpart of slash_col_mask: bit i set iff row r0 + i exists,
+// is causal for the key (n_g >= m_g), and the 64 x 64 block of (row, key)
+// lies on an active block diagonal (bdbits).  The unit's 64 rows are globally
+// contiguous, so they span at most two row blocks.
+__device__ __forceinline__ uint64_t block_col_mask(const Geo& G, const uint64_t* bdbits, int64_t kl, int64_t r0) {
+  const int64_t n0 = qpos_g(G, r0), m = kpos_g(G, kl);
+  const uint64_t a = bits64(bdbits, (n0 >> 6) - (m >> 6), G.WG);  // bit 0: rows' first block, bit 1: the next
+  const uint64_t lo = low_bits(64 - (n0 & 63));
+  uint64_t mask = ((a & 1ull) ? lo : 0ull) | ((a & 2ull) ? ~lo : 0ull);
+  mask &= ~low_bits(m - n0);  // causal rows
+  return mask & low_bits(int64_t(G.Nq) - r0);
+}
+
 // Issues the cp.async gather of `nrows` key rows (index list `keys`, -1 =
 // zero row) of a [*, Hkv, d] bf16 tensor into a 128B-swizzled K-major tile:
 // row r, 16-byte chunk j of half hf lands at dst + hf*rows*128 + r*128 +

@@ -54,17 +54,19 @@ class VSAttention:
     estimator, the index build and the sparse kernels with fixed budgets
     kv / ks, or, when ``pv`` and ``ps`` are given, with per-head top-p
     budgets (Algorithm 1) of at most kv / ks entries (``budgets`` then holds
-    the [B, Hq] budgets of the last forward).  All tensors are BSHD bf16 on
-    the device.
+    the [B, Hq] budgets of the last forward).  ``block_cover`` selects the
+    block-cover reading of the slashes (whole 64 x 64 blocks, see
+    vs_build_block_index_ex).  All tensors are BSHD bf16 on the device.
     """
 
     def __init__(self, B: int, N: int, Hq: int, Hkv: int, d: int, kv: int, ks: int,
                  device="cuda", last_q: int = 64, scale: Optional[float] = None,
-                 pv: Optional[float] = None, ps: Optional[float] = None):
+                 pv: Optional[float] = None, ps: Optional[float] = None, block_cover: bool = False):
         self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N, Hq, Hkv, d, kv, ks
         if (pv is None) != (ps is None):
             raise ValueError("top-p mode needs both pv and ps")
         self.pv, self.ps = pv, ps
+        self.block_cover = block_cover
         self.last_q = last_q
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         dev = torch.device(device)
@@ -107,7 +109,7 @@ class VSAttention:
         else:
             self.v_idx.copy_(selection[0])
             self.s_idx.copy_(selection[1])
-        B_.vs_build_block_index(q, k, self.v_idx, self.s_idx, None, self.arena, stream)
+        B_.vs_build_block_index(q, k, self.v_idx, self.s_idx, None, self.arena, stream, self.block_cover)
         B_.vs_attn_fwd(q, k, v, self.arena, self.scale, self.o, self.lse, None, self.ws_fwd, stream)
         self._qkv = (q, k, v)
         return self.o, self.lse
@@ -155,9 +157,10 @@ class StripedWorker:
 
     def __init__(self, B: int, N_global: int, Hq: int, Hkv: int, d: int, kv: int, ks: int, world: int,
                  rank: int = 0, stripe: int = 64, device="cuda", last_q: int = 64, scale: Optional[float] = None,
-                 inner: int = 0):
+                 inner: int = 0, block_cover: bool = False):
         if N_global % (world * stripe):
             raise ValueError("N_global must be a multiple of world * stripe")
+        self.block_cover = block_cover
         if inner and world % inner:
             raise ValueError("world must be a multiple of the node size")
         self.inner = inner
@@ -217,7 +220,7 @@ class StripedWorker:
         """One index per ring step, on global positions through the stripe map."""
         for s in range(self.world):
             B_.vs_build_block_index(q_shard, k_shards[self.source(s)], self.v_idx, self.s_idx, self.stripes[s],
-                                    self.arenas[s], stream)
+                                    self.arenas[s], stream, self.block_cover)
 
     def forward(self, q_shard, k_shards, v_shards, stream=None):
         """World ring steps; each merges its partial (O, LSE) into the running

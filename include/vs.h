@@ -203,6 +203,21 @@ size_t vs_block_index_bytes(const vs_shape* shape, int kv, int ks, const vs_stri
 vs_status vs_build_block_index(const vs_shape* shape, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                                const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t stream);
 
+/* vs_build_block_index with flags.  VS_INDEX_BLOCK_COVER selects the
+ * block-cover reading of the slashes (section 4.1 (ii): slash lines
+ * aggregated over 64 x 64 token blocks to match the kernel tiling): the mask
+ * becomes
+ *     M[n, m] = (m <= n) and (m in v_idx or block diagonal
+ *               floor(n/64) - floor(m/64) is active),
+ * on global positions, where block diagonal D is active iff some selected
+ * offset o has |o - 64 D| <= 63 (the slash passes through its blocks).  The
+ * attention calls read the flag from the arena.  Other flag bits:
+ * VS_ERR_ARG. */
+enum { VS_INDEX_BLOCK_COVER = 1 };
+vs_status vs_build_block_index_ex(const vs_shape* shape, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
+                                  const vs_stripe* stripe, int flags, void* arena, size_t arena_bytes,
+                                  cudaStream_t stream);
+
 /* Work counts of an arena, for FLOP accounting (copies 4 x int64 per (b, h)
  * to host memory; synchronises the stream):
  *   [0] query-major slash tiles (128 x 64)    [1] query-major bar chunks (128 x 64)

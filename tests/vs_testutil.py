@@ -55,7 +55,7 @@ class Arena:
         self.h = dict(zip(HDR_FIELDS, i32[:12].tolist()))
         i64 = raw[:256].view(np.int64)
         self.N_global = int(i64[6])
-        self.WG, self.WL, self.EMAX, self.KVP, self.sheared = [int(x) for x in i32[14:19]]
+        self.WG, self.WL, self.EMAX, self.KVP, self.sheared, self.block_cover = [int(x) for x in i32[14:20]]
         offs = i64[10:22]
         names = ["offbits", "colbits", "elist", "ecount", "flist", "fcount", "vlist", "vcount", "vlocbits",
                  "vlocpre", "counts", "total"]
@@ -72,6 +72,8 @@ class Arena:
         self.vlist = g("vlist", np.int32, BH * self.KVP).reshape(BH, self.KVP)
         self.vcount = g("vcount", np.int32, BH)
         self.counts = g("counts", np.int64, BH * 4).reshape(BH, 4)
+        self.off["bdbits"] = int(i64[22])
+        self.bdbits = g("bdbits", np.uint64, BH * self.WG).reshape(BH, self.WG)
 
     def bit(self, bm_row, pos):
         pos = np.asarray(pos, np.int64)
@@ -89,6 +91,14 @@ class Arena:
         l = np.asarray(l, np.int64)
         return (W * (l >> 6) + r) * 64 + (l & 63)
 
+    def _slash(self, bh, ng, mg):
+        """Slash part of the mask at global (row, key) positions: the offset
+        selected (exact), or the block diagonal active (block cover)."""
+        off = ng - mg
+        if self.block_cover:
+            return self.bit(self.bdbits[bh], (ng >> 6) - (mg >> 6)) & (off >= 0)
+        return self.bit(self.offbits[bh], off) & (off >= 0)
+
     def coverage_query_major(self, bh):
         """Times each (row, key) entry is computed by the query-major passes."""
         Nq, Nk = self.h["Nq"], self.h["Nk"]
@@ -105,7 +115,7 @@ class Arena:
                 kk = keys[(keys >= 0) & (keys < Nk)]
                 mg = self.kpos(kk) if c >= 0 else kk
                 off = ng[:, None] - mg[None, :]
-                sel = self.bit(self.offbits[bh], off) & (off >= 0) & ~self.bit(self.colbits[bh], mg)[None, :]
+                sel = self._slash(bh, ng[:, None], mg[None, :]) & ~self.bit(self.colbits[bh], mg)[None, :]
                 cov[np.ix_(rows, kk)] += sel
             nb = 0
             while nb * 64 < vl.size and vl[nb * 64] <= 128 * t + 127:
@@ -130,8 +140,7 @@ class Arena:
             for ff in f[k0 + f <= Nq - 1]:
                 r0 = k0 + int(ff)
                 rows = np.arange(r0, min(r0 + 64, Nq))
-                off = self.qpos(rows)[:, None] - mg[None, :]
-                sel = self.bit(self.offbits[bh], off) & (off >= 0) & ~vset[keys][None, :]
+                sel = self._slash(bh, self.qpos(rows)[:, None], mg[None, :]) & ~vset[keys][None, :]
                 cov[np.ix_(rows, keys)] += sel
         for c in range(0, vl.size, 128):
             kk = vl[c:c + 128]
