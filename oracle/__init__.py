@@ -8,7 +8,8 @@ Plain, slow and fp64: the arithmetic lives in ``vs_oracle.c`` (loaded with
 ctypes) plus a few numpy helpers here that follow the pages' definitions
 directly:
 
-* ``estimate`` / ``topk`` / ``select`` / ``topp_budget`` / ``select_topp`` --
+* ``estimate`` / ``topk`` / ``select`` / ``select_group`` / ``topp_budget`` /
+  ``select_topp`` --
   Algorithm 1 of *MTraining:
   Distributed Dynamic Sparse Attention for Efficient Ultra-Long Context
   Training*: the last-``last_q`` observation window, ``sum_v`` / ``sum_s`` and
@@ -109,6 +110,29 @@ def select(v: np.ndarray, s: np.ndarray, kv: int, ks: int):
         for h in range(H):
             iv[b, h] = topk(v[b, h], kv)
             is_[b, h] = topk(s[b, h], ks)
+    return iv, is_
+
+
+def select_group(v: np.ndarray, s: np.ndarray, kv: int, ks: int, g: int, dtype=np.float64):
+    """Per-KV-group shared selection (a variant of Algorithm 1's per-head
+    selection: the g query heads that share a KV head use one index): the
+    group's scores are the sum of its heads' scores, added in head order in
+    `dtype` (the precision in which the sum decides the selection), and every
+    head of the group gets iv = argtopk(sum v, kv), is = argtopk(sum s, ks)."""
+    B, H, N = v.shape
+    G = H // g
+    iv = np.zeros((B, H, kv), np.int32)
+    is_ = np.zeros((B, H, ks), np.int32)
+    vv = np.asarray(v, dtype).reshape(B, G, g, N)
+    ss = np.asarray(s, dtype).reshape(B, G, g, N)
+    for b in range(B):
+        for hk in range(G):
+            sv, sl = vv[b, hk, 0].copy(), ss[b, hk, 0].copy()
+            for j in range(1, g):
+                sv = (sv + vv[b, hk, j]).astype(dtype)
+                sl = (sl + ss[b, hk, j]).astype(dtype)
+            iv[b, hk * g:(hk + 1) * g] = topk(sv, kv)
+            is_[b, hk * g:(hk + 1) * g] = topk(sl, ks)
     return iv, is_
 
 
