@@ -61,6 +61,8 @@ def lib(build_if_missing: bool = True):
     L.vs_estimate_workspace.restype = ctypes.c_size_t
     L.vs_estimate.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, _P, _P, _P,
                               _P, ctypes.c_size_t, _P]
+    L.vs_estimate_group.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, _P,
+                                    _P, _P, _P, ctypes.c_size_t, _P]
     L.vs_estimate_topp.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.vs_select_topp.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_double, ctypes.c_double,
@@ -138,9 +140,10 @@ def _ws(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ entry points
 def vs_estimate(q, k, kv: int, ks: int, scale: Optional[float] = None, last_q: int = 64, v_idx=None, s_idx=None,
-                v_score=None, s_score=None, ws=None, stream=None):
+                v_score=None, s_score=None, ws=None, stream=None, shared: bool = False):
     """Vertical and slash selection (Algorithm 1).  Returns (v_idx, s_idx) int32
-    [B, Hq, kv] / [B, Hq, ks], sorted ascending."""
+    [B, Hq, kv] / [B, Hq, ks], sorted ascending.  shared=True: one selection
+    per KV group (vs_estimate_group)."""
     sh = make_shape(q, k)
     B, N, Hq, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -148,9 +151,9 @@ def vs_estimate(q, k, kv: int, ks: int, scale: Optional[float] = None, last_q: i
     s_idx = torch.empty(B, Hq, ks, dtype=torch.int32, device=q.device) if s_idx is None else s_idx
     need = lib().vs_estimate_workspace(ctypes.byref(sh), last_q)
     ws = _ws(need, q.device) if ws is None else ws
-    _check(lib().vs_estimate(ctypes.byref(sh), _ptr(q), _ptr(k), last_q, kv, ks, scale, _ptr(v_idx), _ptr(s_idx),
-                             _ptr(v_score), _ptr(s_score), _ptr(ws), ws.numel() * ws.element_size(),
-                             _stream(stream)), "vs_estimate")
+    fn = lib().vs_estimate_group if shared else lib().vs_estimate
+    _check(fn(ctypes.byref(sh), _ptr(q), _ptr(k), last_q, kv, ks, scale, _ptr(v_idx), _ptr(s_idx), _ptr(v_score),
+              _ptr(s_score), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "vs_estimate")
     return v_idx, s_idx
 
 

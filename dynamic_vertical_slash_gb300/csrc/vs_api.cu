@@ -175,9 +175,25 @@ size_t vs_estimate_workspace(const vs_shape* s, int last_q) {
   return estimate_workspace_bytes(s, last_q);
 }
 
+static vs_status estimate_any(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks,
+                              float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                              size_t ws_bytes, int shared, cudaStream_t stream);
+
 vs_status vs_estimate(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks, float scale,
                       int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws, size_t ws_bytes,
                       cudaStream_t stream) {
+  return estimate_any(s, q, k, last_q, kv, ks, scale, v_idx, s_idx, v_score, s_score, ws, ws_bytes, 0, stream);
+}
+
+vs_status vs_estimate_group(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks, float scale,
+                            int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  return estimate_any(s, q, k, last_q, kv, ks, scale, v_idx, s_idx, v_score, s_score, ws, ws_bytes, 1, stream);
+}
+
+static vs_status estimate_any(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks,
+                              float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                              size_t ws_bytes, int shared, cudaStream_t stream) {
   vs_status rc = check_shape(s);
   if (rc != VS_OK) return rc;
   if (!q || !k || !v_idx || !s_idx || !ws) return VS_ERR_ARG;
@@ -187,7 +203,7 @@ vs_status vs_estimate(const vs_shape* s, const void* q, const void* k, int last_
   if (!(scale > 0.f)) return VS_ERR_ARG;
   if (!aligned16(q) || !aligned16(k)) return VS_ERR_SHAPE;
   if (ws_bytes < estimate_workspace_bytes(s, last_q)) return VS_ERR_WORKSPACE;
-  return launch_estimate(s, q, k, last_q, kv, ks, scale, v_idx, s_idx, v_score, s_score, ws, stream);
+  return launch_estimate(s, q, k, last_q, kv, ks, scale, v_idx, s_idx, v_score, s_score, ws, shared, stream);
 }
 
 vs_status vs_estimate_topp(const vs_shape* s, const void* q, const void* k, int last_q, double pv, double ps,

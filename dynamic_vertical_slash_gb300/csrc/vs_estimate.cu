@@ -34,7 +34,7 @@ constexpr int kTopkThreads = 1024;
 constexpr size_t kToppMaxSmem = size_t(192) << 10;  // pooled slash units: N <= 1,572,864
 
 struct EstLayout {
-  int64_t off_part, off_lse, off_vbuf, off_spart, off_sbuf, total;
+  int64_t off_part, off_lse, off_vbuf, off_spart, off_sbuf, off_gv, off_gs, total;
 };
 
 EstLayout est_layout(const vs_shape* s) {
@@ -51,6 +51,9 @@ EstLayout est_layout(const vs_shape* s) {
   L.off_vbuf = take(BH * N * 4);
   L.off_spart = take(BH * NT * kEstDiag * 4);
   L.off_sbuf = take(BH * N * 4);
+  const int64_t BHK = int64_t(s->B) * s->Hkv;
+  L.off_gv = take(BHK * N * 4);  // per-KV-group score sums (shared selection)
+  L.off_gs = take(BHK * N * 4);
   L.total = off;
   return L;
 }
@@ -63,6 +66,8 @@ struct EstParams {
   float* v;       // [BH][N]
   float* spart;   // [BH][NT][kEstDiag]
   float* s;       // [BH][N]
+  float* gv;      // shared selection: [BHK][N] group sums (null: per-head selection)
+  float* gs;
   int* err;
 };
 
@@ -480,18 +485,42 @@ __device__ void topk_block(const uint32_t* x, int N, int k, int32_t* out, int ca
 }
 
 struct TopkParams {
-  const float* score;  // [BH][N] for v, then s
+  const float* score;  // [L][N] score lists for v, then s
   const float* score2;
-  int32_t* out;        // [BH][k]
+  int32_t* out;        // [L * rep][k]: list l is written to rows l * rep .. l * rep + rep - 1
   int32_t* out2;
   int N, k, k2;
+  int rep;             // copies of each list (the heads of a group sharing it)
 };
 
 __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
-  const int bh = blockIdx.x, which = blockIdx.y;
-  const uint32_t* x = reinterpret_cast<const uint32_t*>(which == 0 ? p.score : p.score2) + int64_t(bh) * p.N;
+  const int l = blockIdx.x, which = blockIdx.y;
+  const uint32_t* x = reinterpret_cast<const uint32_t*>(which == 0 ? p.score : p.score2) + int64_t(l) * p.N;
   const int k = which == 0 ? p.k : p.k2;
-  topk_block(x, p.N, k, (which == 0 ? p.out : p.out2) + int64_t(bh) * k, k);
+  int32_t* out = (which == 0 ? p.out : p.out2) + int64_t(l) * p.rep * k;
+  topk_block(x, p.N, k, out, k);
+  if (p.rep > 1) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < (p.rep - 1) * k; i += blockDim.x) out[k + i] = out[i % k];
+  }
+}
+
+// Per-KV-group sums of the heads' scores, added in head order (fp32), for
+// the shared selection: gv[b, hk, m] = sum_j v[b, hk g + j, m].
+__global__ void __launch_bounds__(256) est_group_sum(const float* v, const float* s, float* gv, float* gs, int N,
+                                                     int g) {
+  const int l = blockIdx.y;  // b * Hkv + hk
+  const int64_t m = int64_t(blockIdx.x) * 256 + threadIdx.x;
+  if (m >= N) return;
+  const float* pv = v + int64_t(l) * g * N + m;
+  const float* ps = s + int64_t(l) * g * N + m;
+  float a = pv[0], c = ps[0];
+  for (int j = 1; j < g; ++j) {
+    a += pv[int64_t(j) * N];
+    c += ps[int64_t(j) * N];
+  }
+  gv[int64_t(l) * N + m] = a;
+  gs[int64_t(l) * N + m] = c;
 }
 
 // ---------------------------------------------------------------- top-p
@@ -711,8 +740,20 @@ vs_status launch_est_kernels(const vs_shape* s, const void* q, const void* k, Es
   tp.N = s->Nk;
   tp.k = kv;
   tp.k2 = ks;
+  tp.rep = 1;
+  int lists = BH;
+  if (p.gv) {
+    trace_begin("est_group_sum", st);
+    est_group_sum<<<dim3((s->Nk + 255) / 256, BHK), 256, 0, st>>>(p.v, p.s, p.gv, p.gs, s->Nk, p.g);
+    trace_end(st);
+    note_launch();
+    tp.score = p.gv;
+    tp.score2 = p.gs;
+    tp.rep = p.g;
+    lists = BHK;
+  }
   trace_begin("est_topk", st);
-  est_topk<<<dim3(BH, 2), kTopkThreads, 0, st>>>(tp);
+  est_topk<<<dim3(lists, 2), kTopkThreads, 0, st>>>(tp);
   trace_end(st);
   note_launch(5);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
@@ -729,6 +770,7 @@ EstParams est_params(const vs_shape* s, float scale, int* err) {
   p.MT = (p.g + 1) / 2;
   p.scale_log2 = scale * kLog2e;
   p.err = err;
+  p.gv = p.gs = nullptr;
   return p;
 }
 
@@ -790,11 +832,15 @@ vs_status launch_select_topp(int B, int H, int N, const float* v_score, const fl
 }
 
 vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int, int kv, int ks, float scale,
-                          int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                          int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws, int shared,
                           cudaStream_t st) {
   const EstLayout L = est_layout(s);
   uint8_t* W = static_cast<uint8_t*>(ws);
   EstParams p = est_params(s, scale, static_cast<int*>(ws));
+  if (shared) {
+    p.gv = reinterpret_cast<float*>(W + L.off_gv);
+    p.gs = reinterpret_cast<float*>(W + L.off_gs);
+  }
   p.part = reinterpret_cast<float2*>(W + L.off_part);
   p.lse = reinterpret_cast<float*>(W + L.off_lse);
   p.v = v_score ? v_score : reinterpret_cast<float*>(W + L.off_vbuf);

@@ -30,7 +30,7 @@ vs_status launch_bwd(const vs_shape* s, const Geo& G, const void* q, const void*
                      float* dq_acc, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t bwd_workspace_bytes(const vs_shape* s, int kv);
 vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks, float scale,
-                          int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                          int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws, int shared,
                           cudaStream_t st);
 size_t estimate_workspace_bytes(const vs_shape* s, int last_q);
 vs_status launch_estimate_topp(const vs_shape* s, const void* q, const void* k, double pv, double ps, int kv_max,

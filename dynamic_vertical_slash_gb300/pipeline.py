@@ -56,17 +56,20 @@ class VSAttention:
     budgets (Algorithm 1) of at most kv / ks entries (``budgets`` then holds
     the [B, Hq] budgets of the last forward).  ``block_cover`` selects the
     block-cover reading of the slashes (whole 64 x 64 blocks, see
-    vs_build_block_index_ex).  All tensors are BSHD bf16 on the device.
+    vs_build_block_index_ex); ``shared`` one selection per KV group
+    (vs_estimate_group).  All tensors are BSHD bf16 on the device.
     """
 
     def __init__(self, B: int, N: int, Hq: int, Hkv: int, d: int, kv: int, ks: int,
                  device="cuda", last_q: int = 64, scale: Optional[float] = None,
-                 pv: Optional[float] = None, ps: Optional[float] = None, block_cover: bool = False):
+                 pv: Optional[float] = None, ps: Optional[float] = None, block_cover: bool = False,
+                 shared: bool = False):
         self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N, Hq, Hkv, d, kv, ks
         if (pv is None) != (ps is None):
             raise ValueError("top-p mode needs both pv and ps")
         self.pv, self.ps = pv, ps
         self.block_cover = block_cover
+        self.shared = shared
         self.last_q = last_q
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         dev = torch.device(device)
@@ -105,7 +108,7 @@ class VSAttention:
                                 stream)
         elif selection is None:
             B_.vs_estimate(q, k, self.kv, self.ks, self.scale, self.last_q, self.v_idx, self.s_idx, self.v_score,
-                           self.s_score, self.ws_est, stream)
+                           self.s_score, self.ws_est, stream, self.shared)
         else:
             self.v_idx.copy_(selection[0])
             self.s_idx.copy_(selection[1])

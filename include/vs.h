@@ -99,6 +99,17 @@ vs_status vs_estimate(const vs_shape* shape, const void* q, const void* k, int l
                       int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws, size_t ws_bytes,
                       cudaStream_t stream);
 
+/* vs_estimate_group -- vs_estimate with one selection per KV group (a
+ * variant of the per-head selection: the Hq / Hkv query heads that share a
+ * KV head share one index).  The group's scores are the sums of its heads'
+ * scores (fp32, added in head order); every head of the group gets
+ * argtopk of those sums, so v_idx / s_idx rows of one group are equal.
+ * Arguments, workspace and outputs as for vs_estimate (v_score / s_score
+ * still receive the per-head scores). */
+vs_status vs_estimate_group(const vs_shape* shape, const void* q, const void* k, int last_q, int kv, int ks,
+                            float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * vs_estimate_topp / vs_select_topp -- top-p budgets (Algorithm 1, the
  * `topp` and `Pool` lines; section 4.1 (i) online budget approximation and
