@@ -215,9 +215,8 @@ vs_status vs_build_block_index(const vs_shape* shape, const int32_t* v_idx, cons
                                const vs_stripe* stripe, void* arena, size_t arena_bytes, cudaStream_t stream);
 
 /* vs_build_block_index with flags.  VS_INDEX_BLOCK_COVER selects the
- * block-cover reading of the slashes (section 4.1 (ii): slash lines
- * aggregated over 64 x 64 token blocks to match the kernel tiling): the mask
- * becomes
+ * block-cover reading of the slashes (section 4.1 (ii): the slashes taken at
+ * the granularity of the kernel's 64 x 64 tiles): the mask becomes
  *     M[n, m] = (m <= n) and (m in v_idx or block diagonal
  *               floor(n/64) - floor(m/64) is active),
  * on global positions, where block diagonal D is active iff some selected

@@ -215,7 +215,7 @@ class Problem:
     iv [B, Hq, kv] and is_ [B, Hq, ks] index the global sequence of length
     ``n_global``; qpos / kpos give each local row's / key's global position
     (identity when None).  block=True selects the block-cover reading of the
-    slashes (section 4.1 (ii): slashes aggregated over 64 x 64 blocks): every
+    slashes (section 4.1 (ii): the slash budget works on 64 x 64 blocks): every
     causal entry of a 64 x 64 block (on global positions) that a selected
     slash passes through is in the mask, besides the selected columns.
     """

@@ -1,5 +1,5 @@
 """Block-cover reading of the slashes on the GPU (MTraining section 4.1 (ii):
-slash lines aggregated over 64 x 64 token blocks) against the oracle's
+slashes taken at the granularity of 64 x 64 blocks) against the oracle's
 block mask, through the C ABI: exact index coverage, forward and backward
 parity unstriped and on striped ring steps, and the exact-mask path left as
 it was."""

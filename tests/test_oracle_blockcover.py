@@ -1,7 +1,7 @@
 """Pins for the oracle's block-cover mask (MTraining section 4.1 (ii):
-slash lines aggregated over 64 x 64 token blocks to match the kernel
-tiling): closed forms for single slashes, containment of the exact mask,
-whole blocks, and the full causal mask."""
+slashes taken at the granularity of the kernel's 64 x 64 tiles): closed
+forms for single slashes, containment of the exact mask, whole blocks, and
+the full causal mask."""
 import numpy as np
 import pytest
 
