@@ -194,6 +194,29 @@ def reference_arm(args, w, x):
     return line
 
 
+def _variant_kwargs(args, w):
+    """VSAttention options of the selected variant of the path: the exact
+    token mask with fixed budgets (the headline), the block-cover reading,
+    top-p budgets (capped at --kv-cap / --ks-cap), or one selection per KV
+    group."""
+    if args.variant == "block":
+        return {"block_cover": True}
+    if args.variant == "shared":
+        return {"shared": True}
+    if args.variant == "topp":
+        return {"pv": args.pv, "ps": args.ps, "kv_cap": args.kv_cap, "ks_cap": args.ks_cap}
+    return {}
+
+
+def _variant_note(args, attn):
+    if args.variant == "topp":
+        kv, ks = (b.float().cpu().numpy() for b in attn.budgets)
+        return {"name": "topp", "pv": args.pv, "ps": args.ps, "kv_cap": args.kv_cap, "ks_cap": args.ks_cap,
+                "kv_mean": float(kv.mean()), "kv_min": int(kv.min()), "kv_max": int(kv.max()),
+                "ks_mean": float(ks.mean()), "ks_min": int(ks.min()), "ks_max": int(ks.max())}
+    return {"name": args.variant}
+
+
 def _config(w):
     return {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "kv": w.kv, "ks": w.ks,
             "last_q": w.last_q, "parallelism": "replicas",
@@ -210,7 +233,10 @@ def ours(args, w, x, rank, world):
     dev = torch.device("cuda", torch.cuda.current_device())
     to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
     q, k, v, do = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["dout"])
-    attn = vs.VSAttention(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, device=dev, last_q=w.last_q, scale=w.scale)
+    vkw = _variant_kwargs(args, w)
+    attn = vs.VSAttention(w.B, w.N, w.Hq, w.Hkv, w.d, vkw.pop("kv_cap", w.kv), vkw.pop("ks_cap", w.ks), device=dev,
+                          last_q=w.last_q, scale=w.scale, **vkw)
+    args._attn_kwargs = (attn.kv, attn.ks, vkw)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
@@ -317,9 +343,12 @@ def ours(args, w, x, rank, world):
         e2e = _e2e(args, w, attn, q, k, v, do, dev, world, executed)
 
     dense_f = dense_causal_flops(w.B, w.N, w.Hq, w.d)
+    cfg = _config(w)
+    if args.variant != "exact":
+        cfg["variant"] = _variant_note(args, attn)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
             "pct_bf16_peak": 100.0 * value / world / peaks["bf16_burst"],
             "flops": {"executed_per_step": executed, "issued_per_step": fl["fwd_issued"] + fl["bwd_issued"],
@@ -386,7 +415,9 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     attn.check()
 
     # ---- pipelined
-    att = [attn, vs.VSAttention(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, device=dev, last_q=w.last_q, scale=w.scale)]
+    kv_cap, ks_cap, vkw = args._attn_kwargs
+    att = [attn, vs.VSAttention(w.B, w.N, w.Hq, w.Hkv, w.d, kv_cap, ks_cap, device=dev, last_q=w.last_q, scale=w.scale,
+                                **vkw)]
     din = [din0, [torch.empty_like(t) for t in (q, k, v, do)]]
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
@@ -620,6 +651,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--inner", type=int, default=0,
                     help="striped workloads: cards per node for the hierarchical ring order (0 = flat ring)")
+    ap.add_argument("--variant", choices=["exact", "block", "topp", "shared"], default="exact",
+                    help="path variant: exact token mask with fixed budgets (headline), block-cover slashes, "
+                         "top-p budgets, or one selection per KV group")
+    ap.add_argument("--pv", type=float, default=0.9, help="top-p variant: vertical mass fraction")
+    ap.add_argument("--ps", type=float, default=0.9, help="top-p variant: slash mass fraction")
+    ap.add_argument("--kv-cap", type=int, default=4096, help="top-p variant: vertical list capacity")
+    ap.add_argument("--ks-cap", type=int, default=8192, help="top-p variant: slash list capacity")
     ap.add_argument("--all-workers", action="store_true",
                     help="striped workloads: also run every worker's ring and report the imbalance across workers")
     args = ap.parse_args()
