@@ -186,6 +186,41 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Warp-collective forms of the three calls above: every lane of the warp
+// makes the call with the same (warp-uniform) operands and one elected lane
+// issues.  An issuing loop that the whole warp runs in step keeps descriptors
+// and TMEM addresses in the uniform datapath; issued from a one-lane branch
+// each MMA costs a round trip through the per-thread registers (measured on
+// GB300: about 114 cycles per M128 N128 K16 MMA from a lane-0 branch against
+// 70 with the warp convergent, which is the tensor pipe's own rate).
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// mbar_wait for a whole warp: every lane waits and all get the same answer,
+// so the warp stays convergent for the warp-collective calls above.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, Abort ab, int code_timeout) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, code_timeout));
+}
+
 // Instruction descriptor: bf16 x bf16 -> fp32, dense.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

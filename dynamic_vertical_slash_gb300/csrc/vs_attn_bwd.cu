@@ -323,28 +323,29 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
     // ------------------------------------------------------- S / dP issuer
     // Per pair i: S_i, dP_i once the compute warps hold S / dP of pair i - 1
     // in registers.
-    if (lane == 0 && P > 0) {
+    // The whole warp runs the loop; one elected lane issues.
+    if (P > 0) {
       const uint32_t idS = idesc_bf16(128, kDqPairKeys, 0, 0);
-      bool ok = mbar_wait(&s.qdo_full, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait_warp(&s.qdo_full, 0, ab, VS_ERR_TIMEOUT);
       for (int i = 0; ok && i < P; ++i) {
         const int ks = i % kDqKSlots, vsl = i % kDqVSlots;
-        if (!(ok = mbar_wait(&s.k_full[ks], (i / kDqKSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
-        if (!(ok = mbar_wait(&s.v_full[vsl], (i / kDqVSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
-        if (i >= 1 && !(ok = mbar_wait(&s.s_free, (i - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.k_full[ks], (i / kDqKSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.v_full[vsl], (i / kDqVSlots) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (i >= 1 && !(ok = mbar_wait_warp(&s.s_free, (i - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         if (gathered(i)) fence_proxy_async_smem();
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][kk / 4]) + (kk % 4) * 32, 16, 1024);
-          mma_ts(tmem + kDqColS, tmem + kDqColQ + kk * 8, dk_, idS, kk > 0);
+          mma_ts_warp(tmem + kDqColS, tmem + kDqColQ + kk * 8, dk_, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[vsl][kk / 4]) + (kk % 4) * 32, 16, 1024);
-          mma_ts(tmem + kDqColDP, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
+          mma_ts_warp(tmem + kDqColDP, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
         }
-        mma_commit(&s.s_full);
-        mma_commit(&s.v_empty[vsl]);
+        mma_commit_warp(&s.s_full);
+        mma_commit_warp(&s.v_empty[vsl]);
         mma_issued = true;
       }
     }
@@ -352,25 +353,27 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
     // ------------------------------------------------------------ dQ issuer
     // Per pair i, once its dS is in shared memory: dQ += dS K over the pair's
     // keys (K stays in its slot until then).
-    if (lane == 0 && P > 0) {
+    if (P > 0) {
       const uint32_t idQ = idesc_bf16(128, D, 0, 1);
       bool ok = true;
       for (int i = 0; ok && i < P; ++i) {
-        if (!(ok = mbar_wait(&s.ds_full, i & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.ds_full, i & 1, ab, VS_ERR_TIMEOUT))) break;
         if (gathered(i)) fence_proxy_async_smem();
         tc_fence_after();
         const int ks = i % kDqKSlots;
         const int nk = (2 * i + 1 < U) ? kDqPairKeys / 16 : kKTile / 16;
-        for (int kk = 0; kk < nk; ++kk) {
+#pragma unroll
+        for (int kk = 0; kk < kDqPairKeys / 16; ++kk) {
+          if (kk >= nk) break;
           const uint64_t da = sdesc_sw128(smem_u32(s.ds[kk / 4]) + (kk % 4) * 32, 16, 1024);
           const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][0]) + kk * 2048, kDqPairKeys * 128, 1024);
-          mma_ss(tmem + kDqColAcc, da, dk_, idQ, (i > 0 || kk > 0));
+          mma_ss_warp(tmem + kDqColAcc, da, dk_, idQ, (i > 0 || kk > 0));
         }
-        mma_commit(&s.ds_done);
-        mma_commit(&s.k_empty[ks]);
+        mma_commit_warp(&s.ds_done);
+        mma_commit_warp(&s.k_empty[ks]);
         mma_issued = true;
       }
-      mma_commit(&s.fin);
+      mma_commit_warp(&s.fin);
     }
   } else {
     // ------------------------------------------------------------ compute
@@ -800,25 +803,27 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
   } else if (warp == 1) {
     // ---------------------------------------------------- S^T / dP^T issuer
     // Unit j once the compute warps hold S^T / dP^T of unit j - 1.
-    if (lane == 0 && run) {
+    // The whole warp runs the loop; one elected lane issues.
+    if (run) {
       const uint32_t idS = idesc_bf16(128, kRowTile, 0, 0);
-      bool ok = mbar_wait(&s.kv_full, 0, ab, VS_ERR_TIMEOUT) && mbar_wait(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait_warp(&s.kv_full, 0, ab, VS_ERR_TIMEOUT);
+      ok = ok && mbar_wait_warp(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT);
       if (ok && BAR) fence_proxy_async_smem();
       for (int j = 0; ok && j < U; ++j) {
         const int st = j % kBwdStages;
-        if (!(ok = mbar_wait(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
-        if (j >= 1 && !(ok = mbar_wait(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (j >= 1 && !(ok = mbar_wait_warp(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
           const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
           const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-          mma_ts(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
-          mma_ss(tmem + kKvColDP, dva, dg_, idS, kk > 0);
+          mma_ts_warp(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
+          mma_ss_warp(tmem + kKvColDP, dva, dg_, idS, kk > 0);
         }
         mma_issued = true;
-        mma_commit(&s.s_full);
+        mma_commit_warp(&s.s_full);
       }
     }
   } else if (warp == 10) {
@@ -826,25 +831,25 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     // Unit j once its P^T / dS^T are in TMEM; the unit's stage is released
     // after these MMAs (the S^T / dP^T MMAs that read it completed before the
     // compute warps saw the scores).
-    if (lane == 0 && run) {
+    if (run) {
       const uint32_t idG = idesc_bf16(128, D, 0, 1);
       bool ok = true;
       for (int j = 0; ok && j < U; ++j) {
         const int st = j % kBwdStages;
-        if (!(ok = mbar_wait(&s.p_full, j & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.p_full, j & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kRowTile / 16; ++kk) {
           const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][0]) + kk * 2048, kRowTile * 128, 1024);
           const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][0]) + kk * 2048, kRowTile * 128, 1024);
-          mma_ts(tmem + kKvColDV, tmem + kKvColP + kk * 8, dg_, idG, (j > 0 || kk > 0));
-          mma_ts(tmem + kKvColDK, tmem + kKvColDS + kk * 8, dq_, idG, (j > 0 || kk > 0));
+          mma_ts_warp(tmem + kKvColDV, tmem + kKvColP + kk * 8, dg_, idG, (j > 0 || kk > 0));
+          mma_ts_warp(tmem + kKvColDK, tmem + kKvColDS + kk * 8, dq_, idG, (j > 0 || kk > 0));
         }
         mma_issued = true;
-        mma_commit(&s.mm_done);
-        mma_commit(&s.st_empty[st]);
+        mma_commit_warp(&s.mm_done);
+        mma_commit_warp(&s.st_empty[st]);
       }
-      mma_commit(&s.fin);
+      mma_commit_warp(&s.fin);
     }
   } else {
     // ------------------------------------------------------------ compute

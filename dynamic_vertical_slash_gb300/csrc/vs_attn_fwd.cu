@@ -10,10 +10,10 @@
 // pair: fp32 online softmax on the exact token mask in registers (one thread
 // per row), P (bf16) back into TMEM.
 //
-// Warp roles (352 threads): warp 0 issues the loads, warp 10 publishes, per
-// unit, the few words every row's mask is cut from, warp 1 issues MMAs (one
-// lane), warps 2-5 and 6-9 are two softmax warpgroups that take alternate pairs
-// (even / odd).  Each group keeps its own running maximum, sum and O
+// Warp roles (384 threads): warp 0 loads Q and the K blocks, warp 11 the V
+// blocks, warp 10 publishes, per unit, the few words every row's mask is cut
+// from, warp 1 issues MMAs (one lane), warps 2-5 and 6-9 are two softmax
+// warpgroups that take alternate pairs (even / odd).  Each group keeps its own running maximum, sum and O
 // accumulator, so the groups never wait for each other; the epilogue merges
 // the two partial results the way merge_out_and_lse of Algorithm 2 merges
 // ring steps.
@@ -34,8 +34,9 @@
 namespace vs {
 namespace {
 
-constexpr int kFwdThreads = 352;
+constexpr int kFwdThreads = 384;
 constexpr int kFwdRecWarp = 10;
+constexpr int kFwdVWarp = 11;
 constexpr int kFwdGroup = 128;  // threads per softmax warpgroup
 constexpr int kPairKeys = 2 * kKTile;
 constexpr int kFwdSlots = 5;
@@ -88,7 +89,6 @@ struct FwdSmem {
   uint8_t q[NH][kQTile * 128];
   uint8_t slot[kFwdSlots][NH][kPairKeys * 128];  // K or V of one pair, 128B-swizzled, per d-half
   MaskRec rec[kRecRing][2];                      // mask records of a pair's two units
-  int key0[kRecRing][2];                         // loader: first key of each slash half, by pair
   uint64_t q_full;
   uint64_t slot_full[kFwdSlots], slot_empty[kFwdSlots];
   uint64_t rec_full[kRecRing], rec_empty[kRecRing];
@@ -349,48 +349,55 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
   const Abort ab{&s.abort_flag, p.err};
   bool mma_issued = false;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kFwdVWarp) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 loads Q and the K blocks, warp kFwdVWarp the V blocks.  Each walks
+    // the whole block sequence (so both agree on every block's slot and
+    // phase) and acts on its own kind only: one thread's TMA issue blocks
+    // while the copy engine works through its boxes, so with two issuers the
+    // engine never idles while the other does its bookkeeping.
+    const int my_kind = warp == 0 ? 0 : 1;
     int issued[kFwdSlots];
     for (int i = 0; i < kFwdSlots; ++i) issued[i] = -1;
     if (P > 0) {
       if (lane == 0) {
-        prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
-        mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
-        for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
+        if (my_kind == 0) {
+          prefetch_tmap(&tmQ);
+          prefetch_tmap(&tmK);
+          mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
+          for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
+        } else {
+          prefetch_tmap(&tmV);
+        }
       }
-      const uint8_t* kb = p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
-      const uint8_t* vb = p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2;
+      const uint8_t* base = my_kind ? p.v + (int64_t(b) * p.sv[0] + int64_t(hk) * p.sv[2]) * 2
+                                    : p.k + (int64_t(b) * p.sk[0] + int64_t(hk) * p.sk[2]) * 2;
+      const int64_t stok = my_kind ? p.sv[1] : p.sk[1];
+      const CUtensorMap* tm = my_kind ? &tmV : &tmK;
       int c = 0;
       bool ok = true;
       int e_win = -1, e_pref = 0;  // elist[32 e_win + lane]
       for_each_block(P, [&](int kind, int i) {
         if (!ok) return;
-        const int sl = c % kFwdSlots;
-        if (!kind) {
-          // K blocks come in pair order: read the slash entries of both halves
-          // (one 32-entry window per lane) and keep their first keys for V
+        const int cb = c++;
+        if (kind != my_kind) return;
+        const int sl = cb % kFwdSlots;
+        // first keys of the pair's slash halves (one 32-entry window of the
+        // list per lane)
+        int key0[2] = {0, 0};
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int u = 2 * i + hh;
-            if (u >= nslash) continue;
-            if ((u >> 5) != e_win) {
-              e_win = u >> 5;
-              const int j = 32 * e_win + lane;
-              e_pref = j < nslash ? __ldg(elist + j) : 0;
-            }
-            const int e = __shfl_sync(0xffffffffu, e_pref, u & 31);
-            if (lane == 0) s.key0[i % kRecRing][hh] = t * kQTile + 64 - e;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int u = 2 * i + hh;
+          if (u >= nslash) continue;
+          if ((u >> 5) != e_win) {
+            e_win = u >> 5;
+            const int j = 32 * e_win + lane;
+            e_pref = j < nslash ? __ldg(elist + j) : 0;
           }
-          __syncwarp();
+          key0[hh] = t * kQTile + 64 - __shfl_sync(0xffffffffu, e_pref, u & 31);
         }
-        if (c >= kFwdSlots && !(ok = mbar_wait(&s.slot_empty[sl], ((c / kFwdSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)))
+        if (cb >= kFwdSlots && !(ok = mbar_wait(&s.slot_empty[sl], ((cb / kFwdSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)))
           return;
-        const CUtensorMap* tm = kind ? &tmV : &tmK;
-        const uint8_t* base = kind ? vb : kb;
-        const int64_t stok = kind ? p.sv[1] : p.sk[1];
         uint32_t tma_bytes = 0;
         bool gath = false;
         for (int hh = 0; hh < 2; ++hh) {
@@ -413,16 +420,14 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
             for (int hh = 0; hh < 2; ++hh) {
               const int u = 2 * i + hh;
               if (u >= nslash) continue;
-              const int key0 = s.key0[i % kRecRing][hh];
               for (int hf = 0; hf < NH; ++hf)
-                tma_load_4d(s.slot[sl][hf] + hh * kKTile * 128, tm, &s.slot_full[sl], 64 * hf, hk, key0, b);
+                tma_load_4d(s.slot[sl][hf] + hh * kKTile * 128, tm, &s.slot_full[sl], 64 * hf, hk, key0[hh], b);
             }
           } else {
             mbar_arrive(&s.slot_full[sl]);
           }
         }
-        issued[sl] = c;
-        ++c;
+        issued[sl] = cb;
         __syncwarp();
       });
     }
@@ -544,19 +549,20 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     // ------------------------------------------------------------ MMA issuer
     // Pair i belongs to softmax group g = i & 1.  Order: S0, S1, then per
     // pair i: PV_i (once group g has written P_i), S_{i+2} into the same S_g.
-    if (lane == 0 && P > 0) {
+    // The whole warp runs the loop; one elected lane issues.
+    if (P > 0) {
       const uint32_t idS = idesc_bf16(128, kPairKeys, 0, 0);
       const uint32_t idO = idesc_bf16(128, D, 0, 1);
-      bool ok = mbar_wait(&s.q_full, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait_warp(&s.q_full, 0, ab, VS_ERR_TIMEOUT);
       int c = 0;
       for_each_block(P, [&](int kind, int i) {
         if (!ok) return;
         const int g = i & 1;
         if (kind) {
-          if (!(ok = mbar_wait(&s.p_full[g], (i >> 1) & 1, ab, VS_ERR_TIMEOUT))) return;
+          if (!(ok = mbar_wait_warp(&s.p_full[g], (i >> 1) & 1, ab, VS_ERR_TIMEOUT))) return;
         }
         const int sl = c % kFwdSlots;
-        if (!(ok = mbar_wait(&s.slot_full[sl], (c / kFwdSlots) & 1, ab, VS_ERR_TIMEOUT))) return;
+        if (!(ok = mbar_wait_warp(&s.slot_full[sl], (c / kFwdSlots) & 1, ab, VS_ERR_TIMEOUT))) return;
         if (gathered(i)) fence_proxy_async_smem();
         tc_fence_after();
         if (!kind) {
@@ -564,22 +570,24 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t da = sdesc_sw128(smem_u32(s.q[kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t db = sdesc_sw128(smem_u32(s.slot[sl][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ss(tmem + kColS + 128 * g, da, db, idS, kk > 0);
+            mma_ss_warp(tmem + kColS + 128 * g, da, db, idS, kk > 0);
           }
-          mma_commit(&s.s_full[g]);
+          mma_commit_warp(&s.s_full[g]);
         } else {
           const int nk = (2 * i + 1 < U) ? kPairKeys / 16 : kKTile / 16;
-          for (int kk = 0; kk < nk; ++kk) {
+#pragma unroll
+          for (int kk = 0; kk < kPairKeys / 16; ++kk) {
+            if (kk >= nk) break;
             const uint64_t dv = sdesc_sw128(smem_u32(s.slot[sl][0]) + kk * 2048, kPairKeys * 128, 1024);
             const uint32_t a_p = tmem + kColS + 128 * g + (kk >> 2) * 64 + (kk & 3) * 8;  // P of unit kk / 4
-            mma_ts(tmem + kColO + 128 * g, a_p, dv, idO, (i >= 2 || kk > 0));
+            mma_ts_warp(tmem + kColO + 128 * g, a_p, dv, idO, (i >= 2 || kk > 0));
           }
         }
-        mma_commit(&s.slot_empty[sl]);
+        mma_commit_warp(&s.slot_empty[sl]);
         mma_issued = true;
         ++c;
       });
-      mma_commit(&s.o_final);
+      mma_commit_warp(&s.o_final);
     }
   } else if (warp >= 2 && warp < 2 + 8) {
     // ------------------------------------------------------------ softmax
@@ -595,18 +603,24 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     const int64_t n_g = qpos_g(G, n_loc);
     for (int i = grp; i < P; i += 2) {
       const int ri = i % kRecRing;
-      ok = mbar_wait(&s.s_full[grp], (i >> 1) & 1, ab, VS_ERR_TIMEOUT) &&
-           mbar_wait(&s.rec_full[ri], (i / kRecRing) & 1, ab, VS_ERR_TIMEOUT);
+      // the pair's row masks first: the record is published ahead of the
+      // scores, so cutting the masks overlaps the S MMAs
+      ok = mbar_wait(&s.rec_full[ri], (i / kRecRing) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      tc_fence_after();
       const MaskRec& rc0 = s.rec[ri][0];
       const MaskRec& rc1 = s.rec[ri][1];
       const uint64_t mask0 = row_ok ? rec_row_mask<BLOCK>(rc0, rc0.kind, r, n_g) : 0ull;
       const uint64_t mask1 = row_ok ? rec_row_mask<BLOCK>(rc1, rc1.kind, r, n_g) : 0ull;
       mbar_arrive(&s.rec_empty[ri]);
+      ok = mbar_wait(&s.s_full[grp], (i >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       // P against the row's reference maximum m_run (log2 units), one unit at
       // a time.  The reference is lazy: it only moves when a unit's masked sum
       // shows an entry more than 2^64 above it (or for the row's first
