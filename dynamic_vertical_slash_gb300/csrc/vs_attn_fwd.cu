@@ -12,8 +12,9 @@
 //
 // Warp roles (384 threads): warp 0 loads Q and the K blocks, warp 11 the V
 // blocks, warp 10 publishes, per unit, the few words every row's mask is cut
-// from, warp 1 issues MMAs (one lane), warps 2-5 and 6-9 are two softmax
-// warpgroups that take alternate pairs (even / odd).  Each group keeps its own running maximum, sum and O
+// from, warp 1 issues the MMAs (the whole warp runs the loop, an elected lane
+// issues), warps 2-5 and 6-9 are two softmax warpgroups that take alternate
+// pairs (even / odd).  Each group keeps its own running maximum, sum and O
 // accumulator, so the groups never wait for each other; the epilogue merges
 // the two partial results the way merge_out_and_lse of Algorithm 2 merges
 // ring steps.

@@ -16,7 +16,7 @@
 //   pass 4  est_topk     : radix select of the k-th largest score, then an
 //                          index-ordered compaction; ties go to the lower index
 // Warp roles in passes 1 and 2: warp 0 issues TMA loads, warp 1 the MMAs
-// (one lane), warps 2-9 read the scores (one thread per TMEM lane, two warps
+// (the whole warp runs the loop, an elected lane issues), warps 2-9 read the scores (one thread per TMEM lane, two warps
 // per lane quarter, each on half the columns).  Waits are bounded.
 #include "vs_internal.h"
 #include "vs_kernel_common.cuh"
@@ -105,6 +105,7 @@ __device__ __forceinline__ void est_load_q(EstSmem<D>& s, int buf, const CUtenso
 }
 
 // S = Q K^T of one row tile and one key tile into TMEM columns [col, col + 128).
+// Warp-collective: an elected lane issues.
 template <int D>
 __device__ __forceinline__ void est_mma(EstSmem<D>& s, int qb, int kb, uint32_t dst) {
   const uint32_t idS = idesc_bf16(128, kEstKeys, 0, 0);
@@ -112,7 +113,7 @@ __device__ __forceinline__ void est_mma(EstSmem<D>& s, int qb, int kb, uint32_t 
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t da = sdesc_sw128(smem_u32(s.q[qb][kk / 4]) + (kk % 4) * 32, 16, 1024);
     const uint64_t db = sdesc_sw128(smem_u32(s.k[kb][kk / 4]) + (kk % 4) * 32, 16, 1024);
-    mma_ss(dst, da, db, idS, kk > 0);
+    mma_ss_warp(dst, da, db, idS, kk > 0);
   }
 }
 
@@ -190,16 +191,16 @@ __global__ void __launch_bounds__(kEstThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && nchunk > 0) {
-      bool ok = mbar_wait(&s.q_full[0], 0, ab, VS_ERR_TIMEOUT);
+    if (nchunk > 0) {
+      bool ok = mbar_wait_warp(&s.q_full[0], 0, ab, VS_ERR_TIMEOUT);
       for (int c = 0; ok && c < nchunk; ++c) {
         const int kb = c & 1;
-        if (!(ok = mbar_wait(&s.k_full[kb], (c >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
-        if (c >= 2 && !(ok = mbar_wait(&s.s_free[kb], ((c >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.k_full[kb], (c >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (c >= 2 && !(ok = mbar_wait_warp(&s.s_free[kb], ((c >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
         est_mma<D>(s, 0, kb, tmem + 128 * kb);
-        mma_commit(&s.s_full[kb]);
-        mma_commit(&s.k_empty[kb]);
+        mma_commit_warp(&s.s_full[kb]);
+        mma_commit_warp(&s.k_empty[kb]);
         mma_issued = true;
       }
     }
@@ -303,16 +304,16 @@ __global__ void __launch_bounds__(kEstThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait(&s.k_full[0], 0, ab, VS_ERR_TIMEOUT);
+    {
+      bool ok = mbar_wait_warp(&s.k_full[0], 0, ab, VS_ERR_TIMEOUT);
       for (int mt = 0; ok && mt < MT; ++mt) {
         const int qb = mt & 1;
-        if (!(ok = mbar_wait(&s.q_full[qb], (mt >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
-        if (mt >= 2 && !(ok = mbar_wait(&s.s_free[qb], ((mt >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (!(ok = mbar_wait_warp(&s.q_full[qb], (mt >> 1) & 1, ab, VS_ERR_TIMEOUT))) break;
+        if (mt >= 2 && !(ok = mbar_wait_warp(&s.s_free[qb], ((mt >> 1) - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
         est_mma<D>(s, qb, 0, tmem + 128 * qb);
-        mma_commit(&s.s_full[qb]);
-        mma_commit(&s.q_empty[qb]);
+        mma_commit_warp(&s.s_full[qb]);
+        mma_commit_warp(&s.q_empty[qb]);
         mma_issued = true;
       }
     }
