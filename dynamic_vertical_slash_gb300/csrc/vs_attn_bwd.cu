@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
       }
     }
     dd[i] = acc;
-    l2[i] = p.lse[i] * kLog2e;
+    l2[i] = -p.lse[i] * kLog2e;  // stored negated: the kernels add it to the scaled scores
   }
 }
 
@@ -482,18 +482,20 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
         if (pos[kKTile - 1] <= n_g) cnt = kKTile;
         mask = cnt == kKTile ? ~0ull : ((1ull << cnt) - 1);
       }
+      // two keys at a time in paired fp32: P = 2^(S scale log2(e) - LSE log2(e))
+      // (Lr = -LSE log2(e)), dS = P (dP - D) on the mask
       uint32_t pk[32];
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), lr2 = f2_pack(Lr, Lr), dr2 = f2_pack(Dr, Dr);
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        float ds[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = 2 * k + e;
-          const float pv = ex2(fmaf(__uint_as_float(sr[col]), p.scale_log2, -Lr));
-          const float x = pv * (__uint_as_float(pr[col]) - Dr);
-          ds[e] = ((mask >> col) & 1ull) ? x : 0.f;  // after the product: masked scores may be garbage
-        }
-        pk[k] = pack_bf16x2(ds[0], ds[1]);
+        const int col = 2 * k;
+        float t0, t1, x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sc2, lr2), t0, t1);
+        f2_unpack(f2_mul(f2_pack(ex2(t0), ex2(t1)),
+                         f2_sub(f2_pack(__uint_as_float(pr[col]), __uint_as_float(pr[col + 1])), dr2)),
+                  x0, x1);
+        // after the product: masked scores may be garbage
+        pk[k] = pack_bf16x2(((mask >> col) & 1ull) ? x0 : 0.f, ((mask >> (col + 1)) & 1ull) ? x1 : 0.f);
       }
       if (i >= 1) ok = mbar_wait(&s.ds_done, (i - 1) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -934,20 +936,25 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
         ddv[4 * i + 2] = c.z;
         ddv[4 * i + 3] = c.w;
       }
+      // two rows at a time in paired fp32: t = S^T scale log2(e) - LSE log2(e)
+      // (the workspace holds -LSE log2(e)), P = 2^t on the mask, dS = P (dP - D)
       uint32_t pk[16], dk[16];
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        float pv[2], ds[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * i + e;
-          float x = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, -l2v[c]));
-          x = ((hm >> c) & 1u) ? x : 0.f;  // one select: dS inherits the zero
-          pv[e] = x;
-          ds[e] = x * (__uint_as_float(pr[c]) - ddv[c]);
-        }
-        pk[i] = pack_bf16x2(pv[0], pv[1]);
-        dk[i] = pack_bf16x2(ds[0], ds[1]);
+        const int c = 2 * i;
+        float t0, t1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2,
+                         f2_pack(l2v[c], l2v[c + 1])),
+                  t0, t1);
+        const float x0 = ((hm >> c) & 1u) ? ex2(t0) : 0.f;  // one select: dS inherits the zero
+        const float x1 = ((hm >> (c + 1)) & 1u) ? ex2(t1) : 0.f;
+        float d0, d1;
+        f2_unpack(f2_mul(f2_pack(x0, x1), f2_sub(f2_pack(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])),
+                                                  f2_pack(ddv[c], ddv[c + 1]))),
+                  d0, d1);
+        pk[i] = pack_bf16x2(x0, x1);
+        dk[i] = pack_bf16x2(d0, d1);
       }
       if (j >= 1) ok = mbar_wait(&s.mm_done, (j - 1) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {

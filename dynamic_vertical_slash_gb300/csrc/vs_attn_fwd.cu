@@ -631,10 +631,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
       uint32_t pk[32];
       float unit_sum;
       auto make_p = [&](int hh, uint64_t mask, float ref) {
-        float ps[8];
+        // two keys at a time in paired fp32: t = S scale log2(e) - ref, and
+        // four pairs of partial row sums
+        uint64_t ps2[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ps[k] = 0.f;
-        const float nref = -ref;
+        for (int k = 0; k < 4; ++k) ps2[k] = 0ull;
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
         uint32_t sr[64];
         tmem_ld32(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         tmem_ld32(tl + colS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
@@ -647,14 +649,19 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
           const uint32_t w = k < 16 ? mlo : mhi;
           const uint32_t keep0 = uint32_t(int32_t(w << (31 - ((2 * k) & 31))) >> 31);
           const uint32_t keep1 = uint32_t(int32_t(w << (31 - ((2 * k + 1) & 31))) >> 31);
-          const float p0 = __uint_as_float(
-              __float_as_uint(ex2(fmaf(__uint_as_float(sr[2 * k]), p.scale_log2, nref))) & keep0);
-          const float p1 = __uint_as_float(
-              __float_as_uint(ex2(fmaf(__uint_as_float(sr[2 * k + 1]), p.scale_log2, nref))) & keep1);
-          ps[k & 7] += p0 + p1;
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])), sc2, nref2), t0, t1);
+          const float p0 = __uint_as_float(__float_as_uint(ex2(t0)) & keep0);
+          const float p1 = __uint_as_float(__float_as_uint(ex2(t1)) & keep1);
+          ps2[k & 3] = f2_add(ps2[k & 3], f2_pack(p0, p1));
           pk[k] = pack_bf16x2(p0, p1);
         }
-        unit_sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2_unpack(ps2[0], s0, s1);
+        f2_unpack(ps2[1], s2, s3);
+        f2_unpack(ps2[2], s4, s5);
+        f2_unpack(ps2[3], s6, s7);
+        unit_sum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
       };
       auto store_p = [&](int hh) {
         tmem_st16(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
