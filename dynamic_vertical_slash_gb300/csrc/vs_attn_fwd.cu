@@ -644,15 +644,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         const uint32_t mlo = uint32_t(mask), mhi = uint32_t(mask >> 32);
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          // bit (2k, 2k + 1) of the mask moved to the sign and spread over the
-          // word: an AND keeps or clears the fp32 numerator
+          // bits 2k, 2k + 1 of the mask select the numerator or zero
           const uint32_t w = k < 16 ? mlo : mhi;
-          const uint32_t keep0 = uint32_t(int32_t(w << (31 - ((2 * k) & 31))) >> 31);
-          const uint32_t keep1 = uint32_t(int32_t(w << (31 - ((2 * k + 1) & 31))) >> 31);
           float t0, t1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])), sc2, nref2), t0, t1);
-          const float p0 = __uint_as_float(__float_as_uint(ex2(t0)) & keep0);
-          const float p1 = __uint_as_float(__float_as_uint(ex2(t1)) & keep1);
+          const float p0 = ((w >> ((2 * k) & 31)) & 1u) ? ex2(t0) : 0.f;
+          const float p1 = ((w >> ((2 * k + 1) & 31)) & 1u) ? ex2(t1) : 0.f;
           ps2[k & 3] = f2_add(ps2[k & 3], f2_pack(p0, p1));
           pk[k] = pack_bf16x2(p0, p1);
         }
