@@ -40,6 +40,24 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def max_over_ranks(value: float, device, world: int) -> float:
+    """The largest ``value`` over all ranks of the process group (a job's step
+    time is its slowest rank's); ``value`` itself for one process."""
+    if world <= 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms_max: float) -> float:
+    """Whole-job throughput: every rank runs the same step (replicas), the job
+    takes the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def _traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu capture of this
     workload, or None when there is none or the kernel sources have changed
@@ -273,13 +291,10 @@ def ours(args, w, x, rank, world):
     vs.trace_reset()
     attn.check()
     ms = statistics.mean(step_ms)
-    ms_max = ms
+    ms_max = max_over_ranks(ms, dev, world)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
         torch.distributed.barrier()
-    value = world * executed / (ms_max * 1e-3) / 1e12
+    value = job_tflops(world, executed, ms_max)
 
     # per-kernel breakdown and the roofline of the dominant attention kernel
     per_kernel = {name: {"launches": c, "ms_total": t, "ms_avg": t / max(c, 1)} for name, (c, t) in trace.items()}
@@ -384,11 +399,7 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     d2h = sum(t.numel() * t.element_size() for t in hout)
 
     def reduce_max(ms):
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ms, dev, world)
 
     # ---- serial
     din0 = [torch.empty_like(t) for t in (q, k, v, do)]
@@ -462,9 +473,9 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     pipe_ms = reduce_max(start.elapsed_time(end) / args.steps)
     for a_ in att:
         a_.check()
-    return {"value": world * executed / (pipe_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": pipe_ms,
+    return {"value": job_tflops(world, executed, pipe_ms), "unit": UNIT, "ms_per_step": pipe_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "serial": {"value": world * executed / (serial_ms * 1e-3) / 1e12, "ms_per_step": serial_ms},
+            "serial": {"value": job_tflops(world, executed, serial_ms), "ms_per_step": serial_ms},
             "path": "VSAttention.forward/backward (C ABI) with pinned host inputs and outputs; pipelined: next "
                     "step's inputs copied in and previous step's results copied out on separate streams while a "
                     "step computes (two instances, two input sets)"}
@@ -527,12 +538,8 @@ def striped(args, w, x, rank, world):
     trace = vs.trace_report()
     vs.trace_reset()
     wk.check()
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * executed / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(statistics.mean(step_ms), dev, world)
+    value = job_tflops(world, executed, ms)
     per_kernel = {name: {"launches": c, "ms_total": t, "ms_avg": t / max(c, 1)} for name, (c, t) in trace.items()}
     peaks = _peaks()
     tile = 128 * 64 * w.d
