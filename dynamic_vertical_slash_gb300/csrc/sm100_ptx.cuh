@@ -188,11 +188,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // Warp-collective forms of the three calls above: every lane of the warp
 // makes the call with the same (warp-uniform) operands and one elected lane
-// issues.  An issuing loop that the whole warp runs in step keeps descriptors
-// and TMEM addresses in the uniform datapath; issued from a one-lane branch
-// each MMA costs a round trip through the per-thread registers (measured on
-// GB300: about 114 cycles per M128 N128 K16 MMA from a lane-0 branch against
-// 70 with the warp convergent, which is the tensor pipe's own rate).
+// issues, so the issuing loop runs on a convergent warp.  Measured on GB300
+// (M128 N128 K16 bf16, chains of 8 MMAs, each chain committed and waited
+// for): 102 cycles per MMA this way against 122 from a lane-0 branch; in
+// long chains both reach the tensor pipe's own rate of about 69.
 __device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
