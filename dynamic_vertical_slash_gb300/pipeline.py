@@ -134,6 +134,21 @@ class VSAttention:
         return B_.vs_index_counts(self.arena)
 
 
+def ring_source(rank: int, s: int, world: int, inner: int = 0) -> int:
+    """The KV shard that worker ``rank`` attends to at ring step ``s`` of a
+    ``world``-worker ring: the flat ring receives from the previous worker,
+    (rank - s) mod world; with ``inner`` cards per node (Hierarchical
+    Balanced Sparse Ring Attention, Algorithm 2) step s = i * inner + j is
+    inner step j of outer step i, and reads the shard of worker
+    ((n - i) mod nodes) * inner + (c - j) mod inner for rank = n * inner + c."""
+    if not inner:
+        return (rank - s) % world
+    nodes = world // inner
+    n, c = divmod(rank, inner)
+    i, j = divmod(s, inner)
+    return ((n - i) % nodes) * inner + (c - j) % inner
+
+
 class StripedWorker:
     """One worker's side of the striped ring on one GPU (MTraining, section
     4.2 (ii) and Algorithm 2): the sequence of N_global tokens is cut into
@@ -205,12 +220,7 @@ class StripedWorker:
 
     def source(self, s: int) -> int:
         """The KV shard worker ``rank`` attends to at ring step s."""
-        if not self.inner:
-            return (self.rank - s) % self.world
-        nodes = self.world // self.inner
-        n, c = divmod(self.rank, self.inner)
-        i, j = divmod(s, self.inner)
-        return ((n - i) % nodes) * self.inner + (c - j) % self.inner
+        return ring_source(self.rank, s, self.world, self.inner)
 
     def select(self, q_global, k_global, stream=None):
         """Vertical / slash selection on the global sequence (Algorithm 1's
