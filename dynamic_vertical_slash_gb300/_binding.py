@@ -86,11 +86,17 @@ def lib(build_if_missing: bool = True):
                                ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]
     L.vs_check_status.argtypes = [_P, _P]
     L.vs_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, _P]
+    L.vs_estimate_noalloc.argtypes = [_S, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, _P,
+                                      _P, _P, _P]
+    L.vs_estimate_noalloc_status.argtypes = [_P]
+    L.vs_estimate_noalloc_selftest_plant.argtypes = [ctypes.c_int, _P]
     L.vs_status_string.argtypes = [ctypes.c_int]
     L.vs_status_string.restype = ctypes.c_char_p
     L.vs_launch_count.restype = ctypes.c_int64
     for name in ("vs_estimate", "vs_build_block_index", "vs_index_counts", "vs_attn_fwd", "vs_attn_bwd",
-                 "striped_permute", "vs_check_status", "vs_selftest_wait_timeout"):
+                 "striped_permute", "vs_check_status", "vs_selftest_wait_timeout", "vs_estimate_group",
+                 "vs_estimate_topp", "vs_select_topp", "vs_build_block_index_ex", "vs_ring_work",
+                 "vs_estimate_noalloc", "vs_estimate_noalloc_status", "vs_estimate_noalloc_selftest_plant"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

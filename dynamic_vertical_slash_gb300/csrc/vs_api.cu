@@ -91,6 +91,22 @@ static vs_status check_shape(const vs_shape* s) {
   return VS_OK;
 }
 
+// Argument checks of the estimator entry points (vs_estimate,
+// vs_estimate_group, vs_estimate_noalloc), all on the host before any CUDA
+// call: the shape checks of every entry point plus the estimator's own.
+vs_status check_estimate_args(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks,
+                              float scale, const int32_t* v_idx, const int32_t* s_idx) {
+  vs_status rc = check_shape(s);
+  if (rc != VS_OK) return rc;
+  if (!q || !k || !v_idx || !s_idx) return VS_ERR_ARG;
+  if (s->Nq != s->Nk) return VS_ERR_SHAPE;
+  if (last_q != 64) return VS_ERR_ARG;
+  if (kv < 1 || ks < 1 || kv > s->Nk || ks > s->Nk) return VS_ERR_ARG;
+  if (!(scale > 0.f)) return VS_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k)) return VS_ERR_SHAPE;
+  return VS_OK;
+}
+
 }  // namespace vs
 
 using namespace vs;
@@ -194,14 +210,9 @@ vs_status vs_estimate_group(const vs_shape* s, const void* q, const void* k, int
 static vs_status estimate_any(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks,
                               float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws,
                               size_t ws_bytes, int shared, cudaStream_t stream) {
-  vs_status rc = check_shape(s);
+  vs_status rc = check_estimate_args(s, q, k, last_q, kv, ks, scale, v_idx, s_idx);
   if (rc != VS_OK) return rc;
-  if (!q || !k || !v_idx || !s_idx || !ws) return VS_ERR_ARG;
-  if (s->Nq != s->Nk) return VS_ERR_SHAPE;
-  if (last_q != 64) return VS_ERR_ARG;
-  if (kv < 1 || ks < 1 || kv > s->Nk || ks > s->Nk) return VS_ERR_ARG;
-  if (!(scale > 0.f)) return VS_ERR_ARG;
-  if (!aligned16(q) || !aligned16(k)) return VS_ERR_SHAPE;
+  if (!ws) return VS_ERR_ARG;
   if (ws_bytes < estimate_workspace_bytes(s, last_q)) return VS_ERR_WORKSPACE;
   return launch_estimate(s, q, k, last_q, kv, ks, scale, v_idx, s_idx, v_score, s_score, ws, shared, stream);
 }

@@ -84,7 +84,17 @@ struct EstSmem {
   uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], s_full[2], s_free[2], teardown;
   uint32_t tmem_base;
   int abort_flag;
+  int skip;  // the status word already held a failure when the CTA started
 };
+
+// A failure recorded earlier in this call (or left in the status word by an
+// earlier call) makes the estimator's later kernels skip their work, so that
+// no kernel reads scratch a failed kernel left unwritten.  VS_ERR_SCORE is a
+// per-list verdict of the top-p step, not a failure of the scores.
+__device__ __forceinline__ bool est_failed(const int* err) {
+  const int w = *reinterpret_cast<const volatile int*>(err);
+  return w != 0 && w != VS_ERR_SCORE;
+}
 
 // First query head (within the group) of row tile mt's two heads; a tile's
 // second head may not exist (odd g): its rows load the first head again and
@@ -118,10 +128,11 @@ __device__ __forceinline__ void est_mma(EstSmem<D>& s, int qb, int kb, uint32_t 
 }
 
 template <int D>
-__device__ __forceinline__ void est_init(EstSmem<D>& s, int ncols) {
+__device__ __forceinline__ void est_init(EstSmem<D>& s, int ncols, const int* err) {
   const int warp = threadIdx.x / 32;
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
+    s.skip = est_failed(err) ? 1 : 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.q_full[i], 1);
       mbar_init(&s.q_empty[i], 1);
@@ -174,8 +185,8 @@ __global__ void __launch_bounds__(kEstThreads, 1)
   const int mt = int(blockIdx.x) % p.MT, bhk = int(blockIdx.x) / p.MT;
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv, sp = blockIdx.y;
   const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys;
-  const int nchunk = NT > sp ? (NT - sp + kSplits - 1) / kSplits : 0;
-  est_init<D>(s, 256);
+  est_init<D>(s, 256, p.err);
+  const int nchunk = (NT > sp && !s.skip) ? (NT - sp + kSplits - 1) / kSplits : 0;
   const uint32_t tmem = s.tmem_base;
   const Abort ab{&s.abort_flag, p.err};
   bool mma_issued = false;
@@ -245,7 +256,7 @@ __global__ void __launch_bounds__(kEstThreads, 1)
       s.red_l[r] = l;
     }
     bar_sync_and(1, kEstCompute, true);
-    if (half == 0 && ok) {
+    if (half == 0 && ok && !s.skip) {
       const float mo = s.red_m[r], lo = s.red_l[r];
       const float mn = fmaxf(m, mo);
       const float ln = (mn == -INFINITY) ? 0.f
@@ -263,6 +274,7 @@ __global__ void __launch_bounds__(kEstThreads, 1)
 
 // LSE (log2 units) of every (b, h, last-64 row) from its key-split partials.
 __global__ void est_lse(const EstParams p) {
+  if (est_failed(p.err)) return;
   const int bh = blockIdx.x, i = threadIdx.x;
   const float2* pp = p.part + int64_t(bh) * kSplits * kLastQ + i;
   float m = -INFINITY, l = 0.f;
@@ -287,14 +299,15 @@ __global__ void __launch_bounds__(kEstThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int bhk = blockIdx.x, tile = blockIdx.y;
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
-  const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys, MT = p.MT;
+  const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys;
   const int64_t m0 = int64_t(tile) * kEstKeys;
-  est_init<D>(s, 256);
+  est_init<D>(s, 256, p.err);
+  const int MT = s.skip ? 0 : p.MT;
   const uint32_t tmem = s.tmem_base;
   const Abort ab{&s.abort_flag, p.err};
   bool mma_issued = false;
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && MT > 0) {
       mbar_arrive_expect_tx(&s.k_full[0], NH * kEstKeys * 128);
       for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.k[0][hf], &tmK, &s.k_full[0], 64 * hf, hk, int(m0), b);
       for (int mt = 0; mt < MT; ++mt) {
@@ -304,7 +317,7 @@ __global__ void __launch_bounds__(kEstThreads, 1)
       }
     }
   } else if (warp == 1) {
-    {
+    if (MT > 0) {
       bool ok = mbar_wait_warp(&s.k_full[0], 0, ab, VS_ERR_TIMEOUT);
       for (int mt = 0; ok && mt < MT; ++mt) {
         const int qb = mt & 1;
@@ -384,6 +397,7 @@ __global__ void __launch_bounds__(kEstThreads, 1)
 }
 
 __global__ void est_scombine(const EstParams p) {
+  if (est_failed(p.err)) return;
   const int bh = blockIdx.y;
   const int N = p.N, NT = (N + kEstKeys - 1) / kEstKeys;
   const int o = blockIdx.x * blockDim.x + threadIdx.x;
@@ -492,9 +506,14 @@ struct TopkParams {
   int32_t* out2;
   int N, k, k2;
   int rep;             // copies of each list (the heads of a group sharing it)
+  const int* err;      // status word: a recorded failure skips the selection
 };
 
 __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
+  __shared__ int skip;
+  if (threadIdx.x == 0) skip = est_failed(p.err);
+  __syncthreads();
+  if (skip) return;
   const int l = blockIdx.x, which = blockIdx.y;
   const uint32_t* x = reinterpret_cast<const uint32_t*>(which == 0 ? p.score : p.score2) + int64_t(l) * p.N;
   const int k = which == 0 ? p.k : p.k2;
@@ -509,7 +528,8 @@ __global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
 // Per-KV-group sums of the heads' scores, added in head order (fp32), for
 // the shared selection: gv[b, hk, m] = sum_j v[b, hk g + j, m].
 __global__ void __launch_bounds__(256) est_group_sum(const float* v, const float* s, float* gv, float* gs, int N,
-                                                     int g) {
+                                                     int g, const int* err) {
+  if (est_failed(err)) return;
   const int l = blockIdx.y;  // b * Hkv + hk
   const int64_t m = int64_t(blockIdx.x) * 256 + threadIdx.x;
   if (m >= N) return;
@@ -561,6 +581,7 @@ struct ToppShared {
   uint64_t red[32];
   uint64_t prefix, want;
   int above, bad, k;
+  int skip;
 };
 
 // Saturating block sum of one value per thread (values <= 2^62).
@@ -638,8 +659,12 @@ __global__ void __launch_bounds__(kTopkThreads) est_topp(const ToppParams p) {
   const int N = p.N;
   const float* xf = (which == 0 ? p.v : p.s) + int64_t(bh) * N;
   const uint32_t* x = reinterpret_cast<const uint32_t*>(xf);
-  if (threadIdx.x == 0) S.bad = 0;
+  if (threadIdx.x == 0) {
+    S.bad = 0;
+    S.skip = est_failed(p.err);
+  }
   __syncthreads();
+  if (S.skip) return;
   // 1. validate, total mass; the slash list is pooled per 64-offset block
   uint64_t mine = 0;
   int bad = 0;
@@ -742,10 +767,11 @@ vs_status launch_est_kernels(const vs_shape* s, const void* q, const void* k, Es
   tp.k = kv;
   tp.k2 = ks;
   tp.rep = 1;
+  tp.err = p.err;
   int lists = BH;
   if (p.gv) {
     trace_begin("est_group_sum", st);
-    est_group_sum<<<dim3((s->Nk + 255) / 256, BHK), 256, 0, st>>>(p.v, p.s, p.gv, p.gs, s->Nk, p.g);
+    est_group_sum<<<dim3((s->Nk + 255) / 256, BHK), 256, 0, st>>>(p.v, p.s, p.gv, p.gs, s->Nk, p.g, p.err);
     trace_end(st);
     note_launch();
     tp.score = p.gv;
@@ -868,15 +894,32 @@ constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
-// Device address of the static scratch on the current device, looked up once
-// per device (host code may not use the array's name as a device address).
-void* noalloc_scratch_address(int dev) {
+// Device address of the static scratch on the current device (host code may
+// not use the array's name as a device address), looked up once per device.
+// The look-up may load the module onto the device, which must not happen
+// inside a stream capture: while `stream` is capturing and the address is not
+// known yet, the call is refused with VS_ERR_ARG.
+vs_status noalloc_scratch_address(cudaStream_t stream, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return VS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return VS_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return VS_ERR_ARG;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return VS_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
   }
+  *out = g_noalloc_ptr[dev];
+  return VS_OK;
+}
+
+// The scratch address of the current device if a call has looked it up.
+void* noalloc_known_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
   return g_noalloc_ptr[dev];
 }
 
@@ -900,23 +943,19 @@ extern "C" vs_status vs_estimate_noalloc(const vs_shape* s, const void* q, const
                                          float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score,
                                          cudaStream_t stream) {
   using namespace vs;
-  // every check happens on the host, before any CUDA call
-  if (!s || !q || !k || !v_idx || !s_idx || !v_score || !s_score) return VS_ERR_ARG;
-  if (s->B < 1 || s->Nk < 64 || s->Hq < 1 || s->Hkv < 1 || (s->d != 64 && s->d != 128)) return VS_ERR_SHAPE;
-  if (s->Nq != s->Nk || s->Nk % 64 || s->Hq % s->Hkv) return VS_ERR_SHAPE;
-  for (int i = 0; i < 3; ++i)
-    if (s->sq[i] <= 0 || s->sk[i] <= 0 || s->sq[i] % 8 || s->sk[i] % 8) return VS_ERR_SHAPE;
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return VS_ERR_SHAPE;
-  if (last_q != 64) return VS_ERR_ARG;
-  if (kv < 1 || ks < 1 || kv > s->Nk || ks > s->Nk || !(scale > 0.f)) return VS_ERR_ARG;
+  // every argument check happens on the host, before any CUDA call, and
+  // refuses exactly what vs_estimate refuses (plus missing score buffers)
+  if (!v_score || !s_score) return VS_ERR_ARG;
+  vs_status rc = check_estimate_args(s, q, k, last_q, kv, ks, scale, v_idx, s_idx);
+  if (rc != VS_OK) return rc;
   int64_t off_part = 0, off_lse = 0, off_spart = 0;
   if (size_t(noalloc_layout(s, &off_part, &off_lse, &off_spart)) > kNoAllocScratchBytes) return VS_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return VS_ERR_CUDA;
-  uint8_t* W = static_cast<uint8_t*>(noalloc_scratch_address(dev));
-  if (!W) return VS_ERR_CUDA;
+  void* base = nullptr;
+  if ((rc = noalloc_scratch_address(stream, &base)) != VS_OK) return rc;
+  uint8_t* W = static_cast<uint8_t*>(base);
   // The kernels write every scratch element they later read within the
-  // call; only the status header is cleared.
+  // call, unless a kernel records a failure in the status word, after which
+  // the later kernels skip their work; only the status header is cleared.
   if (cudaMemsetAsync(W, 0, 256, stream) != cudaSuccess) return VS_ERR_CUDA;
   EstParams p = est_params(s, scale, reinterpret_cast<int*>(W));
   p.part = reinterpret_cast<float2*>(W + off_part);
@@ -925,4 +964,19 @@ extern "C" vs_status vs_estimate_noalloc(const vs_shape* s, const void* q, const
   p.spart = reinterpret_cast<float*>(W + off_spart);
   p.s = s_score;
   return launch_est(s, q, k, p, kv, ks, v_idx, s_idx, stream);
+}
+
+extern "C" vs_status vs_estimate_noalloc_status(cudaStream_t stream) {
+  void* W = noalloc_known_address();
+  if (!W) return VS_OK;  // no call has run on this device
+  return vs_check_status(W, stream);
+}
+
+extern "C" vs_status vs_estimate_noalloc_selftest_plant(int code, cudaStream_t stream) {
+  void* W = nullptr;
+  vs_status rc = noalloc_scratch_address(stream, &W);
+  if (rc != VS_OK) return rc;
+  const int32_t word = code;
+  if (cudaMemcpyAsync(W, &word, sizeof(word), cudaMemcpyHostToDevice, stream) != cudaSuccess) return VS_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }

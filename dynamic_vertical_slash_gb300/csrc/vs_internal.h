@@ -21,6 +21,10 @@ vs_status make_tmap_bshd(CUtensorMap* m, const void* base, int B, int N, int H, 
 
 Geo make_geo(const vs_shape* s, const ArenaHeader& h);
 
+// Host-side argument checks shared by the estimator entry points.
+vs_status check_estimate_args(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks,
+                              float scale, const int32_t* v_idx, const int32_t* s_idx);
+
 // Kernel launchers (one per translation unit).
 vs_status launch_fwd(const vs_shape* s, const Geo& G, const void* q, const void* k, const void* v,
                      const void* arena, float scale, void* o, float* lse, float* o_acc, int* err,

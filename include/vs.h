@@ -20,13 +20,16 @@
  *    16-byte aligned (TMA requirement).
  *  - The KV head of query head h is h / (Hq / Hkv) (GQA grouping).
  *  - The caller owns every buffer.  The library never allocates, frees or
- *    synchronises, except vs_check_status, which synchronises `stream`.
+ *    synchronises, except the status, count and trace readers
+ *    (vs_check_status, vs_estimate_noalloc_status, vs_index_counts,
+ *    vs_trace_report), which synchronise and say so.
  *  - Every compute call is asynchronous on `stream`.
  *  - Argument and shape errors are returned synchronously and nothing is
  *    launched.  Errors found on the device (bad index lists, a bounded wait
  *    that ran out) are recorded in the first 32-bit word of the workspace or
  *    index arena that the call received; kernels never trap.  Read them with
- *    vs_check_status.
+ *    vs_check_status.  A status word that already holds a failure when a
+ *    call starts makes that call's kernels skip their work.
  *  - Same inputs give the same output bits: no floating-point atomics touch
  *    any output or score.
  *  - Supported: head_dim d in {64, 128}; N a multiple of 64; Hq a multiple of
@@ -172,15 +175,36 @@ vs_status vs_select_topp(int B, int H, int N, const float* v_score, const float*
  *   343936).
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call on a device shares the one array:
- * calls that overlap on the GPU (other streams, other host threads) race and
- * must be serialised by the caller.  Each call writes every scratch element
- * it reads, so stale contents from a previous call do not matter.
+ * (cudaGetSymbolAddress, with that device current), which may load the
+ * library's module onto the device; make that first call before any stream
+ * capture.  A first call made while `stream` is capturing is refused with
+ * VS_ERR_ARG before any CUDA work.  Every call on a device shares the one
+ * array: calls that overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.  The array keeps the last
+ * call's contents; each call clears the status header at its start and
+ * writes every other scratch element it reads.
+ *
+ * Device errors (VS_ERR_TIMEOUT from a bounded wait) go to the status word
+ * at the start of the array instead of a caller workspace; the kernels after
+ * the failing one then skip their work, leaving the outputs unspecified.
+ * Read the word with vs_estimate_noalloc_status after the call and before
+ * the next call on the device, which clears it.
  * ------------------------------------------------------------------------- */
 vs_status vs_estimate_noalloc(const vs_shape* shape, const void* q, const void* k, int last_q, int kv, int ks,
                               float scale, int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score,
                               cudaStream_t stream);
+
+/* Status of the last vs_estimate_noalloc call on the current device: reads
+ * the scratch's status word, resets it to VS_OK and returns the code it held
+ * (VS_OK if no call has run on the device).  Synchronises `stream`, which
+ * should be the stream of that call. */
+vs_status vs_estimate_noalloc_status(cudaStream_t stream);
+
+/* Self-test of the status path above (no counterpart in the paper): writes
+ * `code` into the scratch's status word of the current device, as a failing
+ * kernel would, and synchronises `stream`.  vs_estimate_noalloc_status then
+ * returns `code`. */
+vs_status vs_estimate_noalloc_selftest_plant(int code, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * vs_build_block_index -- the sparse index (Algorithm 1 `sparseformat`,

@@ -88,3 +88,32 @@ def test_workspace_queries(L):
     a = L.vs_attn_bwd_workspace(ctypes.byref(sh), 128)
     b = L.vs_attn_bwd_workspace(ctypes.byref(sh), 1024)
     assert b > a > 0
+
+
+def test_estimator_entry_points_refuse_the_same_arguments(L):
+    # vs_estimate_noalloc validates exactly what vs_estimate validates (one
+    # shared routine), on the host, before any CUDA call
+    fake = ctypes.c_void_p(0x10000)
+    cases = []
+    for kw in (dict(d=96), dict(N=1000), dict(Hq=3, Hkv=2), dict(Hq=130, Hkv=2), dict(B=0)):
+        cases.append((_shape(**kw), 64, 8, 8, 0.1))
+    sh = _shape()
+    sh.sq[2] = 32  # head stride below d
+    cases.append((sh, 64, 8, 8, 0.1))
+    sh = _shape()
+    sh.sk[1] = 12  # token stride not a multiple of 8 elements
+    cases.append((sh, 64, 8, 8, 0.1))
+    sh = _shape()
+    sh.Nk = 512  # Nq != Nk
+    cases.append((sh, 64, 8, 8, 0.1))
+    for args in ((_shape(), 32, 8, 8, 0.1), (_shape(), 64, 0, 8, 0.1), (_shape(), 64, 8, 2000, 0.1),
+                 (_shape(), 64, 8, 8, -1.0)):
+        cases.append(args)
+    for sh, last_q, kv, ks, scale in cases:
+        a = L.vs_estimate(ctypes.byref(sh), fake, fake, last_q, kv, ks, scale, fake, fake, None, None, fake, 1 << 40,
+                          None)
+        b = L.vs_estimate_noalloc(ctypes.byref(sh), fake, fake, last_q, kv, ks, scale, fake, fake, fake, fake, None)
+        assert a == b != 0, (a, b)
+    # missing score buffers are refused by the no-alloc entry point (it keeps no scores of its own)
+    sh = _shape()
+    assert L.vs_estimate_noalloc(ctypes.byref(sh), fake, fake, 64, 8, 8, 0.1, fake, fake, None, fake, None) == 1

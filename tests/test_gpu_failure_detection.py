@@ -43,3 +43,35 @@ def test_bounded_wait_runs_out_and_context_survives():
     p = oracle.Problem(host_f64(x["q"]), host_f64(x["k"]), host_f64(x["v"]), iv, is_, 1 / math.sqrt(d))
     ref = oracle.attention(p)
     assert rel_l2(host_f64(o), ref["o"]) <= 1e-2
+
+
+def test_estimator_skips_its_work_after_a_recorded_failure():
+    # a failure already in the status word (as a timed-out kernel of the same
+    # call would leave it) makes every estimator kernel skip: no kernel reads
+    # scratch that a failed kernel left unwritten, the outputs stay as they
+    # were, and the code is reported once
+    import dynamic_vertical_slash_gb300 as vs
+
+    B, N, Hq, Hkv, d = 1, 1024, 2, 1, 64
+    w, x = make_inputs(B, N, Hq, Hkv, d, seed=32, n_out=4, n_slash=1)
+    q, k = dev_bf16(x["q"]), dev_bf16(x["k"])
+    iv_ok, is_ok = vs.vs_estimate(q, k, 16, 16)
+    import ctypes
+
+    need = vs.lib().vs_estimate_workspace(ctypes.byref(vs.make_shape(q, k)), 64)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ws[:4].view(torch.int32).fill_(5)  # VS_ERR_TIMEOUT
+    iv = torch.full((B, Hq, 16), -7, dtype=torch.int32, device="cuda")
+    is_ = torch.full((B, Hq, 16), -7, dtype=torch.int32, device="cuda")
+    vsc = torch.full((B, Hq, N), -1.0, device="cuda")
+    ssc = torch.full((B, Hq, N), -1.0, device="cuda")
+    vs.vs_estimate(q, k, 16, 16, v_idx=iv, s_idx=is_, v_score=vsc, s_score=ssc, ws=ws)
+    torch.cuda.synchronize()
+    assert bool((iv == -7).all()) and bool((is_ == -7).all())
+    assert bool((vsc == -1).all()) and bool((ssc == -1).all())
+    assert vs.vs_check_status(ws) == 5
+    # with the word read (and reset) the same workspace computes again
+    vs.vs_estimate(q, k, 16, 16, v_idx=iv, s_idx=is_, v_score=vsc, s_score=ssc, ws=ws)
+    torch.cuda.synchronize()
+    assert vs.vs_check_status(ws) == 0
+    assert torch.equal(iv, iv_ok) and torch.equal(is_, is_ok)

@@ -3,8 +3,10 @@ allocate device memory while they run (an engine that owns all device memory,
 or a latency-critical loop that cannot afford cudaMalloc's device-wide
 synchronisation).  Its scratch is a fixed array in the library's static device
 memory; this test checks, through the C ABI, that two calls in a row give the
-same selection and scores as vs_estimate with a caller workspace, and that
-a problem too large for the fixed scratch is refused before any launch.
+same selection and scores as vs_estimate with a caller workspace, that the
+status reader of the fixed scratch reports a clean run and a recorded device
+error (planted through the self-test hook), and that a problem too large for
+the fixed scratch is refused before any launch.
 
 Kept in a file of its own, named to be collected last."""
 import ctypes
@@ -24,6 +26,10 @@ def _lib():
                                       ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]
     L.vs_estimate_noalloc.restype = ctypes.c_int
+    L.vs_estimate_noalloc_status.argtypes = [ctypes.c_void_p]
+    L.vs_estimate_noalloc_status.restype = ctypes.c_int
+    L.vs_estimate_noalloc_selftest_plant.argtypes = [ctypes.c_int, ctypes.c_void_p]
+    L.vs_estimate_noalloc_selftest_plant.restype = ctypes.c_int
     return vs, L
 
 
@@ -62,6 +68,29 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         for a, b in ((v2, vsc), (s2, ssc)):
             tol = 1e-4 * float(b.abs().max())
             assert float((a - b).abs().max()) <= tol
+        # no device error was recorded in the fixed scratch
+        assert L.vs_estimate_noalloc_status(torch.cuda.current_stream().cuda_stream) == 0
+
+
+def test_noalloc_status_word_reports_device_errors_and_is_cleared():
+    vs, L = _lib()
+    st = torch.cuda.current_stream().cuda_stream
+    q, k = _inputs(1, 1024, 2, 1, 64, 14)
+    rc, _ = _noalloc(vs, L, q, k, 16, 16, 0.125)
+    assert rc == 0
+    assert L.vs_estimate_noalloc_status(st) == 0
+    # a failing kernel writes its code into the status word; the reader
+    # returns it once and resets the word
+    assert L.vs_estimate_noalloc_selftest_plant(5, st) == 0  # VS_ERR_TIMEOUT
+    assert L.vs_estimate_noalloc_status(st) == 5
+    assert L.vs_estimate_noalloc_status(st) == 0
+    # the next call clears a word nobody read, and computes again
+    assert L.vs_estimate_noalloc_selftest_plant(5, st) == 0
+    rc, (iv, is_, v2, s2) = _noalloc(vs, L, q, k, 16, 16, 0.125)
+    torch.cuda.synchronize()
+    assert rc == 0 and L.vs_estimate_noalloc_status(st) == 0
+    iv_ref, is_ref = vs.vs_estimate(q, k, 16, 16, 0.125, 64)
+    assert torch.equal(iv, iv_ref) and torch.equal(is_, is_ref)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
