@@ -59,18 +59,20 @@ def job_tflops(world: int, flops_per_rank: float, ms_max: float) -> float:
 
 
 def _traffic(workload: str, kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu capture of this
-    workload, or None when there is none or the kernel sources have changed
-    since it was taken (the capture records the sources' digest)."""
+    """DRAM bytes per launch of `kernel` at `workload` from the committed ncu
+    summary (profiles/dram_traffic_<workload>.json), or None when there is
+    none or the kernel's sources have changed since it was taken (the summary
+    records each kernel's source digest: contents only, no paths)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic_%s.json" % workload)
     try:
         with open(path) as fh:
             d = json.load(fh)
         from dynamic_vertical_slash_gb300 import _build
 
-        if d.get("csrc_digest") != _build._digest():
+        rec = d["kernels"][kernel]
+        if rec.get("source_digest") != _build.source_digest(kernel):
             return None
-        return float(d["bytes_per_launch"][kernel])
+        return float(rec["bytes_per_launch"])
     except Exception:
         return None
 
@@ -147,67 +149,180 @@ def _gpu_id(dev_index: int) -> str:
         return vis.split(",")[dev_index] if vis else str(dev_index)
 
 
+# ------------------------------------------------------------------ accounting
+def query_cover_units(iv: np.ndarray, is_: np.ndarray, N: int) -> np.ndarray:
+    """Query-major work units (128 x 64 entries) of the kernels' cover of an
+    unstriped selection, from the cover's definition: per head the selected
+    offsets dilated to E = {u : some selected o in [u - 127, u]}, covered
+    greedily by 64-wide intervals starting at u_s; the 128-row tile t takes one
+    slash unit per u_s <= 128 t + 127 and one bar chunk per 64 selected
+    columns whose first column is <= 128 t + 127.  Lists may end in -1.
+    Returns int64 [B, H, 2] (slash tiles, bar chunks)."""
+    B, H = iv.shape[:2]
+    T = (N + 127) // 128
+    last = 128 * np.arange(T, dtype=np.int64) + 127
+    out = np.zeros((B, H, 2), np.int64)
+    for b in range(B):
+        for h in range(H):
+            offs = np.unique(is_[b, h][is_[b, h] >= 0].astype(np.int64))
+            starts, nxt, i = [], 0, 0
+            while i < offs.size:  # maximal runs of E, then greedy 64-wide starts
+                a, e = offs[i], offs[i] + 127
+                i += 1
+                while i < offs.size and offs[i] <= e + 1:
+                    e = offs[i] + 127
+                    i += 1
+                u = max(a, nxt)
+                while u <= e:
+                    starts.append(u)
+                    u += 64
+                nxt = max(nxt, u)
+            starts = np.asarray(starts, np.int64)
+            cols = np.sort(iv[b, h][iv[b, h] >= 0].astype(np.int64))
+            first = cols[::64]
+            out[b, h, 0] = np.searchsorted(starts, last, side="right").sum()
+            out[b, h, 1] = np.searchsorted(first, last, side="right").sum()
+    return out
+
+
+def mask_entries(iv: np.ndarray, is_: np.ndarray, N: int) -> np.ndarray:
+    """|M| per head of the exact mask M[n, m] = (m <= n) and (m in iv or
+    n - m in is) on an unstriped sequence of N tokens, in closed form: the
+    column entries sum(N - m), the diagonal entries sum(N - o), minus the
+    entries on both (for each selected column m, the selected offsets
+    o <= N - 1 - m).  int64 [B, H]."""
+    B, H = iv.shape[:2]
+    out = np.zeros((B, H), np.int64)
+    for b in range(B):
+        for h in range(H):
+            cols = np.unique(iv[b, h][iv[b, h] >= 0].astype(np.int64))
+            offs = np.unique(is_[b, h][is_[b, h] >= 0].astype(np.int64))
+            both = np.searchsorted(offs, N - 1 - cols, side="right").sum()
+            out[b, h] = (N - cols).sum() + (N - offs).sum() - both
+    return out
+
+
+def step_flops(units_q: np.ndarray, entries: np.ndarray, B: int, N: int, Hq: int, d: int) -> dict:
+    """Executed (query-major cover, 4 d + 10 d per covered entry), algorithmic
+    (the same per entry of the exact mask, MagiAttention's cost = mask area)
+    and dense causal FLOPs of one forward + backward."""
+    area_q = float(units_q.sum()) * 128 * 64
+    m = float(entries.sum())
+    causal = B * Hq * N * (N + 1) / 2.0
+    return {"executed": 14.0 * area_q * d, "algorithmic": 14.0 * m * d, "dense": 14.0 * causal * d,
+            "mask_entries": m, "mask_density": m / causal, "executed_density": area_q / causal}
+
+
 # ------------------------------------------------------------------ CPU oracle
-def _oracle_sample(x, w, target_s: float = 12.0, rows_hint: int = 0):
-    """Times the CPU oracle on a bounded sample of the workload: head 0 (and
-    its KV head), the last R query rows, forward (O, LSE) and the query-side
-    backward (dQ).  Credited FLOPs: 10 d per mask entry of those rows (4 d
-    forward, 6 d for the S recompute, dP and dQ products)."""
-    import oracle
+def _oracle_inputs(x, h: int, hk: int):
     import synth
 
-    q = synth.bf16_to_f32(x["q"][:, :, 0:1]).astype(np.float64)
-    k = synth.bf16_to_f32(x["k"][:, :, 0:1]).astype(np.float64)
-    v = synth.bf16_to_f32(x["v"][:, :, 0:1]).astype(np.float64)
-    do = synth.bf16_to_f32(x["dout"][:, :, 0:1]).astype(np.float64)
-    t0 = time.perf_counter()
-    vs_, ss_ = oracle.estimate(q[:1], k[:1], w.last_q, w.scale)
-    iv, is_ = oracle.select(vs_, ss_, w.kv, w.ks)
-    t_est = time.perf_counter() - t0
-    p = oracle.Problem(q[:1], k[:1], v[:1], iv, is_, w.scale, dout=do[:1])
-    N = w.N
-
-    def run(R):
-        rows = np.array([(0, 0, n) for n in range(N - R, N)], np.int32)
-        t = time.perf_counter()
-        oracle.rows(p, rows)
-        dt = time.perf_counter() - t
-        return dt, rows
-
-    R = rows_hint or 64
-    if not rows_hint:
-        dt, _ = run(R)
-        R = int(max(16, min(N, R * target_s / max(dt, 1e-3))))
-    return p, run, R, t_est
+    f64 = lambda a: synth.bf16_to_f32(a).astype(np.float64)
+    return (f64(x["q"][:, :, h:h + 1]), f64(x["k"][:, :, hk:hk + 1]), f64(x["v"][:, :, hk:hk + 1]),
+            f64(x["dout"][:, :, h:h + 1]))
 
 
-def _mask_entries(p, R, N):
+def oracle_step_sample(x, w, h: int, R: int):
+    """One bounded sample of the whole step, run by the oracle as it stands:
+    query head h's estimate and selection (Algorithm 1) and a complete
+    forward + backward on its exact mask restricted to R query rows spread
+    evenly over the sequence (O, LSE, dQ of those rows and the dK, dV they
+    contribute to every key).  Returns (seconds, mask entries of the sample,
+    seconds of the estimate + selection)."""
     import oracle
 
-    sub = oracle.Problem(p.q[:, N - R:], p.k, p.v, p.iv, p.is_, p.scale, qpos=np.arange(N - R, N), n_global=N)
-    return oracle.mask_count(sub)
+    q, k, v, do = _oracle_inputs(x, h, h // (w.Hq // w.Hkv))
+    t0 = time.perf_counter()
+    vs_, ss_ = oracle.estimate(q, k, w.last_q, w.scale)
+    iv, is_ = oracle.select(vs_, ss_, w.kv, w.ks)
+    t_est = time.perf_counter() - t0
+    rows = np.sort(w.N - 1 - (w.N // R) * np.arange(R)).astype(np.int64)
+    p = oracle.Problem(q[:, rows], k, v, iv, is_, w.scale, dout=do[:, rows], qpos=rows, n_global=w.N)
+    t1 = time.perf_counter()
+    oracle.attention(p)
+    t_attn = time.perf_counter() - t1
+    return t_attn + t_est, oracle.mask_count(p), t_est, t_attn
+
+
+def oracle_baseline(x, w, target_s: float, heads, executed: float, algorithmic: float):
+    """The oracle's time for a whole step, extrapolated from bounded samples
+    (oracle_step_sample on the given query heads): per head the estimate plus
+    N / R times the R-row forward + backward, summed over B * Hq heads.  Also
+    its rates on the GPU line's two accountings (executed cover FLOPs and
+    algorithmic mask FLOPs per step)."""
+    import oracle
+
+    R = 256
+    _, _, _, ta = oracle_step_sample(x, w, heads[0], R)  # calibration
+    R = int(max(64, min(w.N, R * target_s / max(1, len(heads)) / max(ta, 1e-3))))
+    R = max(64, min(w.N, R))
+    per_head, ent, secs = [], 0, 0.0
+    for h in heads:
+        t, e, te, ta = oracle_step_sample(x, w, h, R)
+        per_head.append(te + ta * w.N / R)
+        ent += e
+        secs += t
+    full = w.B * w.Hq * float(np.mean(per_head))
+    return {"value": executed / full / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "value_algorithmic": algorithmic / full / 1e12,
+            "value_sample_mask_entries": 14.0 * w.d * ent / secs / 1e12,
+            "extrapolated_full_step_s": full, "extrapolated": True,
+            "sample": ("query heads %s of %s, each: the estimate + selection and a full forward + backward (O, LSE, "
+                       "dQ, dK, dV) on the exact mask of %d query rows spread evenly over the sequence, fp64; "
+                       "%.1f s of oracle time, %d mask entries. Whole step extrapolated as B*Hq * (estimate + N/R * "
+                       "sample); value = the GPU line's executed FLOPs per step / that time, value_algorithmic = "
+                       "14 d FLOPs per mask entry of the step / that time" % (list(heads), w.name, R, secs, ent))}
+
+
+def _selection_all_heads(x, w):
+    """The oracle's selection for every query head (outside any timing)."""
+    import oracle
+
+    iv = np.zeros((w.B, w.Hq, w.kv), np.int32)
+    is_ = np.zeros((w.B, w.Hq, w.ks), np.int32)
+    for h in range(w.Hq):
+        q, k, _, _ = _oracle_inputs(x, h, h // (w.Hq // w.Hkv))
+        a, c = oracle.estimate(q, k, w.last_q, w.scale)
+        iv[:, h:h + 1], is_[:, h:h + 1] = oracle.select(a, c, w.kv, w.ks)
+    return iv, is_
 
 
 def reference_arm(args, w, x):
-    """--impl reference: the oracle as it stands, on the host cores."""
+    """--impl reference: the oracle as it stands, on the host cores.  Each
+    step is one bounded sample of the workload (oracle_step_sample, query
+    head rotating with the step); the line's value puts it on the GPU line's
+    accounting: executed cover FLOPs of a whole step over the extrapolated
+    whole-step time."""
     import oracle
 
-    p, run, R, t_est = _oracle_sample(x, w, target_s=max(1.0, 150.0 / max(1, args.steps + args.warmup)))
-    entries = _mask_entries(p, R, w.N)
-    flops = 10.0 * w.d * entries
-    for _ in range(args.warmup):
-        run(R)
-    times = [run(R)[0] for _ in range(args.steps)]
+    iv, is_ = _selection_all_heads(x, w)
+    fl = step_flops(query_cover_units(iv, is_, w.N), mask_entries(iv, is_, w.N), w.B, w.N, w.Hq, w.d)
+    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    _, _, _, ta = oracle_step_sample(x, w, 0, 256)
+    R = int(max(64, min(w.N, 256 * budget / max(ta, 1e-3))))
+    for i in range(args.warmup):
+        oracle_step_sample(x, w, i % w.Hq, R)
+    times, full = [], []
+    for i in range(args.steps):
+        t, _, te, ta = oracle_step_sample(x, w, i % w.Hq, R)
+        times.append(t)
+        full.append(w.B * w.Hq * (te + ta * w.N / R))
     ms = 1e3 * statistics.mean(times)
-    value = flops / (ms * 1e-3) / 1e12
-    sample = ("query head 0, last %d rows of the %s workload: forward (O, LSE) + dQ, fp64, %d mask entries; "
-              "credited 10 d FLOPs per entry" % (R, w.name, entries))
+    full_s = statistics.mean(full)
+    value = fl["executed"] / full_s / 1e12
+    sample = ("per step one query head (rotating) of the %s workload: estimate + selection and a full forward + "
+              "backward on the exact mask of %d query rows spread evenly over the sequence, fp64; whole step "
+              "extrapolated as B*Hq * (estimate + N/R * sample) = %.1f s; value = executed cover FLOPs of a whole "
+              "step (%.4g, the GPU line's accounting) / that time" % (w.name, R, full_s, fl["executed"]))
+    cpu = {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": sample,
+           "value_algorithmic": fl["algorithmic"] / full_s / 1e12, "extrapolated_full_step_s": full_s,
+           "extrapolated": True}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _config(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": sample},
+            "config": _config(w), "cpu_baseline": cpu,
+            "flops": {"executed_per_step": fl["executed"], "algorithmic_per_step": fl["algorithmic"],
+                      "mask_density": fl["mask_density"], "executed_density": fl["executed_density"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     return line
 
@@ -268,6 +383,7 @@ def ours(args, w, x, rank, world):
     counts = attn.counts()
     fl = flop_counts(counts, w.d)
     executed = fl["fwd_executed"] + fl["bwd_executed"]
+    acct = _accounting(attn, counts, w)
 
     # ---------------- timed region: K steps, L2 flushed between them
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -366,12 +482,46 @@ def ours(args, w, x, rank, world):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
             "pct_bf16_peak": 100.0 * value / world / peaks["bf16_burst"],
+            "value_algorithmic": job_tflops(world, acct["algorithmic_per_step"], ms_max) if acct else None,
             "flops": {"executed_per_step": executed, "issued_per_step": fl["fwd_issued"] + fl["bwd_issued"],
                       "dense_causal_per_step": dense_f["fwd"] + dense_f["bwd"],
-                      "executed_density": executed / (dense_f["fwd"] + dense_f["bwd"]), "units": units},
+                      "executed_density": executed / (dense_f["fwd"] + dense_f["bwd"]), "units": units,
+                      **(acct or {})},
             "kernels": per_kernel, "attention_ms_per_step": attn_ms, "step_ms_all": step_ms}
     line.update(extra)
     return line, clk.summary()
+
+
+def _accounting(attn, counts, w):
+    """Algorithmic FLOPs and mask density of the step on the GPU: |M| per head
+    counted by vs_ring_work with one worker (every mask entry), checked against
+    the closed form on the host; the host model of the query-major cover is
+    checked against the arena's unit counts.  None for the block-cover variant
+    (its mask is not the exact VS mask)."""
+    import torch
+
+    import dynamic_vertical_slash_gb300 as vs
+
+    if attn.block_cover:
+        return None
+    per_head = np.zeros((w.B, w.Hq), np.int64)
+    for b in range(w.B):
+        for h in range(w.Hq):
+            cnt = vs.vs_ring_work(attn.v_idx[b:b + 1, h:h + 1].contiguous(),
+                                  attn.s_idx[b:b + 1, h:h + 1].contiguous(), w.N, 1)
+            per_head[b, h] = int(cnt.sum().item())
+    torch.cuda.synchronize()
+    iv, is_ = attn.v_idx.cpu().numpy(), attn.s_idx.cpu().numpy()
+    host_m = mask_entries(iv, is_, w.N)
+    host_u = query_cover_units(iv, is_, w.N)
+    gpu_u = np.asarray(counts).reshape(w.B, w.Hq, 4)[..., :2]
+    fl = step_flops(gpu_u, per_head, w.B, w.N, w.Hq, w.d)
+    dens = per_head / (w.N * (w.N + 1) / 2.0)
+    return {"algorithmic_per_step": fl["algorithmic"], "mask_entries": int(per_head.sum()),
+            "mask_density": fl["mask_density"], "mask_density_per_head": [round(float(x), 5) for x in dens.ravel()],
+            "executed_over_algorithmic": fl["executed"] / fl["algorithmic"] if fl["algorithmic"] else None,
+            "host_checks": {"mask_entries_closed_form_equal": bool(np.array_equal(host_m, per_head)),
+                            "cover_units_equal": bool(np.array_equal(host_u, gpu_u))}}
 
 
 def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
@@ -495,15 +645,20 @@ def striped(args, w, x, rank, world):
     dev = torch.device("cuda", torch.cuda.current_device())
     to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
     W = w.world
-    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    q, k, v, do = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), to_dev(x["dout"])
     q0 = vs.striped_permute(q, W, w.stripe, only_rank=0)
-    do0 = vs.striped_permute(to_dev(x["dout"]), W, w.stripe, only_rank=0)
+    do0 = vs.striped_permute(do, W, w.stripe, only_rank=0)
     ksh, vsh = vs.striped_permute(k, W, w.stripe), vs.striped_permute(v, W, w.stripe)
     wk = vs.StripedWorker(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, W, rank=0, stripe=w.stripe, device=dev,
                           last_q=w.last_q, scale=w.scale, inner=args.inner)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # block-level striping inside the step: worker 0's Q and dO shards, every KV shard
+    permuted = [(q, q0, 0), (do, do0, 0), (k, ksh, -1), (v, vsh, -1)]
+    permute_bytes = 2.0 * sum(y.numel() * y.element_size() for _, y, _ in permuted)  # read + write
 
     def step():
+        for src, dst, r in permuted:
+            vs.striped_permute(src, W, w.stripe, only_rank=r, y=dst)
         wk.select(q, k)
         wk.build_index(q0, ksh)
         wk.forward(q0, ksh, vsh)
@@ -550,7 +705,7 @@ def striped(args, w, x, rank, world):
     dom = max(att, key=lambda kn: att[kn]["ms_total"])
     achieved = issued[dom] / (att[dom]["ms_total"] / args.steps * 1e-3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"], "traffic": _traffic(w.name, dom),
                 "peak_kind": "sustained bf16 (%s): all ring steps of the kernel per timed step" % peaks["source"]}
     ring = []
     for s in range(W):
@@ -577,6 +732,22 @@ def striped(args, w, x, rank, world):
                           "ms_max_over_mean": float(tm.max() / tm.mean())},
             "kernels": per_kernel, "step_ms_all": step_ms}
     line["layouts"] = _layout_work(wk.v_idx, wk.s_idx, w.N, W)
+    ent = np.array(line["layouts"]["striped"]["entries_per_step_worker"], np.float64)[:, 0]  # worker 0, per step
+    for r in ring:
+        r["mask_entries"] = int(ent[r["step"]])
+        r["algorithmic_flops"] = 14.0 * w.d * ent[r["step"]]
+    alg = 14.0 * w.d * float(ent.sum())
+    line["value_algorithmic"] = job_tflops(world, alg, ms)
+    line["flops"].update({"algorithmic_per_step": alg, "executed_over_algorithmic": executed / alg,
+                          "mask_density_worker": float(ent.sum()) / (w.B * w.Hq * w.N * (w.N + 1) / 2.0 / W)})
+    line["imbalance"]["algorithmic_max_over_mean"] = float(ent.max() / ent.mean())
+    if "striped_permute" in per_kernel:
+        pms = per_kernel["striped_permute"]["ms_total"] / args.steps
+        line["permute"] = {"ms_per_step": pms, "bytes_per_step": permute_bytes,
+                           "gbs": permute_bytes / (pms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                           "frac": permute_bytes / (pms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "what": "worker 0's Q and dO shards and all KV shards, 64-token stripes; bytes = "
+                                   "read + write of the permuted elements"}
     if args.all_workers:
         line["workers"] = _all_workers(args, w, q, k, v, to_dev(x["dout"]), dev)
     return line, clk.summary()
@@ -695,17 +866,9 @@ def main():
     x = synth.make_batch(w)
     line, clocks = (striped if w.world > 1 else ours)(args, w, x, rank, world)
     line["clocks"] = clocks
-    if rank == 0 and world == 1 and w.world == 1 and not args.no_cpu_baseline:
-        import oracle
-
-        p, run, R, t_est = _oracle_sample(x, w)
-        dt, _ = run(R)
-        entries = _mask_entries(p, R, w.N)
-        line["cpu_baseline"] = {"value": 10.0 * w.d * entries / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
-                                "kind": "oracle",
-                                "sample": "query head 0, last %d rows of %s: forward (O, LSE) + dQ in fp64 "
-                                          "(%d mask entries, credited 10 d FLOPs each), %.1f s; the oracle's "
-                                          "estimator on that head took %.1f s" % (R, w.name, entries, dt, t_est)}
+    if rank == 0 and world == 1 and w.world == 1 and not args.no_cpu_baseline and line["flops"].get("mask_entries"):
+        line["cpu_baseline"] = oracle_baseline(x, w, 20.0, [0, w.Hq - 1], line["flops"]["executed_per_step"],
+                                               line["flops"]["algorithmic_per_step"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

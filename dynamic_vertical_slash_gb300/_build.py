@@ -30,12 +30,37 @@ def _sources():
 
 
 def _digest() -> str:
+    """Build stamp: the sources' digest plus the compiler flags (paths taken
+    out, so that the stamp does not depend on where the tree lives)."""
+    h = hashlib.sha256(source_digest().encode())
+    h.update(" ".join(ARCH + [("<include>" if f == INC else f) for f in FLAGS]).encode())
+    return h.hexdigest()
+
+
+# The translation unit of each traced kernel name (all headers count for all).
+KERNEL_SOURCES = {
+    "fwd": "vs_attn_fwd.cu", "bwd_dq": "vs_attn_bwd.cu", "bwd_dkv_slash": "vs_attn_bwd.cu",
+    "bwd_dkv_bar": "vs_attn_bwd.cu", "bwd_prep": "vs_attn_bwd.cu", "index": "vs_index.cu",
+    "striped_permute": "vs_permute.cu", "ring_work": "vs_ringwork.cu",
+}
+
+
+def source_digest(kernel: str = None) -> str:
+    """SHA-256 of source contents and file names only (no paths, no flags):
+    every file under csrc/ and include/, or, for a traced kernel name, its
+    translation unit plus every header.  A profile of a kernel records this
+    digest; it stays valid while the digest is unchanged."""
+    files = sorted(glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INC, "*.h")))
+    if kernel is not None:
+        tu = KERNEL_SOURCES.get(kernel, "vs_estimate.cu" if kernel.startswith("est_") else None)
+        if tu is None:
+            raise KeyError(kernel)
+        files = [f for f in files if not f.endswith(".cu") or os.path.basename(f) == tu]
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INC, "*.h"))):
+    for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(ARCH + FLAGS).encode())
     return h.hexdigest()
 
 

@@ -51,3 +51,50 @@ def test_full_cover_credits_the_causal_tiles_plus_their_masked_halves():
     assert cover == N * (N + 1) // 2 + T * (128 * 127 // 2)  # each diagonal 128 x 128 tile masks 128 * 127 / 2
     assert f["fwd_executed"] == pytest.approx(4.0 * cover * d)
     assert f["fwd_executed"] > dense["fwd"]
+
+
+def _bench():
+    import bench
+
+    return bench
+
+
+def test_host_cover_units_match_the_cover_definition():
+    # the benchmark's host model of the query-major cover (used to put the CPU
+    # oracle on the GPU line's accounting) against the brute-force greedy cover
+    from test_cover import greedy_starts
+
+    rng = np.random.default_rng(5)
+    for N in (1024, 1088, 2048):
+        for k in (1, 7, 60, 300):
+            offs = np.sort(rng.choice(N, size=k, replace=False)).astype(np.int32)
+            cols = np.sort(rng.choice(N, size=min(k, 130), replace=False)).astype(np.int32)
+            starts = np.array(greedy_starts(offs, N))
+            T = (N + 127) // 128
+            want_slash = sum(int((starts <= 128 * t + 127).sum()) for t in range(T))
+            want_bar = sum(int((cols[::64] <= 128 * t + 127).sum()) for t in range(T))
+            got = _bench().query_cover_units(cols[None, None], offs[None, None], N)
+            assert got.tolist() == [[[want_slash, want_bar]]], (N, k)
+
+
+def test_host_cover_units_of_every_offset_is_the_causal_tiling():
+    N = 1024
+    got = _bench().query_cover_units(np.array([[[0]]], np.int32), np.arange(N, dtype=np.int32)[None, None], N)
+    assert got[0, 0, 0] == sum(2 * t + 2 for t in range(N // 128))
+
+
+def test_mask_entries_closed_form_against_the_oracle():
+    import oracle
+
+    rng = np.random.default_rng(9)
+    N, H, kv, ks = 512, 3, 40, 70
+    iv = np.stack([np.sort(rng.choice(N, kv, replace=False)) for _ in range(H)])[None].astype(np.int32)
+    is_ = np.stack([np.sort(rng.choice(N, ks, replace=False)) for _ in range(H)])[None].astype(np.int32)
+    is_[0, 1, -5:] = -1  # a padded (top-p) list
+    is_[0, 1, :-5] = np.sort(rng.choice(N, ks - 5, replace=False))
+    z = np.zeros((1, N, H, 1))
+    p = oracle.Problem(z, np.zeros((1, N, 1, 1)), np.zeros((1, N, 1, 1)), iv, is_, 1.0)
+    got = _bench().mask_entries(iv, is_, N)
+    for h in range(H):
+        assert got[0, h] == int(oracle.mask_dense(p, 0, h).sum())
+    assert got.sum() == oracle.mask_count(p)
