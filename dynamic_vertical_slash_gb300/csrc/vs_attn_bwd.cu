@@ -21,8 +21,16 @@
 namespace vs {
 namespace {
 
-constexpr int kIssue2Threads = 352;  // + warp 10, the second MMA-issuing warp
 constexpr int kDqThreads = 384;      // + warp 11, the dQ kernel's V loader
+// Key-major kernel: 12 warps, one besides the compute warps on each SM
+// sub-partition.  A warp that issues MMAs faster than the tensor pipe takes
+// them delays the TMEM loads and stores of the compute warps on its
+// sub-partition by about the length of its queue, and every unit waits for
+// the slowest compute warp; so the two score chains are issued by two warps
+// on different sub-partitions (warp 1: S^T, warp 11: dP^T), warp 0 issues
+// dV / dK and warp 10 loads.
+constexpr int kKvThreads = 384;
+constexpr int kKvWarpGrad = 0, kKvWarpS = 1, kKvWarpLoad = 10, kKvWarpDP = 11;
 constexpr int kDqVWarp = 11;
 constexpr int kBwdCompute = 256;  // two warps per TMEM lane quarter, each owning half the columns
 constexpr int kBwdStages = 4;
@@ -445,20 +453,6 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
       const uint64_t ob = (slash && wo + 1 >= 0 && wo + 1 < G.WG) ? __ldg(diagbits + wo + 1) : 0ull;
       const uint64_t ca = (slash && wc >= 0 && wc < G.WG) ? __ldg(colbits + wc) : 0ull;
       const uint64_t cb = (slash && wc + 1 >= 0 && wc + 1 < G.WG) ? __ldg(colbits + wc + 1) : 0ull;
-      ok = mbar_wait(&s.s_full, i & 1, ab, VS_ERR_TIMEOUT);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[64], pr[64];
-      tmem_ld32(tl + kDqColS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tl + kDqColS + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tl + kDqColDP + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-      tmem_ld32(tl + kDqColDP + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&s.s_free);
       uint64_t mask = 0;
       if (slash) {
         const int so = int(lo & 63), sc = int(m0 & 63);
@@ -482,20 +476,47 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
         if (pos[kKTile - 1] <= n_g) cnt = kKTile;
         mask = cnt == kKTile ? ~0ull : ((1ull << cnt) - 1);
       }
+      // only the 16-key chunks holding a mask entry of the warp's rows are
+      // computed (warp-uniform; on the slash units of sparse selections about
+      // half of them are empty); dS of the others is zero.  The row mask is
+      // built before the scores arrive.
+      const uint32_t occ = chunk_occupancy16(mask);
+      ok = mbar_wait(&s.s_full, i & 1, ab, VS_ERR_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[64], pr[64];
+      tmem_ld32(tl + kDqColS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tl + kDqColS + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tl + kDqColDP + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
+      tmem_ld32(tl + kDqColDP + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.s_free);
       // two keys at a time in paired fp32: P = 2^(S scale log2(e) - LSE log2(e))
       // (Lr = -LSE log2(e)), dS = P (dP - D) on the mask
       uint32_t pk[32];
       const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), lr2 = f2_pack(Lr, Lr), dr2 = f2_pack(Dr, Dr);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int col = 2 * k;
-        float t0, t1, x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sc2, lr2), t0, t1);
-        f2_unpack(f2_mul(f2_pack(ex2(t0), ex2(t1)),
-                         f2_sub(f2_pack(__uint_as_float(pr[col]), __uint_as_float(pr[col + 1])), dr2)),
-                  x0, x1);
-        // after the product: masked scores may be garbage
-        pk[k] = pack_bf16x2(((mask >> col) & 1ull) ? x0 : 0.f, ((mask >> (col + 1)) & 1ull) ? x1 : 0.f);
+      for (int cq = 0; cq < 4; ++cq) {
+        if (!((occ >> cq) & 1u)) {
+#pragma unroll
+          for (int k = 8 * cq; k < 8 * cq + 8; ++k) pk[k] = 0u;
+          continue;
+        }
+#pragma unroll
+        for (int k = 8 * cq; k < 8 * cq + 8; ++k) {
+          const int col = 2 * k;
+          float t0, t1, x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sc2, lr2), t0, t1);
+          f2_unpack(f2_mul(f2_pack(ex2(t0), ex2(t1)),
+                           f2_sub(f2_pack(__uint_as_float(pr[col]), __uint_as_float(pr[col + 1])), dr2)),
+                    x0, x1);
+          // after the product: masked scores may be garbage
+          pk[k] = pack_bf16x2(((mask >> col) & 1ull) ? x0 : 0.f, ((mask >> (col + 1)) & 1ull) ? x1 : 0.f);
+        }
       }
       if (i >= 1) ok = mbar_wait(&s.ds_done, (i - 1) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -605,8 +626,8 @@ struct KvSmem {
   int32_t head_units[kMaxGroup];  // slash: units of each head of the group
   uint64_t kv_full, k_tmem;
   uint64_t st_full[kBwdStages], st_empty[kBwdStages];
-  uint64_t s_full, s_free, p_full, mm_done;
-  uint64_t fin, teardown, teardown_g;
+  uint64_t s_full, sd_full, s_free, p_full, mm_done;
+  uint64_t fin, teardown, teardown_g, teardown_d;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -695,12 +716,14 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
       mbar_init(&s.st_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
+    mbar_init(&s.sd_full, 1);
     mbar_init(&s.s_free, kBwdCompute);
     mbar_init(&s.p_full, kBwdCompute);
     mbar_init(&s.mm_done, 1);
     mbar_init(&s.fin, 1);
     mbar_init(&s.teardown, 1);
     mbar_init(&s.teardown_g, 1);
+    mbar_init(&s.teardown_d, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -715,7 +738,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
   bool mma_issued = false;
   const int32_t* bar_keys = BAR ? av.vlist + (int64_t(b) * p.Hq + h_bar) * G.KVP + k0 : nullptr;
 
-  if (warp == 0) {
+  if (warp == kKvWarpLoad) {
     // ------------------------------------------------------------ producer
     int issued[kBwdStages];
     for (int i = 0; i < kBwdStages; ++i) issued[i] = -1;
@@ -802,33 +825,42 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
           }
         }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------- S^T / dP^T issuer
-    // Unit j once the compute warps hold S^T / dP^T of unit j - 1.
-    // The whole warp runs the loop; one elected lane issues.
+  } else if (warp == kKvWarpS || warp == kKvWarpDP) {
+    // ------------------------------------------ S^T issuer, dP^T issuer
+    // Unit j once the compute warps hold S^T / dP^T of unit j - 1: warp
+    // kKvWarpS issues S^T = K Q^T (A = K in TMEM), warp kKvWarpDP issues
+    // dP^T = V dO^T (A = V in shared memory).  Each whole warp runs its
+    // loop; one elected lane issues.
     if (run) {
+      const bool is_s = warp == kKvWarpS;
       const uint32_t idS = idesc_bf16(128, kRowTile, 0, 0);
-      bool ok = mbar_wait_warp(&s.kv_full, 0, ab, VS_ERR_TIMEOUT);
-      ok = ok && mbar_wait_warp(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT);
-      if (ok && BAR) fence_proxy_async_smem();
+      bool ok = is_s ? mbar_wait_warp(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT) : mbar_wait_warp(&s.kv_full, 0, ab, VS_ERR_TIMEOUT);
+      if (ok && BAR && !is_s) fence_proxy_async_smem();
       for (int j = 0; ok && j < U; ++j) {
         const int st = j % kBwdStages;
         if (!(ok = mbar_wait_warp(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
         if (j >= 1 && !(ok = mbar_wait_warp(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
+        if (is_s) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
-          const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-          const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
-          mma_ts_warp(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
-          mma_ss_warp(tmem + kKvColDP, dva, dg_, idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            mma_ts_warp(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
+          }
+          mma_commit_warp(&s.s_full);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            mma_ss_warp(tmem + kKvColDP, dva, dg_, idS, kk > 0);
+          }
+          mma_commit_warp(&s.sd_full);
         }
         mma_issued = true;
-        mma_commit_warp(&s.s_full);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kKvWarpGrad) {
     // ------------------------------------------------------- dV / dK issuer
     // Unit j once its P^T / dS^T are in TMEM; the unit's stage is released
     // after these MMAs (the S^T / dP^T MMAs that read it completed before the
@@ -887,7 +919,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     bool ok = true;
     for (int j = 0; run && j < U; ++j) {
       const int st = j % kBwdStages;
-      ok = mbar_wait(&s.s_full, j & 1, ab, VS_ERR_TIMEOUT) &&
+      ok = mbar_wait(&s.s_full, j & 1, ab, VS_ERR_TIMEOUT) && mbar_wait(&s.sd_full, j & 1, ab, VS_ERR_TIMEOUT) &&
            mbar_wait(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -1075,8 +1107,8 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     }
   }
   // an issuer that gave up waits (bounded) for its own MMAs in flight
-  if ((warp == 1 || warp == 10) && lane == 0 && mma_issued && s.abort_flag) {
-    uint64_t* tb = warp == 1 ? &s.teardown : &s.teardown_g;
+  if ((warp == kKvWarpS || warp == kKvWarpGrad || warp == kKvWarpDP) && lane == 0 && mma_issued && s.abort_flag) {
+    uint64_t* tb = warp == kKvWarpS ? &s.teardown : (warp == kKvWarpGrad ? &s.teardown_g : &s.teardown_d);
     mma_commit(tb);
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(tb, 0) && global_ns() - t0 < kWaitBudgetNs) {
@@ -1092,7 +1124,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
 
 // Bars hold whole columns: only the slash kernel depends on the reading.
 template <int D, bool BAR>
-__global__ void __launch_bounds__(kIssue2Threads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     vs_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
                      const BwdParams p) {
@@ -1163,12 +1195,12 @@ vs_status launch_bwd_d(const vs_shape* sh, const BwdParams& p, int grid_per_bh, 
   trace_end(st);
   // bar partials first: the slash kernel's epilogue reads them
   trace_begin("bwd_dkv_bar", st);
-  vs_bwd_kv_kernel<D, true><<<unsigned(int64_t(sh->B) * sh->Hq * grid_per_bh), kIssue2Threads, sm_kv, st>>>(
+  vs_bwd_kv_kernel<D, true><<<unsigned(int64_t(sh->B) * sh->Hq * grid_per_bh), kKvThreads, sm_kv, st>>>(
       tk128, tv128, tq64, tg64, p);
   trace_end(st);
   const int TK = (sh->Nk + kBarK - 1) / kBarK;
   trace_begin("bwd_dkv_slash", st);
-  vs_bwd_kv_kernel<D, false><<<unsigned(int64_t(sh->B) * sh->Hkv * TK), kIssue2Threads, sm_kv, st>>>(
+  vs_bwd_kv_kernel<D, false><<<unsigned(int64_t(sh->B) * sh->Hkv * TK), kKvThreads, sm_kv, st>>>(
       tk128, tv128, tq64, tg64, p);
   trace_end(st);
   const int T = (sh->Nq + kQTile - 1) / kQTile;

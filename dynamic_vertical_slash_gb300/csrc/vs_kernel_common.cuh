@@ -12,6 +12,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Bit c (c < 4) set iff some lane of the warp has a set bit among bits
+// [16 c, 16 c + 16) of its 64-bit mask: the 16-column chunks of a unit that
+// hold any mask entry of the warp's 32 rows.  Warp-collective; the result is
+// warp-uniform, so it may steer tcgen05.ld / tcgen05.st.
+__device__ __forceinline__ uint32_t chunk_occupancy16(uint64_t mask) {
+  uint32_t mine = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) mine |= ((mask >> (16 * c)) & 0xFFFFull) ? (1u << c) : 0u;
+  return __reduce_or_sync(0xffffffffu, mine);
+}
+
 __device__ __forceinline__ Geo geo_from(const ArenaHeader* h, int Hkv, int d) {
   Geo G;
   G.B = h->B;
