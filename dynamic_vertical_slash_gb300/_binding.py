@@ -80,6 +80,10 @@ def lib(build_if_missing: bool = True):
     L.vs_attn_bwd_workspace.argtypes = [_S, ctypes.c_int]
     L.vs_attn_bwd_workspace.restype = ctypes.c_size_t
     L.vs_attn_bwd.argtypes = [_S, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.vs_attn_bwd_ex.argtypes = [_S, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P,
+                                 ctypes.c_size_t, _P]
+    L.vs_ring_permute.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     L.striped_permute.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     L.vs_ring_work.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, _P, ctypes.c_int, _P, ctypes.c_int,
@@ -96,7 +100,8 @@ def lib(build_if_missing: bool = True):
     for name in ("vs_estimate", "vs_build_block_index", "vs_index_counts", "vs_attn_fwd", "vs_attn_bwd",
                  "striped_permute", "vs_check_status", "vs_selftest_wait_timeout", "vs_estimate_group",
                  "vs_estimate_topp", "vs_select_topp", "vs_build_block_index_ex", "vs_ring_work",
-                 "vs_estimate_noalloc", "vs_estimate_noalloc_status", "vs_estimate_noalloc_selftest_plant"):
+                 "vs_estimate_noalloc", "vs_estimate_noalloc_status", "vs_estimate_noalloc_selftest_plant",
+                 "vs_attn_bwd_ex", "vs_ring_permute"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -223,6 +228,14 @@ def make_stripe(world: int, q_rank: int, kv_rank: int, N_global: int, stripe: in
     return vs_stripe(world, stripe, q_rank, kv_rank, N_global)
 
 
+def make_window(q_start: int, k_start: int, N_global: int) -> vs_stripe:
+    """Query rows and keys that are contiguous windows of the global sequence
+    starting at tokens q_start / k_start (multiples of 64)."""
+    if q_start % 64 or k_start % 64:
+        raise ValueError("windows start on 64-token blocks")
+    return vs_stripe(1, 64, q_start // 64, k_start // 64, N_global)
+
+
 VS_INDEX_BLOCK_COVER = 1
 
 
@@ -266,8 +279,9 @@ def vs_attn_fwd(q, k, v, arena, scale: Optional[float] = None, o=None, lse=None,
 
 
 def vs_attn_bwd(q, k, v, o, lse, dO, arena, kv: int, scale: Optional[float] = None, dq=None, dk=None, dv=None,
-                dq_acc=None, ws=None, stream=None):
-    """Sparse backward.  Returns (dq, dk, dv) bf16."""
+                dq_acc=None, ws=None, stream=None, dkv_acc=None):
+    """Sparse backward.  Returns (dq, dk, dv) bf16.  dq_acc / dkv_acc: fp32
+    accumulate modes (dkv_acc [2, B, Nk, Hkv, d], vs_attn_bwd_ex)."""
     d = q.shape[-1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
@@ -277,9 +291,14 @@ def vs_attn_bwd(q, k, v, o, lse, dO, arena, kv: int, scale: Optional[float] = No
         raise ValueError("dO must have the layout of o")
     sh = make_shape(q, k, v, o)
     ws = _ws(lib().vs_attn_bwd_workspace(ctypes.byref(sh), kv), q.device) if ws is None else ws
-    _check(lib().vs_attn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(arena),
-                             scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dq_acc), _ptr(ws), ws.numel(),
-                             _stream(stream)), "vs_attn_bwd")
+    if dkv_acc is None:
+        _check(lib().vs_attn_bwd(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                 _ptr(arena), scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dq_acc), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "vs_attn_bwd")
+    else:
+        _check(lib().vs_attn_bwd_ex(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                    _ptr(arena), scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dq_acc), _ptr(dkv_acc),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "vs_attn_bwd_ex")
     return dq, dk, dv
 
 
@@ -297,6 +316,25 @@ def striped_permute(x, world: int, stripe: int = 64, inverse: bool = False, only
     y = torch.empty(shape, dtype=x.dtype, device=x.device) if y is None else y
     _check(lib().striped_permute(_ptr(x), _ptr(y), B, N, H, d, world, stripe, int(inverse), only_rank,
                                  _stream(stream)), "striped_permute")
+    return y
+
+
+def ring_permute(x, world: int, layout: str = "zigzag", inverse: bool = False, only_rank: int = -1, y=None,
+                 stream=None):
+    """x [B, N, H, d] -> [world, B, N/world, H, d] shards of a striped or
+    ZigZag ring (or one shard with only_rank >= 0), or back with inverse=True
+    (vs_ring_permute)."""
+    lay = {"striped": VS_LAYOUT_STRIPED, "zigzag": VS_LAYOUT_ZIGZAG}[layout]
+    if not inverse:
+        B, N, H, d = x.shape
+        shape = (B, N // world, H, d) if only_rank >= 0 else (world, B, N // world, H, d)
+    else:
+        W_, B, Nl, H, d = x.shape
+        N = Nl * W_
+        shape = (B, N, H, d)
+    y = torch.empty(shape, dtype=x.dtype, device=x.device) if y is None else y
+    _check(lib().vs_ring_permute(_ptr(x), _ptr(y), B, N, H, d, world, lay, int(inverse), only_rank, _stream(stream)),
+           "vs_ring_permute")
     return y
 
 

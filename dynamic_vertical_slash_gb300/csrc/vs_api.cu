@@ -269,10 +269,13 @@ vs_status vs_build_block_index_ex(const vs_shape* s, const int32_t* v_idx, const
   if (!v_idx || !s_idx || !arena) return VS_ERR_ARG;
   if (stripe) {
     if (stripe->world < 1 || stripe->stripe != kBlk) return VS_ERR_ARG;
-    if (stripe->q_rank < 0 || stripe->q_rank >= stripe->world || stripe->kv_rank < 0 ||
-        stripe->kv_rank >= stripe->world)
-      return VS_ERR_ARG;
-    if (s->Nq != s->Nk || stripe->N_global != int64_t(stripe->world) * s->Nq) return VS_ERR_SHAPE;
+    if (stripe->q_rank < 0 || stripe->kv_rank < 0) return VS_ERR_ARG;
+    if (s->Nq != s->Nk || stripe->N_global % kBlk || stripe->N_global > (int64_t(1) << 31) - 1) return VS_ERR_SHAPE;
+    // every local block must map inside the global sequence
+    const int64_t nbg = stripe->N_global / kBlk;
+    if (int64_t(stripe->world) * (s->Nq / kBlk - 1) + stripe->q_rank >= nbg ||
+        int64_t(stripe->world) * (s->Nk / kBlk - 1) + stripe->kv_rank >= nbg)
+      return VS_ERR_SHAPE;
   } else if (s->Nq != s->Nk) {
     return VS_ERR_SHAPE;
   }
@@ -322,18 +325,25 @@ size_t vs_attn_bwd_workspace(const vs_shape* s, int kv) {
 vs_status vs_attn_bwd(const vs_shape* s, const void* q, const void* k, const void* v, const void* o, const float* lse,
                       const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv, float* dq_acc,
                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return vs_attn_bwd_ex(s, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, nullptr, ws, ws_bytes, stream);
+}
+
+vs_status vs_attn_bwd_ex(const vs_shape* s, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk,
+                         void* dv, float* dq_acc, float* dkv_acc, void* ws, size_t ws_bytes, cudaStream_t stream) {
   vs_status rc = check_shape(s);
   if (rc != VS_OK) return rc;
   if (!q || !k || !v || !o || !lse || !dO || !arena || !dq || !dk || !dv || !ws) return VS_ERR_ARG;
   if (!(scale > 0.f)) return VS_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
-      !aligned16(dk) || !aligned16(dv) || !aligned16(arena) || (dq_acc && !aligned16(dq_acc)))
+      !aligned16(dk) || !aligned16(dv) || !aligned16(arena) || (dq_acc && !aligned16(dq_acc)) ||
+      (dkv_acc && !aligned16(dkv_acc)))
     return VS_ERR_SHAPE;
   if (ws_bytes < bwd_workspace_bytes(s, 1)) return VS_ERR_WORKSPACE;
   // The bar-partial region grows with kv, which the arena header holds on the
   // device; the kernels compare it with ws_bytes and record VS_ERR_WORKSPACE.
   Geo G{};
-  return launch_bwd(s, G, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, ws, ws_bytes, stream);
+  return launch_bwd(s, G, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, dkv_acc, ws, ws_bytes, stream);
 }
 
 vs_status vs_ring_work(int B, int H, int64_t N, const int32_t* v_idx, int kv, const int32_t* s_idx, int ks,
@@ -358,7 +368,19 @@ vs_status striped_permute(const void* x, void* y, int B, int64_t N, int H, int d
   if (only_rank < -1 || only_rank >= world) return VS_ERR_ARG;
   if (inverse && only_rank != -1) return VS_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return VS_ERR_SHAPE;
-  return launch_permute(x, y, B, N, H, d, world, stripe, inverse, only_rank, stream);
+  return launch_permute(x, y, B, N, H, d, world, VS_LAYOUT_STRIPED, inverse, only_rank, stream);
+}
+
+vs_status vs_ring_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int layout, int inverse,
+                          int only_rank, cudaStream_t stream) {
+  if (!x || !y) return VS_ERR_ARG;
+  if (layout != VS_LAYOUT_STRIPED && layout != VS_LAYOUT_ZIGZAG) return VS_ERR_ARG;
+  if (B < 1 || N < 1 || H < 1 || (d != 64 && d != 128) || world < 1) return VS_ERR_SHAPE;
+  if (N % (int64_t(world) * kBlk * (layout == VS_LAYOUT_ZIGZAG ? 2 : 1))) return VS_ERR_SHAPE;
+  if (only_rank < -1 || only_rank >= world) return VS_ERR_ARG;
+  if (inverse && only_rank != -1) return VS_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y)) return VS_ERR_SHAPE;
+  return launch_permute(x, y, B, N, H, d, world, layout, inverse, only_rank, stream);
 }
 
 }  // extern "C"

@@ -96,6 +96,7 @@ struct BwdParams {
   uint8_t* dk;
   uint8_t* dv;
   float* dq_acc;
+  float* dkv_acc;  // NULL, or fp32 [2][B][Nk][Hkv][d]: dK then dV, accumulated
   uint8_t* ws;
   size_t ws_bytes;
   int bar_nchunk;  // chunks per (b, h) in the bar kernel's grid (>= KVP / 128)
@@ -212,21 +213,10 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
   const int t = T - 1 - int(blockIdx.x) / BH;
   const int bh = int(blockIdx.x) % BH;
   const int b = bh / p.Hq, h = bh % p.Hq, hk = h / G.g;
-  const int32_t* elist = av.elist + int64_t(bh) * G.EMAX;
+  const TileWork tw = inputs_ok ? tile_work(av, G, bh, t) : TileWork{0, 0, 0};
+  const int32_t* elist = av.elist + int64_t(bh) * G.EMAX + tw.lo;  // this tile's slash units
   const int32_t* vlist = av.vlist + int64_t(bh) * G.KVP;
-  const int64_t last_row = int64_t(t) * kQTile + kQTile - 1;
-  int nslash = 0, nbar = 0;
-  if (inputs_ok) {
-    nslash = count_le(elist, __ldg(av.ecount + bh), last_row);
-    const int vc = __ldg(av.vcount + bh);
-    int lo = 0, hi = (vc + kKTile - 1) / kKTile;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(vlist + mid * kKTile) <= last_row) lo = mid + 1;
-      else hi = mid;
-    }
-    nbar = lo;
-  }
+  const int nslash = tw.nslash, nbar = tw.nbar;
   const int U = nslash + nbar;
   const int P = (U + 1) / 2;  // pairs
   if (threadIdx.x == 0) {
@@ -458,7 +448,7 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
         const int so = int(lo & 63), sc = int(m0 & 63);
         const uint64_t x = so ? ((oa >> so) | (ob << (64 - so))) : oa;
         const uint64_t cw = sc ? ((ca >> sc) | (cb << (64 - sc))) : ca;
-        const uint64_t keep = ~cw & (c < 0 ? ((~0ull) << (-c)) : ~0ull);
+        const uint64_t keep = ~cw & (c < 0 ? ((~0ull) << (-c)) : ~0ull) & low_bits(int64_t(G.Nk) - c);
         if (block_cover) {
           // keys below the split are in the first key block (diagonal bit 1),
           // the rest in the next one (bit 0); causal keys only
@@ -624,6 +614,7 @@ struct KvSmem {
   int32_t unit_head[kBwdStages];
   int32_t unit_row[kBwdStages];
   int32_t head_units[kMaxGroup];  // slash: units of each head of the group
+  int32_t head_lo[kMaxGroup];     // slash: the head's first f-list entry of this key tile
   uint64_t kv_full, k_tmem;
   uint64_t st_full[kBwdStages], st_empty[kBwdStages];
   uint64_t s_full, sd_full, s_free, p_full, mm_done;
@@ -674,10 +665,17 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     k0 = int64_t(int(blockIdx.x) / BHK) * kBarK;
     if (cta_ok) {
       w.heads = G.g;
+      // the entries f whose rows [k0 + f, + 64) meet [0, Nq)
       for (int hh = 0; hh < G.g; ++hh) {
         const int bh = b * p.Hq + hk * G.g + hh;
-        const int c = count_le(av.flist + int64_t(bh) * G.EMAX, __ldg(av.fcount + bh), int64_t(p.Nq) - 1 - k0);
-        if (threadIdx.x == 0) s.head_units[hh] = c;
+        const int32_t* fl = av.flist + int64_t(bh) * G.EMAX;
+        const int nf = __ldg(av.fcount + bh);
+        const int lo = count_le(fl, nf, -k0 - 64);
+        const int c = count_le(fl, nf, int64_t(p.Nq) - 1 - k0) - lo;
+        if (threadIdx.x == 0) {
+          s.head_units[hh] = c;
+          s.head_lo[hh] = lo;
+        }
         w.n_units += c;
       }
     }
@@ -693,7 +691,9 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     if (cta_ok) {
       const int vc = __ldg(av.vcount + bh);
       if (chunk * kBarK < vc && chunk * kBarK < G.KVP) {
-        const int64_t rs = (int64_t(__ldg(av.vlist + int64_t(bh) * G.KVP + chunk * kBarK)) / kBlk) * kBlk;
+        const int64_t rs =
+            first_causal_row_block(G.world, G.q_rank, kpos_g(G, __ldg(av.vlist + int64_t(bh) * G.KVP + chunk * kBarK))) *
+            kBlk;
         const int64_t tiles = (p.Nq - rs + kRowTile - 1) / kRowTile;
         const int64_t first = int64_t(split) * kBarSplitTiles;
         if (first < tiles) {
@@ -769,7 +769,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
           ++cur_h;
         }
         h_nxt = hk * G.g + cur_h;
-        f_nxt = __ldg(av.flist + (int64_t(b) * G.Hq + h_nxt) * G.EMAX + cur_j);
+        f_nxt = __ldg(av.flist + (int64_t(b) * G.Hq + h_nxt) * G.EMAX + s.head_lo[cur_h] + cur_j);
         ++cur_j;
       };
       if (!BAR && U > 0) next_unit();
@@ -792,7 +792,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
         const float* ddr = ddg + (int64_t(b) * p.Hq + h) * p.Nq;
         for (int i = lane; i < kRowTile; i += 32) {
           const int64_t n = r0 + i;
-          const bool in = n < p.Nq;
+          const bool in = n >= 0 && n < p.Nq;
           cp_async_4(smem_u32(&s.l2[st][i]), in ? l2r + n : l2r, in ? 4u : 0u);
           cp_async_4(smem_u32(&s.dd[st][i]), in ? ddr + n : ddr, in ? 4u : 0u);
         }
@@ -1061,7 +1061,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
             const int64_t rank =
                 __ldg(av.vlocpre + bh * G.WL + (kl >> 6)) + __popcll(vw & ((1ull << (kl & 63)) - 1));
             const int64_t first = __ldg(av.vlist + bh * G.KVP + (rank / kBarK) * kBarK);
-            const int64_t rs = (first / kBlk) * kBlk;
+            const int64_t rs = first_causal_row_block(G.world, G.q_rank, kpos_g(G, first)) * kBlk;
             const int64_t tiles = (p.Nq - rs + kRowTile - 1) / kRowTile;
             const int nsplit = int((tiles + kBarSplitTiles - 1) / kBarSplitTiles);
             for (int sp = 0; sp < nsplit; ++sp) {
@@ -1079,6 +1079,34 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
                 yv[i + 2] += c4.z;
                 yv[i + 3] += c4.w;
               }
+            }
+          }
+          if (p.dkv_acc) {
+            // accumulate mode: acc += this call's dK / dV; the outputs are the sums
+            float* ak = p.dkv_acc + ((int64_t(b) * p.Nk + kl) * p.Hkv + hk) * D + cc;
+            float* avv = ak + int64_t(p.B) * p.Nk * p.Hkv * D;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              float4 a4 = *reinterpret_cast<float4*>(ak + i);
+              float4 c4 = *reinterpret_cast<float4*>(avv + i);
+              a4.x += yk[i];
+              a4.y += yk[i + 1];
+              a4.z += yk[i + 2];
+              a4.w += yk[i + 3];
+              c4.x += yv[i];
+              c4.y += yv[i + 1];
+              c4.z += yv[i + 2];
+              c4.w += yv[i + 3];
+              *reinterpret_cast<float4*>(ak + i) = a4;
+              *reinterpret_cast<float4*>(avv + i) = c4;
+              yk[i] = a4.x;
+              yk[i + 1] = a4.y;
+              yk[i + 2] = a4.z;
+              yk[i + 3] = a4.w;
+              yv[i] = c4.x;
+              yv[i + 1] = c4.y;
+              yv[i + 2] = c4.z;
+              yv[i + 3] = c4.w;
             }
           }
           uint4 k0w, k1w, v0w, v1w;
@@ -1134,7 +1162,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
 BwdParams make_params(const vs_shape* sh, const void* q, const void* k, const void* v, const void* o,
                       const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
-                      float* dq_acc, void* ws, size_t ws_bytes) {
+                      float* dq_acc, float* dkv_acc, void* ws, size_t ws_bytes) {
   BwdParams p;
   p.arena = arena;
   p.q = static_cast<const uint8_t*>(q);
@@ -1160,6 +1188,7 @@ BwdParams make_params(const vs_shape* sh, const void* q, const void* k, const vo
   p.dk = static_cast<uint8_t*>(dk);
   p.dv = static_cast<uint8_t*>(dv);
   p.dq_acc = dq_acc;
+  p.dkv_acc = dkv_acc;
   p.ws = static_cast<uint8_t*>(ws);
   p.ws_bytes = ws_bytes;
   p.err = static_cast<int*>(ws);
@@ -1219,8 +1248,8 @@ size_t bwd_workspace_bytes(const vs_shape* s, int kv) {
 
 vs_status launch_bwd(const vs_shape* s, const Geo&, const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
-                     float* dq_acc, void* ws, size_t ws_bytes, cudaStream_t st) {
-  BwdParams p = make_params(s, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, ws, ws_bytes);
+                     float* dq_acc, float* dkv_acc, void* ws, size_t ws_bytes, cudaStream_t st) {
+  BwdParams p = make_params(s, q, k, v, o, lse, dO, arena, scale, dq, dk, dv, dq_acc, dkv_acc, ws, ws_bytes);
   // Grid of the bar kernel: (KVP / 128) chunks x splits per (b, h).  KVP
   // lives in the arena header on the device; the largest value the
   // workspace can hold bounds it, and CTAs beyond the real count exit.

@@ -297,22 +297,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
   // a workspace already holding an error makes the call skip its work
   const bool arena_ok = (av.hdr->status == 0) && (av.hdr->magic == kArenaMagic) &&
                         (*reinterpret_cast<volatile int*>(p.err) == 0);
-  const int32_t* elist = av.elist + int64_t(bh) * G.EMAX;
+  const TileWork tw = arena_ok ? tile_work(av, G, bh, t) : TileWork{0, 0, 0};
+  const int32_t* elist = av.elist + int64_t(bh) * G.EMAX + tw.lo;  // this tile's slash units
   const int32_t* vlist = av.vlist + int64_t(bh) * G.KVP;
-  const int64_t last_row = int64_t(t) * kQTile + kQTile - 1;
-  int nslash = 0, nbar = 0;
-  if (arena_ok) {
-    nslash = count_le(elist, __ldg(av.ecount + bh), last_row);
-    const int vc = __ldg(av.vcount + bh);
-    // chunks whose first column can precede a row of the tile
-    int lo = 0, hi = (vc + kKTile - 1) / kKTile;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(vlist + mid * kKTile) <= last_row) lo = mid + 1;
-      else hi = mid;
-    }
-    nbar = lo;
-  }
+  const int nslash = tw.nslash, nbar = tw.nbar;
   const int U = nslash + nbar;
   const int P = (U + 1) / 2;  // pairs
   // a pair holds a gathered (bar) half
@@ -521,7 +509,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
             if (j == 6) {
               const int shc = int(m0[hh] & 63);
               const uint64_t colw = shc ? ((wv >> shc) | (c1 << (64 - shc))) : wv;
-              const uint64_t keep = ~colw & ((cc[hh] < 0) ? ((~0ull) << (-cc[hh])) : ~0ull);
+              // keys that exist: c + k in [0, Nk)
+              const uint64_t keep =
+                  ~colw & ((cc[hh] < 0) ? ((~0ull) << (-cc[hh])) : ~0ull) & low_bits(int64_t(G.Nk) - cc[hh]);
               if (block_cover) {
                 // keys below the split lie in the first key block (diagonal
                 // D2 + 1, bit 1), the rest in the next (D2, bit 0)

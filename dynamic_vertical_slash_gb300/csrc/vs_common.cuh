@@ -86,12 +86,32 @@ struct Geo {
   int64_t N_global;
 };
 
-// Global position of a local query row / key under 64-token striping.
+// Local 64-token block j of the query (key) tensor is global block
+// world * j + q_rank (kv_rank): the striped shards of a ring (ranks below
+// world) and contiguous windows of the sequence (world 1, rank = the window's
+// first block, e.g. the two chunks of a ZigZag worker) are both of this form.
+// Global position of a local query row / key:
 __host__ __device__ __forceinline__ int64_t qpos_g(const Geo& G, int64_t l) {
   return (int64_t(G.world) * (l >> 6) + G.q_rank) * kBlk + (l & 63);
 }
 __host__ __device__ __forceinline__ int64_t kpos_g(const Geo& G, int64_t l) {
   return (int64_t(G.world) * (l >> 6) + G.kv_rank) * kBlk + (l & 63);
+}
+
+// The first local 64-row block whose rows can attend global key position
+// m_g: the smallest rb >= 0 with qpos_g(64 rb + 63) >= m_g.
+__host__ __device__ __forceinline__ int64_t first_causal_row_block(int world, int q_rank, int64_t m_g) {
+  const int64_t num = (m_g >> 6) - q_rank;
+  return num <= 0 ? 0 : (num + world - 1) / world;
+}
+
+// Local index of global key position x in a key window of Nk tokens, or -1
+// when the window does not hold it.
+__host__ __device__ __forceinline__ int64_t local_key_of(int world, int kv_rank, int64_t Nk, int64_t x) {
+  const int64_t rb = (x >> 6) - kv_rank;
+  if (rb < 0 || rb % world) return -1;
+  const int64_t lb = rb / world;
+  return lb < Nk / kBlk ? lb * kBlk + (x & 63) : -1;
 }
 
 // Bits [lo, lo + 64) of a bitmap of `nwords` words; positions outside the
@@ -113,6 +133,35 @@ __device__ __forceinline__ int count_le(const int32_t* list, int n, int64_t x) {
     else hi = mid;
   }
   return lo;
+}
+
+// Query-major work of 128-row tile t of head bh: its slash units are
+// elist[lo, lo + nslash) (the entries e <= 128 t + 127 whose 64 keys
+// c = 128 t + 64 - e start before Nk), its bar chunks the first nbar chunks
+// of the vertical list (those whose first column precedes, on global
+// positions, the tile's last row).
+struct TileWork {
+  int lo, nslash, nbar;
+};
+__device__ __forceinline__ TileWork tile_work(const ArenaView& av, const Geo& G, int64_t bh, int t) {
+  TileWork w;
+  const int32_t* elist = av.elist + bh * G.EMAX;
+  const int ne = __ldg(av.ecount + bh);
+  const int64_t last_row = int64_t(t) * kQTile + kQTile - 1;
+  w.lo = count_le(elist, ne, last_row - 63 - G.Nk);
+  w.nslash = count_le(elist, ne, last_row) - w.lo;
+  const int32_t* vlist = av.vlist + bh * G.KVP;
+  const int vc = __ldg(av.vcount + bh);
+  int lo = 0, hi = (vc + kKTile - 1) / kKTile;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (first_causal_row_block(G.world, G.q_rank, kpos_g(G, __ldg(vlist + mid * kKTile))) <= 2 * int64_t(t) + 1)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  w.nbar = lo;
+  return w;
 }
 
 }  // namespace vs

@@ -10,11 +10,14 @@
 //                      and a key tile of 128 keys at k0 reads rows
 //                      [k0 + u, k0 + u + 63]; together the intervals cover
 //                      every entry with a selected offset exactly once.
-//                      Striped, the cover is block-aligned: elist holds
-//                      64 (D + 1) for each active local block diagonal D of a
-//                      (2 row blocks x 1 key block) tile, flist 64 D for each
-//                      active D of a (1 row block x 2 key blocks) tile;
-//   vlist              selected columns that live in this key shard, as local
+//                      Striped (local block j = global block world j + rank,
+//                      see vs_common.cuh), the cover is block-aligned: elist
+//                      holds 64 (D + 1) for each active local block diagonal
+//                      D of a (2 row blocks x 1 key block) tile, flist 64 D for
+//                      each active D of a (1 row block x 2 key blocks) tile;
+//                      D may be negative when the key window lies before the
+//                      query window on the sequence;
+//   vlist              selected columns that live in this key window, as local
 //                      key indices, ascending, padded with -1;
 //   vlocbits/vlocpre   the same as a bitmap with word prefix counts;
 //   counts             work units of the four attention passes;
@@ -114,11 +117,8 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     const int x = iv[i];
     if (x < 0) continue;
     atomicOr(reinterpret_cast<unsigned long long*>(colbits + (x >> 6)), 1ull << (x & 63));
-    const int blk = x >> 6;
-    if (blk % W == H.kv_rank) {
-      const int64_t l = int64_t(blk / W) * kBlk + (x & 63);
-      atomicOr(reinterpret_cast<unsigned long long*>(vloc + (l >> 6)), 1ull << (l & 63));
-    }
+    const int64_t l = local_key_of(W, H.kv_rank, H.Nk, x);
+    if (l >= 0) atomicOr(reinterpret_cast<unsigned long long*>(vloc + (l >> 6)), 1ull << (l & 63));
   }
   __threadfence_block();
   __syncthreads();
@@ -205,13 +205,16 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
       }
       nf = ne;
     } else {
+      // local block diagonals from the key window's end to the query
+      // window's end (negative D: keys after the rows locally, which the
+      // window offsets may still make causal)
       const int64_t rel = int64_t(H.q_rank) - H.kv_rank;
-      const int nb = H.Nq / kBlk;
-      for (int D = -1; D <= nb && ne < H.EMAX; ++D)
+      const int nb = H.Nq / kBlk, nbk = H.Nk / kBlk;
+      for (int D = -nbk; D <= nb && ne < H.EMAX; ++D)
         if (block_diag_active(offbits, H.WG, int64_t(W) * D + rel) ||
             block_diag_active(offbits, H.WG, int64_t(W) * D + W + rel))
           elist[ne++] = 64 * D + 64;
-      for (int D = 0; D <= nb && nf < H.EMAX; ++D)
+      for (int D = -nbk; D <= nb && nf < H.EMAX; ++D)
         if (block_diag_active(offbits, H.WG, int64_t(W) * D + rel) ||
             block_diag_active(offbits, H.WG, int64_t(W) * D - W + rel))
           flist[nf++] = 64 * D;
@@ -222,23 +225,35 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     const int64_t T = (H.Nq + kQTile - 1) / kQTile;
     const int64_t TK = (H.Nk + kBarK - 1) / kBarK;
     int64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    // the same unit ranges as the kernels: query tile t takes the entries
+    // e in [128 t + 64 - Nk + 1, 128 t + 127] (its 64 keys start before Nk)
+    // and the bar chunks whose first column precedes its last row; key tile
+    // tau the entries f with rows [128 tau + f, + 64) meeting [0, Nq); a
+    // key-major bar chunk runs from the first row block that can attend its
+    // first column
+    auto ceil_div = [](int64_t a, int64_t b) { return a >= 0 ? (a + b - 1) / b : -((-a) / b); };
+    auto floor_div = [](int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
     for (int i = 0; i < ne; ++i) {
       const int64_t e = elist[i];
-      const int64_t tmin = e > 127 ? (e - 127 + kQTile - 1) / kQTile : 0;
-      c0 += max(int64_t(0), T - tmin);
+      const int64_t tmin = max(int64_t(0), ceil_div(e - 127, kQTile));
+      const int64_t tmax = min(T - 1, floor_div(e - 65 + H.Nk, kQTile));
+      c0 += max(int64_t(0), tmax - tmin + 1);
     }
     for (int c = 0; c * kKTile < nv; ++c) {
-      const int64_t f = vlist[c * kKTile];
-      const int64_t tmin = f > 127 ? (f - 127 + kQTile - 1) / kQTile : 0;
+      const int64_t m_g = (int64_t(W) * (vlist[c * kKTile] >> 6) + H.kv_rank) * kBlk + (vlist[c * kKTile] & 63);
+      const int64_t tmin = first_causal_row_block(W, H.q_rank, m_g) / 2;
       c1 += max(int64_t(0), T - tmin);
     }
     for (int i = 0; i < nf; ++i) {
       const int64_t f = flist[i];
-      if (f <= H.Nq - 1) c2 += min(TK, (H.Nq - 1 - f) / kBarK + 1);
+      const int64_t tmin = max(int64_t(0), ceil_div(-f - 63, kBarK));
+      const int64_t tmax = min(TK - 1, floor_div(H.Nq - 1 - f, kBarK));
+      c2 += max(int64_t(0), tmax - tmin + 1);
     }
     for (int c = 0; c * kBarK < nv; ++c) {
-      const int64_t rs = (vlist[c * kBarK] / kBlk) * kBlk;
-      c3 += (H.Nq - rs + kRowTile - 1) / kRowTile;
+      const int64_t m_g = (int64_t(W) * (vlist[c * kBarK] >> 6) + H.kv_rank) * kBlk + (vlist[c * kBarK] & 63);
+      const int64_t rs = first_causal_row_block(W, H.q_rank, m_g) * kBlk;
+      c3 += max(int64_t(0), (H.Nq - rs + kRowTile - 1) / kRowTile);
     }
     counts[0] = c0;
     counts[1] = c1;
@@ -266,7 +281,7 @@ size_t index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* stripe, A
   h.N_global = stripe ? stripe->N_global : s->Nq;
   h.WG = int32_t(h.N_global / 64 + 4);
   h.WL = s->Nk / 64 + 2;
-  h.EMAX = (s->Nq > s->Nk ? s->Nq : s->Nk) / 64 + 8;
+  h.EMAX = (s->Nq + s->Nk) / 64 + 8;
   h.KVP = (kv + kBarK - 1) / kBarK * kBarK;
   h.sheared = stripe ? 0 : 1;
   const int64_t BH = int64_t(s->B) * s->Hq;

@@ -31,7 +31,7 @@ vs_status launch_fwd(const vs_shape* s, const Geo& G, const void* q, const void*
                      cudaStream_t st);
 vs_status launch_bwd(const vs_shape* s, const Geo& G, const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
-                     float* dq_acc, void* ws, size_t ws_bytes, cudaStream_t st);
+                     float* dq_acc, float* dkv_acc, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t bwd_workspace_bytes(const vs_shape* s, int kv);
 vs_status launch_estimate(const vs_shape* s, const void* q, const void* k, int last_q, int kv, int ks, float scale,
                           int32_t* v_idx, int32_t* s_idx, float* v_score, float* s_score, void* ws, int shared,
@@ -50,7 +50,7 @@ vs_status launch_ring_work(int B, int H, int64_t N, const int32_t* v_idx, int kv
 vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                        const vs_stripe* stripe, int flags, void* arena, size_t arena_bytes, cudaStream_t st);
 size_t index_bytes(const vs_shape* s, int kv, int ks, const vs_stripe* stripe, ArenaHeader* hdr_out);
-vs_status launch_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int stripe,
+vs_status launch_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int layout,
                          int inverse, int only_rank, cudaStream_t st);
 
 }  // namespace vs

@@ -97,6 +97,7 @@ __device__ __forceinline__ uint64_t slash_col_mask(const Geo& G, const uint64_t*
   uint64_t m = bits64(offbits, base, G.WG);
   const int64_t rows = int64_t(G.Nq) - r0;
   if (rows < 64) m &= (rows <= 0) ? 0ull : ((1ull << rows) - 1);
+  if (r0 < 0) m &= ~low_bits(-r0);  // rows before the query window
   return m;
 }
 
@@ -110,6 +111,7 @@ __device__ __forceinline__ uint64_t block_col_mask(const Geo& G, const uint64_t*
   const uint64_t lo = low_bits(64 - (n0 & 63));
   uint64_t mask = ((a & 1ull) ? lo : 0ull) | ((a & 2ull) ? ~lo : 0ull);
   mask &= ~low_bits(m - n0);  // causal rows
+  if (r0 < 0) mask &= ~low_bits(-r0);  // rows before the query window
   return mask & low_bits(int64_t(G.Nq) - r0);
 }
 

@@ -277,3 +277,147 @@ class StripedWorker:
     def counts(self) -> np.ndarray:
         """Work units per ring step: [world, B, Hq, 4]."""
         return np.stack([B_.vs_index_counts(a) for a in self.arenas])
+
+
+class ZigZagWorker:
+    """One worker's side of a ZigZag ring on one GPU (the layout MTraining
+    contrasts with striping, section 2 and Figure 1): the sequence of N_global
+    tokens is cut into 2 * world chunks of C = N_global / (2 world) tokens and
+    worker ``rank`` holds chunks rank and 2 world - 1 - rank (its shard is the
+    two chunks in that order, see ring_permute).  At ring step s it attends to
+    the KV shard of source (rank - s) mod world.
+
+    A step is made of chunk pairs (a query chunk of this worker, a key chunk
+    of the source) with the query chunk not before the key chunk on the
+    sequence (a pair in the other order has no causal entry).  Each pair is a
+    windowed problem (make_window) with its own index built on global
+    positions: the forward merges the pair's (O, LSE) into its query chunk's
+    running result, the backward accumulates dQ per query chunk and dK / dV
+    per key chunk of the source (vs_attn_bwd_ex), with the merged LSE.  Each
+    step's forward and backward are timed with CUDA events.  The KV shards of
+    every source sit in this GPU's memory; the selection is made once, on the
+    global sequence, by ``select``.
+    """
+
+    def __init__(self, B: int, N_global: int, Hq: int, Hkv: int, d: int, kv: int, ks: int, world: int,
+                 rank: int = 0, device="cuda", last_q: int = 64, scale: Optional[float] = None):
+        if N_global % (2 * world * 64):
+            raise ValueError("N_global must be a multiple of 128 * world")
+        self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N_global, Hq, Hkv, d, kv, ks
+        self.world, self.rank, self.last_q = world, rank, last_q
+        self.scale = 1.0 / math.sqrt(d) if scale is None else scale
+        dev = torch.device(device)
+        C = N_global // (2 * world)
+        self.C = C
+        L = B_.lib()
+        import ctypes
+        qg = torch.empty(B, N_global, Hq, d, dtype=torch.bfloat16, device="meta")
+        kg = torch.empty(B, N_global, Hkv, d, dtype=torch.bfloat16, device="meta")
+        shg = B_.make_shape(qg, kg)
+        self.v_idx = torch.empty(B, Hq, kv, dtype=torch.int32, device=dev)
+        self.s_idx = torch.empty(B, Hq, ks, dtype=torch.int32, device=dev)
+        self.v_score = torch.empty(B, Hq, N_global, dtype=torch.float32, device=dev)
+        self.s_score = torch.empty(B, Hq, N_global, dtype=torch.float32, device=dev)
+        self.ws_est = torch.zeros(max(256, L.vs_estimate_workspace(ctypes.byref(shg), last_q)), dtype=torch.uint8,
+                                  device=dev)
+        qc = torch.empty(B, C, Hq, d, dtype=torch.bfloat16, device=dev)
+        kc = torch.empty(B, C, Hkv, d, dtype=torch.bfloat16, device=dev)
+        shc = B_.make_shape(qc, kc)
+        # per ring step: the chunk pairs (query chunk i, key chunk j, window)
+        self.pairs = []
+        for s in range(world):
+            src = self.source(s)
+            qch, kch = self.chunks(rank), self.chunks(src)
+            ps = []
+            for i in range(2):
+                for j in range(2):
+                    if qch[i] >= kch[j]:
+                        ps.append((i, j, B_.make_window(qch[i] * C, kch[j] * C, N_global)))
+            self.pairs.append(ps)
+        self.arenas = [[torch.empty(L.vs_block_index_bytes(ctypes.byref(shc), kv, ks, ctypes.byref(st)),
+                                    dtype=torch.uint8, device=dev) for (_, _, st) in ps] for ps in self.pairs]
+        self.o = torch.empty(B, 2 * C, Hq, d, dtype=torch.bfloat16, device=dev)
+        self.lse = [torch.empty(B, Hq, C, dtype=torch.float32, device=dev) for _ in range(2)]  # per query chunk
+        # fp32 accumulators are contiguous [B][C][Hq][d] per query chunk
+        self.o_acc = [torch.empty(B, C, Hq, d, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.ws_fwd = torch.zeros(256, dtype=torch.uint8, device=dev)
+        self.dq = torch.empty_like(self.o)
+        self.dq_acc = [torch.empty(B, C, Hq, d, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.dk = torch.empty(world, B, 2 * C, Hkv, d, dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty_like(self.dk)
+        self.dkv_acc = [torch.empty(2, B, C, Hkv, d, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.ws_bwd = torch.zeros(L.vs_attn_bwd_workspace(ctypes.byref(shc), kv), dtype=torch.uint8, device=dev)
+        self.events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(world)]
+        self._qkv = None
+
+    def chunks(self, r: int):
+        """The two chunks (of C tokens, in sequence order) worker r holds."""
+        return (r, 2 * self.world - 1 - r)
+
+    def source(self, s: int) -> int:
+        return ring_source(self.rank, s, self.world)
+
+    def _rows(self, t, i):
+        return t[:, i * self.C:(i + 1) * self.C]
+
+    def select(self, q_global, k_global, stream=None):
+        B_.vs_estimate(q_global, k_global, self.kv, self.ks, self.scale, self.last_q, self.v_idx, self.s_idx,
+                       self.v_score, self.s_score, self.ws_est, stream)
+        return self.v_idx, self.s_idx
+
+    def build_index(self, q_shard, k_shards, stream=None):
+        """One index per chunk pair of every ring step, on global positions."""
+        for s in range(self.world):
+            src = self.source(s)
+            for (i, j, st), arena in zip(self.pairs[s], self.arenas[s]):
+                B_.vs_build_block_index(self._rows(q_shard, i), self._rows(k_shards[src], j), self.v_idx, self.s_idx,
+                                        st, arena, stream)
+
+    def forward(self, q_shard, k_shards, v_shards, stream=None):
+        for l, a in zip(self.lse, self.o_acc):
+            l.fill_(-math.inf)
+            a.zero_()
+        for s in range(self.world):
+            src = self.source(s)
+            self.events[s][0].record(stream)
+            for (i, j, _), arena in zip(self.pairs[s], self.arenas[s]):
+                B_.vs_attn_fwd(self._rows(q_shard, i), self._rows(k_shards[src], j), self._rows(v_shards[src], j),
+                               arena, self.scale, self._rows(self.o, i), self.lse[i], self.o_acc[i],
+                               self.ws_fwd, stream)
+            self.events[s][1].record(stream)
+        self._qkv = (q_shard, k_shards, v_shards)
+        return self.o, self.lse
+
+    def backward(self, dO_shard, stream=None):
+        q, ks_, vs_ = self._qkv
+        for a in self.dq_acc:
+            a.zero_()
+        for s in range(self.world):
+            src = self.source(s)
+            self.events[s][2].record(stream)
+            for a in self.dkv_acc:
+                a.zero_()
+            self.dk[src].zero_()  # key chunks with no causal pair keep zero gradients
+            self.dv[src].zero_()
+            for (i, j, _), arena in zip(self.pairs[s], self.arenas[s]):
+                B_.vs_attn_bwd(self._rows(q, i), self._rows(ks_[src], j), self._rows(vs_[src], j),
+                               self._rows(self.o, i), self.lse[i], self._rows(dO_shard, i), arena, self.kv,
+                               self.scale, self._rows(self.dq, i), self._rows(self.dk[src], j),
+                               self._rows(self.dv[src], j), self.dq_acc[i], self.ws_bwd, stream,
+                               dkv_acc=self.dkv_acc[j])
+            self.events[s][3].record(stream)
+        return self.dq, self.dk, self.dv
+
+    def step_times(self):
+        return [(e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3])) for e in self.events]
+
+    def check(self):
+        for buf in [self.ws_est, self.ws_fwd, self.ws_bwd] + [a for ar in self.arenas for a in ar]:
+            code = B_.vs_check_status(buf)
+            if code:
+                raise B_.VSError(code, "device status")
+
+    def counts(self) -> np.ndarray:
+        """Work units per ring step, summed over the step's chunk pairs: [world, B, Hq, 4]."""
+        return np.stack([sum((B_.vs_index_counts(a) for a in ar), np.zeros((self.B, self.Hq, 4), np.int64))
+                         for ar in self.arenas])

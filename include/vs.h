@@ -66,11 +66,18 @@ typedef struct {
   int64_t sq[3], sk[3], sv[3], so[3];
 } vs_shape;
 
-/* Striped-shard description (Balanced Sparse Ring Attention, section 4.2 (ii)
- * and Algorithm 2).  Global 64-token block j lives on worker j mod world at
- * local block j / world.  The local queries belong to worker q_rank and the
- * local keys to worker kv_rank; N_global = world * Nq.  Pass NULL for an
- * unstriped problem (world 1, identity positions). */
+/* Where the local tokens sit on the global sequence of N_global tokens: local
+ * 64-token block j of the query tensor is global block world * j + q_rank,
+ * that of the key tensor world * j + kv_rank.  Two uses:
+ *   - a striped shard pair (Balanced Sparse Ring Attention, section 4.2 (ii)
+ *     and Algorithm 2): global block j lives on worker j mod world at local
+ *     block j / world; the queries belong to worker q_rank, the keys to worker
+ *     kv_rank (ranks below world), N_global = world * Nq;
+ *   - a pair of contiguous windows (world 1, rank = the window's first
+ *     global block), e.g. one chunk of a ZigZag worker's queries against one
+ *     chunk of another worker's keys (section 2, Figure 1).
+ * Every local block must lie inside the global sequence.  Pass NULL for an
+ * unstriped problem (identity positions). */
 typedef struct {
   int world, stripe, q_rank, kv_rank;
   int64_t N_global;
@@ -305,6 +312,16 @@ vs_status vs_attn_bwd(const vs_shape* shape, const void* q, const void* k, const
                       const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk, void* dv,
                       float* dq_acc, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* vs_attn_bwd with an accumulate mode for dK and dV as well (a key window
+ * that receives the gradients of several query windows, as the two chunks of
+ * a ZigZag worker do at one ring step):
+ *   dkv_acc  NULL, or fp32 [2][B][Nk][Hkv][d] contiguous (dK, then dV):
+ *            dkv_acc += this call's dK / dV; dk = bf16(dK sum), dv likewise.
+ * Other arguments as for vs_attn_bwd. */
+vs_status vs_attn_bwd_ex(const vs_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, const void* arena, float scale, void* dq, void* dk,
+                         void* dv, float* dq_acc, float* dkv_acc, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * striped_permute -- block-level striping (section 4.2 (ii), 64-token
  * stripes): global block j of x [B, N, H, d] goes to shard j mod world at
@@ -313,6 +330,15 @@ vs_status vs_attn_bwd(const vs_shape* shape, const void* q, const void* k, const
  * (y then holds one shard [B, N/world, H, d]); -1 writes all.
  * ------------------------------------------------------------------------- */
 vs_status striped_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int stripe, int inverse,
+                          int only_rank, cudaStream_t stream);
+
+/* vs_ring_permute -- striped_permute for either ring layout (layout as for
+ * vs_ring_work below): VS_LAYOUT_STRIPED (64-token stripes, N a multiple of
+ * 64 world) or VS_LAYOUT_ZIGZAG (section 2, Figure 1: 2 world chunks of
+ * N / (2 world) tokens, worker r holds chunks r and 2 world - 1 - r in that
+ * order; N a multiple of 128 world).  Shard layout, inverse and only_rank as
+ * for striped_permute. */
+vs_status vs_ring_permute(const void* x, void* y, int B, int64_t N, int H, int d, int world, int layout, int inverse,
                           int only_rank, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------

@@ -19,8 +19,9 @@ directly:
 * ``merge`` -- ``merge_out_and_lse`` of Algorithm 2.
 * ``stripe_positions`` / ``striped_permute`` -- 64-token block-level
   striping (section 4.2 (ii)).
-* ``ring_owners`` / ``ring_work`` -- per (query worker, key worker) mask
-  entries under the striped and ZigZag ring layouts (sections 2, 3.3, 4.2).
+* ``ring_owners`` / ``ring_positions`` / ``ring_permute`` / ``ring_work`` --
+  the striped and ZigZag ring layouts and the mask entries per (query
+  worker, key worker) under them (sections 2, 3.3, 4.2).
 
 Inputs are converted to float64 (bf16 values widen exactly); all arithmetic is fp64.
 """
@@ -348,6 +349,25 @@ def ring_owners(N: int, W: int, layout: str, stripe: int = 64) -> np.ndarray:
         c = n // (N // (2 * W))
         return np.where(c < W, c, 2 * W - 1 - c)
     raise ValueError(layout)
+
+
+def ring_positions(N: int, W: int, r: int, layout: str, stripe: int = 64) -> np.ndarray:
+    """Global positions of worker r's tokens in its shard's (local) order.
+    striped: stripe_positions; zigzag: chunk r then chunk 2W - 1 - r of the
+    2W chunks of N / (2W) tokens (section 2, Figure 1)."""
+    if layout == "striped":
+        return stripe_positions(N, W, stripe, r)
+    if layout == "zigzag":
+        C = N // (2 * W)
+        first, second = r, 2 * W - 1 - r
+        return np.concatenate([np.arange(first * C, (first + 1) * C), np.arange(second * C, (second + 1) * C)])
+    raise ValueError(layout)
+
+
+def ring_permute(x: np.ndarray, W: int, layout: str) -> np.ndarray:
+    """x [B, N, H, d] -> [W, B, N/W, H, d]: shard r holds x at ring_positions(r)."""
+    N = x.shape[1]
+    return np.stack([x[:, ring_positions(N, W, r, layout)] for r in range(W)])
 
 
 def ring_work(iv, is_, N: int, W: int, layout: str, stripe: int = 64) -> np.ndarray:

@@ -62,3 +62,34 @@ def test_single_worker_is_everything():
         got = oracle.ring_work(iv, is_, 512, 1, layout)
         p = oracle.Problem(np.zeros((1, 512, 2, 1)), np.zeros((1, 512, 1, 1)), np.zeros((1, 512, 1, 1)), iv, is_, 1.0)
         assert got.shape == (1, 1) and got[0, 0] == oracle.mask_count(p)
+
+
+def test_zigzag_positions_hand_worked():
+    # N = 16, W = 2: four chunks of 4 tokens; worker 0 holds chunks 0 and 3,
+    # worker 1 chunks 1 and 2 (the mirrored pairs of the folded sequence)
+    assert oracle.ring_positions(16, 2, 0, "zigzag").tolist() == [0, 1, 2, 3, 12, 13, 14, 15]
+    assert oracle.ring_positions(16, 2, 1, "zigzag").tolist() == [4, 5, 6, 7, 8, 9, 10, 11]
+
+
+@pytest.mark.parametrize("layout", ["striped", "zigzag"])
+def test_ring_positions_are_the_owned_tokens_in_sequence_order(layout):
+    N, W = 2048, 4
+    own = oracle.ring_owners(N, W, layout)
+    seen = np.zeros(N, np.int64)
+    for r in range(W):
+        pos = oracle.ring_positions(N, W, r, layout)
+        np.testing.assert_array_equal(pos, np.nonzero(own == r)[0])  # ascending: local order = sequence order
+        seen[pos] += 1
+    assert np.all(seen == 1)
+
+
+def test_ring_permute_moves_each_token_to_its_owner():
+    N, W = 1024, 4
+    x = np.arange(N, dtype=np.int64).reshape(1, N, 1, 1)
+    for layout in ("striped", "zigzag"):
+        y = oracle.ring_permute(x, W, layout)
+        assert y.shape == (W, 1, N // W, 1, 1)
+        own = oracle.ring_owners(N, W, layout)
+        for r in range(W):
+            assert np.all(own[y[r, 0, :, 0, 0]] == r)
+    np.testing.assert_array_equal(oracle.ring_permute(x, W, "striped"), oracle.striped_permute(x, W, 64))
