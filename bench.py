@@ -732,6 +732,8 @@ def striped(args, w, x, rank, world):
                           "ms_max_over_mean": float(tm.max() / tm.mean())},
             "kernels": per_kernel, "step_ms_all": step_ms}
     line["layouts"] = _layout_work(wk.v_idx, wk.s_idx, w.N, W)
+    if args.layouts:
+        line["layouts_measured"] = _layouts_measured(args, w, q, k, v, do, dev, wk.v_idx, wk.s_idx)
     ent = np.array(line["layouts"]["striped"]["entries_per_step_worker"], np.float64)[:, 0]  # worker 0, per step
     for r in ring:
         r["mask_entries"] = int(ent[r["step"]])
@@ -773,6 +775,76 @@ def _layout_work(iv, is_, N, W):
                        "worker_level_mean": float(wl.mean()), "worker_level_max": float(wl.max()),
                        "step_level_mean": float(sl.mean()), "step_level_max": float(sl.max()),
                        "worker_totals_max_over_mean": float(tot.max() / tot.mean())}
+    return out
+
+
+def _ring_times(wk, q_r, ksh, vsh, do_r, reps: int):
+    """Per ring step of one worker: device time (forward + backward, mean over
+    `reps` timed repetitions after one warm-up) and executed FLOPs."""
+    import torch
+
+    from dynamic_vertical_slash_gb300.pipeline import flop_counts
+
+    wk.build_index(q_r, ksh)
+    wk.forward(q_r, ksh, vsh)
+    wk.backward(do_r)
+    torch.cuda.synchronize()
+    wk.check()
+    W = len(wk.events)
+    ms = np.zeros(W)
+    for _ in range(reps):
+        wk.forward(q_r, ksh, vsh)
+        wk.backward(do_r)
+        torch.cuda.synchronize()
+        ms += np.array([a + b for a, b in wk.step_times()])
+    wk.check()
+    fl = [flop_counts(c, wk.d) for c in wk.counts()]
+    return ms / reps, np.array([f["fwd_executed"] + f["bwd_executed"] for f in fl])
+
+
+def _layouts_measured(args, w, q, k, v, do, dev, iv, is_):
+    """The ring run on the GPU under both layouts of the same global
+    selection: striped (64-token stripes) and ZigZag (2W chunks, worker r
+    holds chunks r and 2W - 1 - r; each step is its causal chunk pairs).  For
+    worker 0 (every worker with --all-workers): per ring step the device time
+    and executed FLOPs; step-level imbalance = max / mean over a worker's
+    steps; worker-level imbalance = max / mean over the workers at one step
+    (mean and max over the steps); the imbalance of the workers' total times."""
+    import torch
+
+    import dynamic_vertical_slash_gb300 as vs
+
+    W = w.world
+    workers = range(W) if args.all_workers else [0]
+    out = {}
+    for layout in ("striped", "zigzag"):
+        ksh, vsh = vs.ring_permute(k, W, layout), vs.ring_permute(v, W, layout)
+        per = []
+        for r in workers:
+            q_r = vs.ring_permute(q, W, layout, only_rank=r)
+            do_r = vs.ring_permute(do, W, layout, only_rank=r)
+            cls = vs.StripedWorker if layout == "striped" else vs.ZigZagWorker
+            wk = cls(w.B, w.N, w.Hq, w.Hkv, w.d, w.kv, w.ks, W, rank=r, device=dev, last_q=w.last_q, scale=w.scale)
+            wk.v_idx.copy_(iv)
+            wk.s_idx.copy_(is_)
+            ms, fl = _ring_times(wk, q_r, ksh, vsh, do_r, args.layout_reps)
+            per.append({"worker": r, "src": [wk.source(s) for s in range(W)], "ms": ms.tolist(),
+                        "executed_flops": fl.tolist(), "step_imbalance_ms": float(ms.max() / ms.mean()),
+                        "step_imbalance_flops": float(fl.max() / fl.mean())})
+            del wk, q_r, do_r
+            torch.cuda.synchronize()
+        rec = {"per_worker": per}
+        if len(per) > 1:
+            st = np.array([[p["ms"][s] for p in per] for s in range(W)])  # [step][worker]
+            wl = st.max(1) / st.mean(1)
+            tot = st.sum(0)
+            rec.update({"worker_level_ms_mean": float(wl.mean()), "worker_level_ms_max": float(wl.max()),
+                        "worker_totals_ms_max_over_mean": float(tot.max() / tot.mean())})
+        out[layout] = rec
+        del ksh, vsh
+        torch.cuda.synchronize()
+    out["how"] = ("flat ring src = rank - s mod W; one warm-up, then the mean of %d timed repetitions per step "
+                  "(CUDA events around each step's forward and backward)" % args.layout_reps)
     return out
 
 
@@ -836,6 +908,9 @@ def main():
     ap.add_argument("--ps", type=float, default=0.9, help="top-p variant: slash mass fraction")
     ap.add_argument("--kv-cap", type=int, default=4096, help="top-p variant: vertical list capacity")
     ap.add_argument("--ks-cap", type=int, default=8192, help="top-p variant: slash list capacity")
+    ap.add_argument("--layouts", action="store_true",
+                    help="striped workloads: also time the ring under both layouts (striped and ZigZag)")
+    ap.add_argument("--layout-reps", type=int, default=2, help="timed repetitions per layout and worker")
     ap.add_argument("--all-workers", action="store_true",
                     help="striped workloads: also run every worker's ring and report the imbalance across workers")
     args = ap.parse_args()
