@@ -7,11 +7,15 @@ outputs the fp64 oracle computes one at a time:
   replay rule (the oracle's top-k on the GPU's own scores), and every index
   on which the two selections differ inside the tolerance band of the k-th
   score;
-* attention, on the oracle's own selection: O, LSE and dQ of sampled query
-  rows (first, last and random rows of every head) and dK / dV of sampled
-  keys (the last keys of the sequence, vertical ones among them, and a key in
-  the middle that only slash lines reach), with O / dQ / dK / dV relative L2
-  <= 1e-2 over the sample and LSE absolute <= 1e-3.
+* attention, on the oracle's own selection: O, LSE and dQ of 64 sampled
+  query rows of every head (the first rows, which only the vertical bars
+  reach, rows of the heaviest last query tile, and random rows) and dK / dV
+  of 32 sampled keys of every KV head (the last keys of the sequence,
+  vertical ones among them, keys in the middle that only slash lines reach,
+  and vertical keys past the middle whose attending rows cross several of the
+  key-major bar kernel's split pieces), with O / dQ / dK / dV relative L2
+  <= 1e-2 over the sample (per-head values printed; each head's own sample
+  below 3e-2) and LSE absolute <= 1e-3.
 
 The oracle widens only the rows it needs: the query / dO rows of the sampled
 rows and of every row that reaches a sampled key.
@@ -67,9 +71,12 @@ def _check_selection(v_gpu, s_gpu, iv_gpu, is_gpu, v_ref, s_ref, iv_ref, is_ref,
                     assert np.all(np.abs(sc_r[b, h][diff] - kth) <= 2 * SCORE_TOL * top), (b, h, diff)
 
 
-def _sample_rows(N, rng, count=6):
-    mid = rng.choice(np.arange(2, N - 2), count - 4, replace=False)
-    return np.unique(np.concatenate([[0, 1, N - 2, N - 1], mid]))
+def _sample_rows(N, rng, count=64):
+    """The first rows, rows of the last 128-row tile (the heaviest), random rows."""
+    first = np.arange(8)
+    last = np.sort(rng.choice(np.arange(N - 128, N), 16, replace=False))
+    mid = rng.choice(np.arange(8, N - 128), count - 24, replace=False)
+    return np.unique(np.concatenate([first, last, mid]))
 
 
 def _rows_reaching(m, ivh, ish, N):
@@ -83,25 +90,50 @@ def _rows_reaching(m, ivh, ish, N):
 
 
 def _sample_keys(b, hk, g, iv, is_, N, rng, dense):
-    """Keys of KV head hk: the last ones (vertical ones preferred) and one
-    mid-sequence key no vertical list holds."""
+    """32 keys of KV head hk: the last ones (vertical ones preferred); unless
+    the mask is dense, also mid-sequence keys no vertical list holds (only
+    slash lines reach them) and vertical keys in [5N/8, 3N/4), whose
+    attending rows span more than one 16384-row piece of the key-major bar
+    kernel."""
     tail = 128 if dense else 2048
     ivh = iv[b, hk * g:(hk + 1) * g]
     vert = sorted({int(m) for m in ivh.ravel() if m >= N - tail})
-    keys = vert[-2:] + sorted(rng.choice(np.arange(N - tail, N), 3, replace=False).tolist())
+    keys = set(vert[-8:])
     if not dense:
         held = set(ivh.ravel().tolist())
-        for m in rng.permutation(np.arange(N // 4, 3 * N // 4)):
-            if int(m) not in held:
-                keys.append(int(m))
-                break
-    return sorted(set(keys))
+        slash_only = [int(m) for m in rng.permutation(np.arange(N // 4, 3 * N // 4))[:64] if int(m) not in held]
+        keys |= set(slash_only[:4])
+        mid_vert = sorted({int(m) for m in ivh.ravel() if 5 * N // 8 <= m < 3 * N // 4})
+        if mid_vert:
+            keys |= set(rng.choice(mid_vert, min(4, len(mid_vert)), replace=False).tolist())
+    for m in rng.permutation(np.arange(N - tail, N)):
+        if len(keys) >= 32:
+            break
+        keys.add(int(m))
+    return sorted(keys)
+
+
+HEAD_TOL = 3e-2  # a single head's small sample: only a gross per-head fault exceeds it
+
+
+def _per_head(name, got, ref, heads):
+    """Relative L2 of every head's sample (heads: the head of each sample
+    row), reported with the worst; the tolerance of the comparison is the
+    whole sample's (asserted by the caller), a head's own sample only has to
+    stay below HEAD_TOL."""
+    errs = {int(h): rel_l2(got[heads == h], ref[heads == h]) for h in np.unique(heads)}
+    worst = max(errs, key=errs.get)
+    print("%s: worst head %d rel-L2 %.3g, sample rel-L2 %.3g; per head %s" % (
+        name, worst, errs[worst], rel_l2(got, ref), {h: round(e, 4) for h, e in errs.items()}))
+    assert errs[worst] <= HEAD_TOL, (name, errs)
 
 
 def _compare_rows(p, rows_bhn, o_gpu, lse_gpu, dq_gpu):
     o_ref, lse_ref, dq_ref = oracle.rows(p, rows_bhn)
     assert rel_l2(o_gpu, o_ref) <= TOL
     assert rel_l2(dq_gpu, dq_ref) <= TOL
+    _per_head("O", o_gpu, o_ref, rows_bhn[:, 1])
+    _per_head("dQ", dq_gpu, dq_ref, rows_bhn[:, 1])
     fin = np.isfinite(lse_ref)
     np.testing.assert_array_equal(np.isfinite(lse_gpu), fin)
     assert np.max(np.abs(lse_gpu[fin] - lse_ref[fin]), initial=0.0) <= 1e-3
@@ -152,8 +184,12 @@ def test_fullsize_sampled_parity(vs, name):
                       np.stack([dq_h[b, n, h] for h in range(Hq) for n in rows]))
         kb = np.array([(0, hk, m) for hk in range(Hkv) for m in keys[hk]], np.int32)
         dk_ref, dv_ref = oracle.keys(p, kb)
-        assert rel_l2(np.stack([dk_h[b, m, hk] for hk in range(Hkv) for m in keys[hk]]), dk_ref) <= TOL
-        assert rel_l2(np.stack([dv_h[b, m, hk] for hk in range(Hkv) for m in keys[hk]]), dv_ref) <= TOL
+        got_k = np.stack([dk_h[b, m, hk] for hk in range(Hkv) for m in keys[hk]])
+        got_v = np.stack([dv_h[b, m, hk] for hk in range(Hkv) for m in keys[hk]])
+        assert rel_l2(got_k, dk_ref) <= TOL
+        assert rel_l2(got_v, dv_ref) <= TOL
+        _per_head("dK", got_k, dk_ref, kb[:, 1])
+        _per_head("dV", got_v, dv_ref, kb[:, 1])
 
 
 def test_fullsize_striped_ring_sampled_parity(vs):
