@@ -236,13 +236,14 @@ def make_window(q_start: int, k_start: int, N_global: int) -> vs_stripe:
     return vs_stripe(1, 64, q_start // 64, k_start // 64, N_global)
 
 
-VS_INDEX_BLOCK_COVER = 1
+VS_INDEX_BLOCK_COVER, VS_INDEX_PACK_GQA = 1, 2
 
 
 def vs_build_block_index(q, k, v_idx, s_idx, stripe: Optional[vs_stripe] = None, arena=None, stream=None,
-                         block_cover: bool = False):
+                         block_cover: bool = False, pack_gqa: bool = False):
     """Sparse index arena (uint8 device tensor) for the shape of q / k;
-    block_cover selects the block-cover reading of the slashes."""
+    block_cover selects the block-cover reading of the slashes, pack_gqa the
+    head-packed query-major tiles (lists equal within each KV group)."""
     sh = make_shape(q, k)
     kv, ks = v_idx.shape[-1], s_idx.shape[-1]
     sp = ctypes.byref(stripe) if stripe is not None else None
@@ -251,7 +252,8 @@ def vs_build_block_index(q, k, v_idx, s_idx, stripe: Optional[vs_stripe] = None,
         raise VSError(VS_ERR_SHAPE, "vs_block_index_bytes")
     arena = torch.empty(need, dtype=torch.uint8, device=q.device) if arena is None else arena
     _check(lib().vs_build_block_index_ex(ctypes.byref(sh), _ptr(v_idx), _ptr(s_idx), kv, ks, sp,
-                                         VS_INDEX_BLOCK_COVER if block_cover else 0, _ptr(arena), arena.numel(),
+                                         (VS_INDEX_BLOCK_COVER if block_cover else 0) |
+                                         (VS_INDEX_PACK_GQA if pack_gqa else 0), _ptr(arena), arena.numel(),
                                          _stream(stream)), "vs_build_block_index")
     return arena
 

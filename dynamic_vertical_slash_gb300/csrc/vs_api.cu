@@ -57,12 +57,12 @@ static EncodeTiledFn encode_fn() {
 }
 
 vs_status make_tmap_bshd(CUtensorMap* m, const void* base, int B, int N, int H, int d, const int64_t s[3],
-                         int box_rows) {
+                         int box_rows, int box_heads) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return VS_ERR_CUDA;
   cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(N), cuuint64_t(B)};
   cuuint64_t strides[3] = {cuuint64_t(s[2]) * 2, cuuint64_t(s[1]) * 2, cuuint64_t(s[0]) * 2};
-  cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
+  cuuint32_t box[4] = {64, cuuint32_t(box_heads), cuuint32_t(box_rows), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -263,9 +263,16 @@ vs_status vs_build_block_index(const vs_shape* s, const int32_t* v_idx, const in
 vs_status vs_build_block_index_ex(const vs_shape* s, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                                   const vs_stripe* stripe, int flags, void* arena, size_t arena_bytes,
                                   cudaStream_t stream) {
-  if (flags & ~int(VS_INDEX_BLOCK_COVER)) return VS_ERR_ARG;
+  if (flags & ~int(VS_INDEX_BLOCK_COVER | VS_INDEX_PACK_GQA)) return VS_ERR_ARG;
   vs_status rc = check_shape(s);
   if (rc != VS_OK) return rc;
+  if (flags & VS_INDEX_PACK_GQA) {
+    // one head-packed tile is 128 / g tokens of the g heads of a KV group
+    // (unstriped, exact token mask)
+    const int g = s->Hq / s->Hkv;
+    if (stripe || (flags & VS_INDEX_BLOCK_COVER)) return VS_ERR_ARG;
+    if (g < 2 || kQTile % g) return VS_ERR_SHAPE;
+  }
   if (!v_idx || !s_idx || !arena) return VS_ERR_ARG;
   if (stripe) {
     if (stripe->world < 1 || stripe->stripe != kBlk) return VS_ERR_ARG;

@@ -208,12 +208,29 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
   const ArenaView av = arena_view(p.arena);
   const bool inputs_ok = bwd_inputs_ok(p, av, D);
   const Geo G = geo_from(av.hdr, p.Hkv, D);
-  const int T = (p.Nq + kQTile - 1) / kQTile;
-  const int BH = p.B * p.Hq;
-  const int t = T - 1 - int(blockIdx.x) / BH;
-  const int bh = int(blockIdx.x) % BH;
-  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / G.g;
-  const TileWork tw = inputs_ok ? tile_work(av, G, bh, t) : TileWork{0, 0, 0};
+  // A tile is R = 128 rows of one query head, or with GQA packing (gp = g)
+  // R = 128 / g tokens of the g heads of a KV group: tile row r is token
+  // r / gp of head h + r % gp.  Heavy (late) tiles first.
+  const int gp = av.hdr->pack;
+  const int R = gp ? kQTile / gp : kQTile;
+  int t, b, h, hk;
+  if (gp) {
+    const int BHK = p.B * p.Hkv, TS = (p.Nq + R - 1) / R;
+    if (int(blockIdx.x) >= TS * BHK) return;  // the grid is sized for unpacked tiles
+    t = TS - 1 - int(blockIdx.x) / BHK;
+    b = int(blockIdx.x) % BHK / p.Hkv;
+    hk = int(blockIdx.x) % p.Hkv;
+    h = hk * gp;
+  } else {
+    const int T = (p.Nq + kQTile - 1) / kQTile, BH = p.B * p.Hq;
+    t = T - 1 - int(blockIdx.x) / BH;
+    b = int(blockIdx.x) % BH / p.Hq;
+    h = int(blockIdx.x) % p.Hq;
+    hk = h / G.g;
+  }
+  const int bh = b * p.Hq + h;  // the lists of this head serve the whole tile
+  const int64_t r0 = int64_t(t) * R;
+  const TileWork tw = inputs_ok ? tile_work(av, G, bh, r0, R) : TileWork{0, 0, 0};
   const int32_t* elist = av.elist + int64_t(bh) * G.EMAX + tw.lo;  // this tile's slash units
   const int32_t* vlist = av.vlist + int64_t(bh) * G.KVP;
   const int nslash = tw.nslash, nbar = tw.nbar;
@@ -278,7 +295,7 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int u = 2 * i + hf;
-        c[hf] = u >= U ? kUnitNone : (u < nslash ? int64_t(t) * kQTile + 64 - e_cur[hf] : kUnitBar);
+        c[hf] = u >= U ? kUnitNone : (u < nslash ? r0 + R - 64 - e_cur[hf] : kUnitBar);
         if (!isv) {
           if (c[hf] == kUnitBar) {
             const int32_t* keys = vlist + (u - nslash) * kKTile;
@@ -380,8 +397,9 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
+    const int hrow = gp ? h + r % gp : h;  // the row's query head
     const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
-    const int64_t n_loc = int64_t(t) * kQTile + r;
+    const int64_t n_loc = r0 + (gp ? r / gp : r);
     const bool row_ok = n_loc < p.Nq && inputs_ok;
     const int64_t n_g = qpos_g(G, n_loc);
     const uint64_t* offbits = av.offbits + int64_t(bh) * G.WG;
@@ -393,8 +411,9 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
     float Lr = 0.f, Dr = 0.f;
     if (row_ok) {
       const BwdLayout L = bwd_layout_dev(av.hdr, D);
-      Lr = reinterpret_cast<const float*>(p.ws + L.off_l2)[int64_t(bh) * p.Nq + n_loc];
-      Dr = reinterpret_cast<const float*>(p.ws + L.off_d)[int64_t(bh) * p.Nq + n_loc];
+      const int64_t bhr = int64_t(b) * p.Hq + hrow;
+      Lr = reinterpret_cast<const float*>(p.ws + L.off_l2)[bhr * p.Nq + n_loc];
+      Dr = reinterpret_cast<const float*>(p.ws + L.off_d)[bhr * p.Nq + n_loc];
     }
     // Q row r and dO row r, d columns [half D/2, (half + 1) D/2), into TMEM
     // as bf16 pairs
@@ -402,8 +421,8 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
     for (int which = 0; which < 2; ++which) {
       uint32_t w[D / 4];
       const uint8_t* src =
-          which ? p.dO + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(h) * p.so[2]) * 2 + half * D
-                : p.q + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(h) * p.sq[2]) * 2 + half * D;
+          which ? p.dO + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(hrow) * p.so[2]) * 2 + half * D
+                : p.q + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(hrow) * p.sq[2]) * 2 + half * D;
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
         const uint4 x = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
@@ -528,8 +547,8 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
       // TMEM reads are warp-collective: every lane loads, valid rows store;
       // each half writes its half of the d columns
       const bool store = n_loc < p.Nq;
-      uint8_t* drow = p.dq + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(h) * p.sq[2]) * 2;
-      float* acc = (p.dq_acc && store) ? p.dq_acc + ((int64_t(b) * p.Nq + n_loc) * p.Hq + h) * D : nullptr;
+      uint8_t* drow = p.dq + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(hrow) * p.sq[2]) * 2;
+      float* acc = (p.dq_acc && store) ? p.dq_acc + ((int64_t(b) * p.Nq + n_loc) * p.Hq + hrow) * D : nullptr;
 #pragma unroll 1
       for (int cc = (D / 2) * half; cc < (D / 2) * (half + 1); cc += 16) {
         uint32_t gv[16];

@@ -62,7 +62,8 @@ struct MaskRec {
   int64_t kg[kKTile];
 };
 
-// Row r's mask (bit k: key k of the unit) from its unit's record.
+// The mask of the row whose token is the tile's token r (bit k: key k of the
+// unit), from its unit's record.
 template <bool BLOCK>
 __device__ __forceinline__ uint64_t rec_row_mask(const MaskRec& rc, int kind, int r, int64_t ng) {
   if (kind == 1) {
@@ -278,8 +279,8 @@ __device__ __noinline__ RowRef fwd_rebase_second(uint32_t tl, uint32_t colS, uin
 // The kernel body, compiled once per mask reading (BLOCK: block-cover
 // slashes) so that neither reading carries the other's code.
 template <int D, bool BLOCK>
-__device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                         const FwdParams& p) {
+__device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorMap& tmQp, const CUtensorMap& tmK,
+                                         const CUtensorMap& tmV, const FwdParams& p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -287,17 +288,34 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
 
   const ArenaView av = arena_view(p.arena);
   const Geo G = geo_from(av.hdr, p.Hkv, D);
-  const int T = (p.Nq + kQTile - 1) / kQTile;
-  const int BH = p.B * p.Hq;
-  const int t = T - 1 - int(blockIdx.x) / BH;  // heavy (late) tiles first
-  const int bh = int(blockIdx.x) % BH;
-  const int b = bh / p.Hq, h = bh % p.Hq, hk = h / G.g;
+  // A tile is R = 128 rows of one query head, or with GQA packing (gp = g)
+  // R = 128 / g tokens of the g heads of a KV group: tile row r is token
+  // r / gp of head h + r % gp.  Heavy (late) tiles first.
+  const int gp = av.hdr->pack;
+  const int R = gp ? kQTile / gp : kQTile;
+  int t, b, h, hk;
+  if (gp) {
+    const int BHK = p.B * p.Hkv, TS = (p.Nq + R - 1) / R;
+    if (int(blockIdx.x) >= TS * BHK) return;  // the grid is sized for unpacked tiles
+    t = TS - 1 - int(blockIdx.x) / BHK;
+    b = int(blockIdx.x) % BHK / p.Hkv;
+    hk = int(blockIdx.x) % p.Hkv;
+    h = hk * gp;
+  } else {
+    const int T = (p.Nq + kQTile - 1) / kQTile, BH = p.B * p.Hq;
+    t = T - 1 - int(blockIdx.x) / BH;
+    b = int(blockIdx.x) % BH / p.Hq;
+    h = int(blockIdx.x) % p.Hq;
+    hk = h / G.g;
+  }
+  const int bh = b * p.Hq + h;  // the lists of this head serve the whole tile
+  const int64_t r0 = int64_t(t) * R;
 
   // Work list of this tile.
   // a workspace already holding an error makes the call skip its work
   const bool arena_ok = (av.hdr->status == 0) && (av.hdr->magic == kArenaMagic) &&
                         (*reinterpret_cast<volatile int*>(p.err) == 0);
-  const TileWork tw = arena_ok ? tile_work(av, G, bh, t) : TileWork{0, 0, 0};
+  const TileWork tw = arena_ok ? tile_work(av, G, bh, r0, R) : TileWork{0, 0, 0};
   const int32_t* elist = av.elist + int64_t(bh) * G.EMAX + tw.lo;  // this tile's slash units
   const int32_t* vlist = av.vlist + int64_t(bh) * G.KVP;
   const int nslash = tw.nslash, nbar = tw.nbar;
@@ -354,7 +372,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
           prefetch_tmap(&tmQ);
           prefetch_tmap(&tmK);
           mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
-          for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], &tmQ, &s.q_full, 64 * hf, h, t * kQTile, b);
+          // packed: a box of R tokens x g heads, rows in (token, head) order
+          for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], gp ? &tmQp : &tmQ, &s.q_full, 64 * hf, h, int(r0), b);
         } else {
           prefetch_tmap(&tmV);
         }
@@ -383,7 +402,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
             const int j = 32 * e_win + lane;
             e_pref = j < nslash ? __ldg(elist + j) : 0;
           }
-          key0[hh] = t * kQTile + 64 - __shfl_sync(0xffffffffu, e_pref, u & 31);
+          key0[hh] = int(r0) + R - 64 - __shfl_sync(0xffffffffu, e_pref, u & 31);
         }
         if (cb >= kFwdSlots && !(ok = mbar_wait(&s.slot_empty[sl], ((cb / kFwdSlots) - 1) & 1, ab, VS_ERR_TIMEOUT)))
           return;
@@ -456,11 +475,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
             const int j = 32 * e_win + lane;
             e_pref = j < nslash ? __ldg(elist + j) : 0;
           }
-          cc[hh] = int64_t(t) * kQTile + 64 - __shfl_sync(0xffffffffu, e_pref, u & 31);
+          cc[hh] = r0 + R - 64 - __shfl_sync(0xffffffffu, e_pref, u & 31);
         }
         m0[hh] = (cc[hh] >= 0) ? kpos_g(G, cc[hh]) : cc[hh];  // c < 0 only without striping
-        L0a[hh] = qpos_g(G, int64_t(t) * kQTile) - m0[hh] - 63;
-        L0b[hh] = qpos_g(G, int64_t(t) * kQTile + 64) - m0[hh] - 63;
+        L0a[hh] = qpos_g(G, r0) - m0[hh] - 63;
+        L0b[hh] = qpos_g(G, r0 + 64) - m0[hh] - 63;
       }
       // issue every load of the pair
       uint64_t wv = 0;
@@ -485,7 +504,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
           // the unit's two key blocks (bits D2 = I - J - 1 and D2 + 1)
           const int u = (lane - 16) >> 1, rb = lane & 1;
           if (kind[u] == 1) {
-            const int64_t D2 = (qpos_g(G, int64_t(t) * kQTile + 64 * rb) >> 6) - (m0[u] >> 6) - 1;
+            const int64_t D2 = (qpos_g(G, r0 + 64 * rb) >> 6) - (m0[u] >> 6) - 1;
             wv = bits64(bdbits_p, D2, G.WG) & 3ull;
           }
         }
@@ -585,8 +604,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     const int grp = (warp - 2) >> 2;         // softmax group: pairs i with i & 1 == grp
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;       // query row within the tile
+    const int ti = gp ? r / gp : r;          // its token within the tile
+    const int hrow = gp ? h + r % gp : h;    // and its query head
     const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
-    const int64_t n_loc = int64_t(t) * kQTile + r;
+    const int64_t n_loc = r0 + ti;
     const bool row_ok = n_loc < p.Nq;
     const uint32_t colO = kColO + 128 * grp, colS = kColS + 128 * grp;
     float m_run = -INFINITY, l_run = 0.f;
@@ -603,8 +624,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
       }
       const MaskRec& rc0 = s.rec[ri][0];
       const MaskRec& rc1 = s.rec[ri][1];
-      const uint64_t mask0 = row_ok ? rec_row_mask<BLOCK>(rc0, rc0.kind, r, n_g) : 0ull;
-      const uint64_t mask1 = row_ok ? rec_row_mask<BLOCK>(rc1, rc1.kind, r, n_g) : 0ull;
+      const uint64_t mask0 = row_ok ? rec_row_mask<BLOCK>(rc0, rc0.kind, ti, n_g) : 0ull;
+      const uint64_t mask1 = row_ok ? rec_row_mask<BLOCK>(rc1, rc1.kind, ti, n_g) : 0ull;
       mbar_arrive(&s.rec_empty[ri]);
       ok = mbar_wait(&s.s_full[grp], (i >> 1) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -696,12 +717,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
       const bool empty = !(l_run2 > 0.f);
       const float inv = empty ? 0.f : 1.f / l_run2;
       const float lse_step = empty ? -INFINITY : (mm + __log2f(l_run2)) * kLn2;
-      float* lse_p = p.lse + (int64_t(b) * p.Hq + h) * p.Nq + n_loc;
-      uint8_t* orow = p.o + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(h) * p.so[2]) * 2;
+      float* lse_p = p.lse + (int64_t(b) * p.Hq + hrow) * p.Nq + n_loc;
+      uint8_t* orow = p.o + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(hrow) * p.so[2]) * 2;
       float wa = 0.f, wb = 1.f, lse_new = lse_step;
       float* acc = nullptr;
       if (p.o_acc && row_ok) {
-        acc = p.o_acc + ((int64_t(b) * p.Nq + n_loc) * p.Hq + h) * D;
+        acc = p.o_acc + ((int64_t(b) * p.Nq + n_loc) * p.Hq + hrow) * D;
         const float lse_old = *lse_p;
         if (lse_old == -INFINITY && empty) {
           lse_new = -INFINITY;
@@ -783,18 +804,26 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmQ, tmK, tmV, p);
-  else fwd_body<D, false>(tmQ, tmK, tmV, p);
+    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQp,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const FwdParams p) {
+  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmQ, tmQp, tmK, tmV, p);
+  else fwd_body<D, false>(tmQ, tmQp, tmK, tmV, p);
 }
 
 template <int D>
 vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const void* v, const void* arena,
                        float scale, void* o, float* lse, float* o_acc, int* err, cudaStream_t st) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tqp, tk, tv;
   vs_status rc;
   if ((rc = make_tmap_bshd(&tq, q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile)) != VS_OK) return rc;
+  // GQA-packed tiles (when the arena asks for them): 128 / g tokens x g heads
+  const int g = sh->Hq / sh->Hkv;
+  if (g >= 2 && kQTile % g == 0) {
+    if ((rc = make_tmap_bshd(&tqp, q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile / g, g)) != VS_OK) return rc;
+  } else {
+    tqp = tq;
+  }
   if ((rc = make_tmap_bshd(&tk, k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kKTile)) != VS_OK) return rc;
   if ((rc = make_tmap_bshd(&tv, v, sh->B, sh->Nk, sh->Hkv, D, sh->sv, kKTile)) != VS_OK) return rc;
   FwdParams p;
@@ -821,7 +850,7 @@ vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const v
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   const dim3 grid(unsigned(T) * sh->B * sh->Hq);
   trace_begin("fwd", st);
-  vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, p);
+  vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tqp, tk, tv, p);
   trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;

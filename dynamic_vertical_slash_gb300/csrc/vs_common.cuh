@@ -35,6 +35,7 @@ struct ArenaHeader {
   int64_t off_vlist, off_vcount, off_vlocbits, off_vlocpre, off_counts;
   int64_t total_bytes;
   int64_t off_bdbits;
+  int32_t pack;  // GQA packing: g (query-major tiles of 128 / g tokens x g heads), 0 = one head per tile
 };
 static_assert(sizeof(ArenaHeader) <= 256, "arena header exceeds 256 bytes");
 
@@ -135,30 +136,30 @@ __device__ __forceinline__ int count_le(const int32_t* list, int n, int64_t x) {
   return lo;
 }
 
-// Query-major work of 128-row tile t of head bh: its slash units are
-// elist[lo, lo + nslash) (the entries e <= 128 t + 127 whose 64 keys
-// c = 128 t + 64 - e start before Nk), its bar chunks the first nbar chunks
-// of the vertical list (those whose first column precedes, on global
+// Query-major work of the tile of R tokens starting at local row r0 (R = 128,
+// or 128 / g with GQA packing) of head bh: its slash units are
+// elist[lo, lo + nslash) (the entries e <= r0 + R - 1 whose 64 keys
+// c = r0 + R - 64 - e start before Nk), its bar chunks the first nbar chunks
+// of the vertical list (those whose first column is not after, on global
 // positions, the tile's last row).
 struct TileWork {
   int lo, nslash, nbar;
 };
-__device__ __forceinline__ TileWork tile_work(const ArenaView& av, const Geo& G, int64_t bh, int t) {
+__device__ __forceinline__ TileWork tile_work(const ArenaView& av, const Geo& G, int64_t bh, int64_t r0, int R) {
   TileWork w;
   const int32_t* elist = av.elist + bh * G.EMAX;
   const int ne = __ldg(av.ecount + bh);
-  const int64_t last_row = int64_t(t) * kQTile + kQTile - 1;
-  w.lo = count_le(elist, ne, last_row - 63 - G.Nk);
+  const int64_t last_row = r0 + R - 1;
+  w.lo = count_le(elist, ne, r0 + R - 64 - G.Nk);
   w.nslash = count_le(elist, ne, last_row) - w.lo;
   const int32_t* vlist = av.vlist + bh * G.KVP;
   const int vc = __ldg(av.vcount + bh);
+  const int64_t last_g = qpos_g(G, last_row);
   int lo = 0, hi = (vc + kKTile - 1) / kKTile;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (first_causal_row_block(G.world, G.q_rank, kpos_g(G, __ldg(vlist + mid * kKTile))) <= 2 * int64_t(t) + 1)
-      lo = mid + 1;
-    else
-      hi = mid;
+    if (kpos_g(G, __ldg(vlist + mid * kKTile)) <= last_g) lo = mid + 1;
+    else hi = mid;
   }
   w.nbar = lo;
   return w;

@@ -25,6 +25,12 @@
 //                      |o - 64 D| <= 63, i.e. a selected slash passes through
 //                      the 64 x 64 blocks of block diagonal D; the sheared cover
 //                      is then built over the offsets of those blocks.
+// GQA packing (pack = g): the g query heads of a KV group share one selection
+// and a query-major tile holds R = 128 / g tokens of all g heads, so elist is
+// the sheared cover for R-row strips: the greedy 64-wide cover of
+// E_R = {u : some selected o in [u - R + 1, u]}; a strip at r0 reads keys
+// [r0 + R - 64 - u, r0 + R - 1 - u].  flist stays the 128-key cover.  The
+// query-major counts of a group are reported at its first head.
 #include "vs_internal.h"
 
 namespace vs {
@@ -77,6 +83,7 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   const int W = H.world;
 
   __shared__ int bad, nks;
+  const int gp = H.pack;  // heads per packed tile (0: no packing)
   __shared__ int part[kIdxThreads + 1];
   if (tid == 0) bad = nks = 0;
   __syncthreads();
@@ -90,6 +97,17 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     const int x = is[i];
     if (x < -1 || x >= NG || (x >= 0 && i > 0 && !(is[i - 1] >= 0 && is[i - 1] < x))) bad = 1;
     if (x >= 0) atomicAdd(&nks, 1);
+  }
+  if (gp) {
+    // packing needs one selection per KV group: every head's lists equal its
+    // group's first head's
+    const int h0 = (bh % H.Hq) / gp * gp, b = bh / H.Hq;
+    const int32_t* iv0 = P.v_idx + (int64_t(b) * H.Hq + h0) * H.kv;
+    const int32_t* is0 = P.s_idx + (int64_t(b) * H.Hq + h0) * H.ks;
+    for (int i = tid; i < H.kv; i += kIdxThreads)
+      if (iv[i] != iv0[i]) bad = 1;
+    for (int i = tid; i < H.ks; i += kIdxThreads)
+      if (is[i] != is0[i]) bad = 1;
   }
   // 2. clear bitmaps
   for (int w = tid; w < H.WG; w += kIdxThreads) offbits[w] = colbits[w] = 0ull;
@@ -184,26 +202,35 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
       return -1;
     };
     if (H.sheared) {
-      int64_t cur = 0;
-      int j = 0;
-      while (true) {
-        int64_t o;
-        if (H.block_cover) {
-          o = next_eff(cur - 127);
-          if (o < 0) break;
-        } else {
-          while (j < nks && is[j] < cur - 127) ++j;
-          if (j == nks) break;
-          o = is[j];
+      // greedy cover by disjoint 64-wide intervals of the selected offsets
+      // dilated by `dil` (tile height - 1)
+      auto cover = [&](int32_t* list, int64_t dil) {
+        int64_t cur = 0;
+        int j = 0, n = 0;
+        while (true) {
+          int64_t o;
+          if (H.block_cover) {
+            o = next_eff(cur - dil);
+            if (o < 0) break;
+          } else {
+            while (j < nks && is[j] < cur - dil) ++j;
+            if (j == nks) break;
+            o = is[j];
+          }
+          const int64_t u = max(cur, o);
+          if (u > int64_t(H.Nq) + dil - 1 || n >= H.EMAX) break;
+          list[n++] = int32_t(u);
+          cur = u + 64;
         }
-        const int64_t u = max(cur, o);
-        if (u > int64_t(H.Nq) + 126 || ne >= H.EMAX) break;
-        elist[ne] = int32_t(u);
-        flist[ne] = int32_t(u);
-        ++ne;
-        cur = u + 64;
+        return n;
+      };
+      nf = cover(flist, kQTile - 1);
+      if (gp) {
+        ne = cover(elist, kQTile / gp - 1);
+      } else {
+        for (int i = 0; i < nf; ++i) elist[i] = flist[i];
+        ne = nf;
       }
-      nf = ne;
     } else {
       // local block diagonals from the key window's end to the query
       // window's end (negative D: keys after the rows locally, which the
@@ -233,16 +260,33 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     // first column
     auto ceil_div = [](int64_t a, int64_t b) { return a >= 0 ? (a + b - 1) / b : -((-a) / b); };
     auto floor_div = [](int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
-    for (int i = 0; i < ne; ++i) {
-      const int64_t e = elist[i];
-      const int64_t tmin = max(int64_t(0), ceil_div(e - 127, kQTile));
-      const int64_t tmax = min(T - 1, floor_div(e - 65 + H.Nk, kQTile));
-      c0 += max(int64_t(0), tmax - tmin + 1);
-    }
-    for (int c = 0; c * kKTile < nv; ++c) {
-      const int64_t m_g = (int64_t(W) * (vlist[c * kKTile] >> 6) + H.kv_rank) * kBlk + (vlist[c * kKTile] & 63);
-      const int64_t tmin = first_causal_row_block(W, H.q_rank, m_g) / 2;
-      c1 += max(int64_t(0), T - tmin);
+    if (!gp) {
+      for (int i = 0; i < ne; ++i) {
+        const int64_t e = elist[i];
+        const int64_t tmin = max(int64_t(0), ceil_div(e - 127, kQTile));
+        const int64_t tmax = min(T - 1, floor_div(e - 65 + H.Nk, kQTile));
+        c0 += max(int64_t(0), tmax - tmin + 1);
+      }
+      for (int c = 0; c * kKTile < nv; ++c) {
+        const int64_t m_g = (int64_t(W) * (vlist[c * kKTile] >> 6) + H.kv_rank) * kBlk + (vlist[c * kKTile] & 63);
+        const int64_t tmin = first_causal_row_block(W, H.q_rank, m_g) / 2;
+        c1 += max(int64_t(0), T - tmin);
+      }
+    } else if ((bh % H.Hq) % gp == 0) {
+      // packed strips of R tokens (unstriped): strip s takes the entries e
+      // in [R s + R - 63 - Nk, R s + R - 1] and the bar chunks whose first
+      // column is at most its last token
+      const int64_t R = kQTile / gp, TS = (H.Nq + R - 1) / R;
+      for (int i = 0; i < ne; ++i) {
+        const int64_t e = elist[i];
+        const int64_t smin = max(int64_t(0), ceil_div(e - R + 1, R));
+        const int64_t smax = min(TS - 1, floor_div(e - R + 63 + H.Nk, R));
+        c0 += max(int64_t(0), smax - smin + 1);
+      }
+      for (int c = 0; c * kKTile < nv; ++c) {
+        const int64_t f = vlist[c * kKTile];
+        c1 += max(int64_t(0), TS - max(int64_t(0), ceil_div(f - R + 1, R)));
+      }
     }
     for (int i = 0; i < nf; ++i) {
       const int64_t f = flist[i];
@@ -313,6 +357,7 @@ vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s
   IndexParams P;
   index_bytes(s, kv, ks, stripe, &P.hdr);
   P.hdr.block_cover = (flags & VS_INDEX_BLOCK_COVER) ? 1 : 0;
+  P.hdr.pack = (flags & VS_INDEX_PACK_GQA) ? s->Hq / s->Hkv : 0;
   P.arena = static_cast<uint8_t*>(arena);
   P.v_idx = v_idx;
   P.s_idx = s_idx;

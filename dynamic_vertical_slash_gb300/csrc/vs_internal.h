@@ -14,10 +14,11 @@ void note_launch(int n = 1);
 void trace_begin(const char* name, cudaStream_t st);
 void trace_end(cudaStream_t st);
 
-// Encodes a 4-D BSHD bf16 tensor map: dims {d, H, N, B}, box {64, 1, rows, 1},
+// Encodes a 4-D BSHD bf16 tensor map: dims {d, H, N, B}, box
+// {64, box_heads, box_rows, 1} (rows land in smem in (token, head) order),
 // 128-byte swizzle.  Returns VS_OK or VS_ERR_CUDA / VS_ERR_SHAPE.
 vs_status make_tmap_bshd(CUtensorMap* m, const void* base, int B, int N, int H, int d, const int64_t s[3],
-                         int box_rows);
+                         int box_rows, int box_heads = 1);
 
 Geo make_geo(const vs_shape* s, const ArenaHeader& h);
 

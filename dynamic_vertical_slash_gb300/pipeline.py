@@ -57,19 +57,24 @@ class VSAttention:
     the [B, Hq] budgets of the last forward).  ``block_cover`` selects the
     block-cover reading of the slashes (whole 64 x 64 blocks, see
     vs_build_block_index_ex); ``shared`` one selection per KV group
-    (vs_estimate_group).  All tensors are BSHD bf16 on the device.
+    (vs_estimate_group); ``packed`` (with ``shared``) packs the group's query
+    heads into the query-major tiles (VS_INDEX_PACK_GQA: 128 / g tokens of the
+    g heads per tile).  All tensors are BSHD bf16 on the device.
     """
 
     def __init__(self, B: int, N: int, Hq: int, Hkv: int, d: int, kv: int, ks: int,
                  device="cuda", last_q: int = 64, scale: Optional[float] = None,
                  pv: Optional[float] = None, ps: Optional[float] = None, block_cover: bool = False,
-                 shared: bool = False):
+                 shared: bool = False, packed: bool = False):
         self.B, self.N, self.Hq, self.Hkv, self.d, self.kv, self.ks = B, N, Hq, Hkv, d, kv, ks
         if (pv is None) != (ps is None):
             raise ValueError("top-p mode needs both pv and ps")
         self.pv, self.ps = pv, ps
         self.block_cover = block_cover
         self.shared = shared
+        if packed and not shared:
+            raise ValueError("head packing needs one selection per KV group (shared=True)")
+        self.packed = packed
         self.last_q = last_q
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         dev = torch.device(device)
@@ -112,7 +117,8 @@ class VSAttention:
         else:
             self.v_idx.copy_(selection[0])
             self.s_idx.copy_(selection[1])
-        B_.vs_build_block_index(q, k, self.v_idx, self.s_idx, None, self.arena, stream, self.block_cover)
+        B_.vs_build_block_index(q, k, self.v_idx, self.s_idx, None, self.arena, stream, self.block_cover,
+                                self.packed)
         B_.vs_attn_fwd(q, k, v, self.arena, self.scale, self.o, self.lse, None, self.ws_fwd, stream)
         self._qkv = (q, k, v)
         return self.o, self.lse

@@ -251,10 +251,19 @@ vs_status vs_build_block_index(const vs_shape* shape, const int32_t* v_idx, cons
  *     M[n, m] = (m <= n) and (m in v_idx or block diagonal
  *               floor(n/64) - floor(m/64) is active),
  * on global positions, where block diagonal D is active iff some selected
- * offset o has |o - 64 D| <= 63 (the slash passes through its blocks).  The
- * attention calls read the flag from the arena.  Other flag bits:
+ * offset o has |o - 64 D| <= 63 (the slash passes through its blocks).
+ * VS_INDEX_PACK_GQA packs the query heads of a KV group into the query-major
+ * tiles (a variant for one selection per KV group, as vs_estimate_group
+ * makes): a tile holds 128 / g tokens of all g = Hq / Hkv heads, so every
+ * K / V block it loads feeds g heads and a slash costs one 64-key unit per
+ * 128 / g tokens instead of two per 128 rows of one head.  It needs the
+ * lists of a group's heads to be equal (else VS_ERR_INDEX on the device),
+ * an unstriped problem without VS_INDEX_BLOCK_COVER (else VS_ERR_ARG) and
+ * g dividing 128, g >= 2 (else VS_ERR_SHAPE).  The mask is unchanged; the
+ * query-major work counts of a group are reported at its first head.  The
+ * attention calls read the flags from the arena.  Other flag bits:
  * VS_ERR_ARG. */
-enum { VS_INDEX_BLOCK_COVER = 1 };
+enum { VS_INDEX_BLOCK_COVER = 1, VS_INDEX_PACK_GQA = 2 };
 vs_status vs_build_block_index_ex(const vs_shape* shape, const int32_t* v_idx, const int32_t* s_idx, int kv, int ks,
                                   const vs_stripe* stripe, int flags, void* arena, size_t arena_bytes,
                                   cudaStream_t stream);

@@ -117,3 +117,22 @@ def test_estimator_entry_points_refuse_the_same_arguments(L):
     # missing score buffers are refused by the no-alloc entry point (it keeps no scores of its own)
     sh = _shape()
     assert L.vs_estimate_noalloc(ctypes.byref(sh), fake, fake, 64, 8, 8, 0.1, fake, fake, None, fake, None) == 1
+
+
+def test_packed_index_host_validation(L):
+    from dynamic_vertical_slash_gb300._binding import VS_ERR_ARG, VS_ERR_SHAPE, make_stripe
+
+    fake = ctypes.c_void_p(0x10000)
+    PACK, BLOCK = 2, 1
+    sh = _shape(Hq=8, Hkv=1)
+    need = L.vs_block_index_bytes(ctypes.byref(sh), 32, 32, None)
+    st = make_stripe(2, 0, 1, 2048)
+    assert L.vs_build_block_index_ex(ctypes.byref(sh), fake, fake, 32, 32, ctypes.byref(st), PACK, fake, 1 << 30,
+                                     None) == VS_ERR_ARG
+    assert L.vs_build_block_index_ex(ctypes.byref(sh), fake, fake, 32, 32, None, PACK | BLOCK, fake, need,
+                                     None) == VS_ERR_ARG
+    sh1 = _shape(Hq=2, Hkv=2)  # g = 1: nothing to pack
+    assert L.vs_build_block_index_ex(ctypes.byref(sh1), fake, fake, 32, 32, None, PACK, fake, need, None) == VS_ERR_SHAPE
+    sh3 = _shape(Hq=3, Hkv=1)  # g = 3 does not divide a 128-row tile
+    assert L.vs_build_block_index_ex(ctypes.byref(sh3), fake, fake, 32, 32, None, PACK, fake, need, None) == VS_ERR_SHAPE
+    assert L.vs_build_block_index_ex(ctypes.byref(sh), fake, fake, 32, 32, None, 4, fake, need, None) == VS_ERR_ARG
