@@ -1,34 +1,37 @@
 // Sparse attention forward on the Vertical-Slash mask (tcgen05 / TMEM / TMA).
 //
-// One CTA owns one 128-row query tile of one query head and walks its units
-//   * slash tiles: 64 keys starting at local key c = 128 t + 64 - e for every
-//     entry e <= 128 t + 127 of the head's query-major list, loaded by TMA;
+// One CTA owns one query tile (128 rows of one query head, or with GQA
+// packing 128 / g tokens of the g heads of a KV group) and walks its units
+//   * slash tiles: 64 keys starting at local key c = r0 + R - 64 - e for every
+//     entry e of the head's query-major list that reaches the tile, by TMA;
 //   * bar chunks: 64 selected columns gathered with cp.async
 // two at a time: a pair of units is one 128-key block, so S = Q K^T is one
 // M=128, N=128 MMA chain and O += P V one K=128 chain (an odd last unit
-// leaves the second half of its pair masked and out of the PV chain).  Per
-// pair: fp32 online softmax on the exact token mask in registers (one thread
-// per row), P (bf16) back into TMEM.
+// leaves the second half of its pair masked and out of the PV chain).
 //
-// Warp roles (384 threads): warp 0 loads Q and the K blocks, warp 11 the V
+// Warp roles (384 threads): warp 0 loads the K blocks, warp 11 the V
 // blocks, warp 10 publishes, per unit, the few words every row's mask is cut
 // from, warp 1 issues the MMAs (the whole warp runs the loop, an elected lane
-// issues), warps 2-5 and 6-9 are two softmax warpgroups that take alternate
-// pairs (even / odd).  Each group keeps its own running maximum, sum and O
-// accumulator, so the groups never wait for each other; the epilogue merges
-// the two partial results the way merge_out_and_lse of Algorithm 2 merges
-// ring steps.
+// issues), warps 2-9 run the softmax: every pair goes through all eight, the
+// two warps of a TMEM lane quarter holding the same 32 rows, one the pair's
+// first unit and one its second.  fp32 online softmax on the exact token mask
+// in registers, P (bf16) into TMEM columns of its own.
 //
-// TMEM columns: O_g [128 g, 128 g + d), S_g [256 + 128 g, +128) for group g.
-// The P of a pair's first unit (keys 0-63) overwrites columns 0-31 of S_g and
-// that of its second unit columns 64-95, each once those scores are in
-// registers, so the MMA issues S of pair i + 2 into S_g only after the PV of
-// pair i; since S of pair i completes after the PV of pair i - 2, a group
-// never has to wait for its own PV before it rescales O or writes P.
+// TMEM columns: O [0, d), score buffers S_j [128 + 128 j, +128) for j < 2,
+// Q [384, 384 + d / 2) and P [448, 512) as bf16 pairs.  The softmax threads
+// write their row of Q there once per tile, so every S = Q K^T chain reads
+// its A operand from TMEM and only K from shared memory.  S of pair i goes to
+// buffer i % 2.  The MMA order is S0 S1, then per pair i: PV_i (once P_i is
+// stored), S_{i+2} into buffer i % 2, whose scores the softmax has read by
+// then: the scores of pair i + 1 are computed while pair i is in softmax.
+// P_i is stored once PV_{i-1} has read P_{i-1}.  The row's reference maximum
+// is lazy (it moves only for the row's first entries or an entry 2^64 above
+// it); the two threads of a row agree on it through a named barrier of their
+// two warps, and before O is rescaled every PV issued so far has completed.
 //
-// Shared memory: Q, a ring of slots that each hold K or V of one pair (128
-// rows), filled and released in the MMA's order S0 S1 PV0 S2 PV1 S3 ..., and
-// a ring of per-pair mask records.
+// Shared memory: a ring of slots that each hold K or V of one pair (128 rows),
+// filled and released in the MMA's order K0 K1 V0 K2 V1 K3 ..., and a ring of
+// per-pair mask records.
 #include "vs_internal.h"
 #include "vs_kernel_common.cuh"
 
@@ -38,11 +41,12 @@ namespace {
 constexpr int kFwdThreads = 384;
 constexpr int kFwdRecWarp = 10;
 constexpr int kFwdVWarp = 11;
-constexpr int kFwdGroup = 128;  // threads per softmax warpgroup
+constexpr int kFwdSoftmax = 256;  // softmax threads (warps 2-9): two per row, one per unit of a pair
 constexpr int kPairKeys = 2 * kKTile;
-constexpr int kFwdSlots = 5;
+constexpr int kFwdSlots = 6;
 constexpr int kRecRing = 8;
-constexpr uint32_t kColO = 0, kColS = 256, kTmemCols = 512;
+constexpr int kSBufs = 2;  // score buffers: S of pair i + 1 is computed while pair i is in softmax
+constexpr uint32_t kColO = 0, kColS = 128, kColQ = 128 + 128 * kSBufs, kColP = 448, kTmemCols = 512;
 constexpr float kRefSlack = 18446744073709551616.0f;  // 2^64: largest masked pair sum accepted against the reference
 
 // What a unit's 128 row masks are cut from (written by the loader).
@@ -88,25 +92,26 @@ __device__ __forceinline__ uint64_t rec_row_mask(const MaskRec& rc, int kind, in
 template <int D>
 struct FwdSmem {
   static constexpr int NH = D / 64;
-  uint8_t q[NH][kQTile * 128];
   uint8_t slot[kFwdSlots][NH][kPairKeys * 128];  // K or V of one pair, 128B-swizzled, per d-half
   MaskRec rec[kRecRing][2];                      // mask records of a pair's two units
-  uint64_t q_full;
+  uint64_t q_tmem;  // Q rows written to TMEM by the softmax threads
   uint64_t slot_full[kFwdSlots], slot_empty[kFwdSlots];
   uint64_t rec_full[kRecRing], rec_empty[kRecRing];
-  uint64_t s_full[2], p_full[2];  // per softmax group
+  uint64_t s_full[kSBufs], p_full[kSBufs];  // per score buffer
+  uint64_t pv_done[kSBufs];  // PV of pair i completes on pv_done[i % kSBufs]
   uint64_t o_final, teardown;
-  float red_m[2][kQTile];  // per group: reference maximum (log2 units)
-  float red_l[2][kQTile];  // per group: row sum
+  float red_m[2][kQTile];  // per half (unit of a pair): masked maximum, for re-basing
+  float red_l[2][kQTile];  // per half: row sum
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct FwdParams {
   const void* arena;
-  const uint8_t* k;  // K base (bytes)
+  const uint8_t* q;  // Q base (bytes)
+  const uint8_t* k;
   const uint8_t* v;
-  int64_t sk[3], sv[3], so[3];
+  int64_t sq[3], sk[3], sv[3], so[3];
   int B, Nq, Hq, Hkv;
   float scale_log2;
   uint8_t* o;
@@ -119,168 +124,48 @@ struct FwdParams {
 // slot ring): K0, K1, then per pair i: V_i, K_{i+2}.
 template <typename F>
 __device__ __forceinline__ void for_each_block(int P, F&& f) {
-  f(0, 0);
-  if (P > 1) f(0, 1);
+  for (int j = 0; j < kSBufs && j < P; ++j) f(0, j);
   for (int i = 0; i < P; ++i) {
     f(1, i);
-    if (i + 2 < P) f(0, i + 2);
+    if (i + kSBufs < P) f(0, i + kSBufs);
   }
 }
 
-// Moves the rows' reference maxima for one pair (the exact online-softmax
-// update, for every row of the warp) and writes the pair's P: exact masked
-// maximum from the scores still in TMEM, O and the running sum rescaled where
-// the maximum grows, P recomputed
-// unit by unit against the new references and stored as it is made (the P
-// of unit hh lands on score columns of that unit the recomputation has
-// already read).  Rare (the row's first pair, or an entry 2^64 above the
-// reference), so it lives out of line and keeps the common path's registers
-// free.  Warp-collective.
-struct RowRef {
-  float m_run, l_run;
-};
-template <int D>
-__device__ __noinline__ RowRef fwd_rebase_pair(uint32_t tl, uint32_t colS, uint32_t colO, uint64_t mask0,
-                                               uint64_t mask1, float m_run, float l_run, float scale_log2) {
-  float mx[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    const uint64_t mask = hh ? mask1 : mask0;
-    uint32_t sr[64];
-    tmem_ld32(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-    tmem_ld32(tl + colS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-    tmem_ld_wait();
-#pragma unroll
-    for (int k = 0; k < 64; ++k)
-      if ((mask >> k) & 1ull) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]) * scale_log2);
-  }
-  const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-  const bool grow = (m_run != -INFINITY) && (mt > m_run);
-  if (m_run == -INFINITY) m_run = mt;  // first entries (or still none): the O row is zero
-  if (__any_sync(0xffffffffu, grow)) {
-    const float alpha = grow ? ex2(m_run - mt) : 1.f;
-#pragma unroll 1
-    for (int cc = 0; cc < D; cc += 16) {
-      uint32_t ov[16];
-      tmem_ld16(tl + colO + cc, ov);
-      tmem_ld_wait();
-#pragma unroll
-      for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-      tmem_st16(tl + colO + cc, ov);
-    }
-    tmem_st_wait();
-    if (grow) {
-      l_run *= alpha;
-      m_run = mt;
-    }
-  }
-  const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
-  float ps[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) ps[k] = 0.f;
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    const uint64_t mask = hh ? mask1 : mask0;
-    uint32_t sr[64], pk[32];
-    tmem_ld32(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-    tmem_ld32(tl + colS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-    tmem_ld_wait();
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      float p0 = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, nref));
-      float p1 = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, nref));
-      p0 = ((mask >> (2 * k)) & 1ull) ? p0 : 0.f;
-      p1 = ((mask >> (2 * k + 1)) & 1ull) ? p1 : 0.f;
-      ps[k & 7] += p0 + p1;
-      pk[k] = pack_bf16x2(p0, p1);
-    }
-    tmem_st16(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-    tmem_st16(tl + colS + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-  }
-  l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-  return RowRef{m_run, l_run};
-}
-
-// The same for the pair's second unit once the first unit's P (against the
-// old references) is already in TMEM: the maximum comes from the second
-// unit's scores, and where it grows O, the running sum and the stored P of
-// the first unit are rescaled too.  A row whose reference was still unset
-// has no entry in the first unit, so its stored P is zero.
-template <int D>
-__device__ __noinline__ RowRef fwd_rebase_second(uint32_t tl, uint32_t colS, uint32_t colO, uint64_t mask1,
-                                                 float m_run, float l_run, float scale_log2) {
-  float mx[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-  {
-    uint32_t sr[64];
-    tmem_ld32(tl + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-    tmem_ld32(tl + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-    tmem_ld_wait();
-#pragma unroll
-    for (int k = 0; k < 64; ++k)
-      if ((mask1 >> k) & 1ull) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]) * scale_log2);
-  }
-  const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-  const bool grow = (m_run != -INFINITY) && (mt > m_run);
-  if (m_run == -INFINITY) m_run = mt;
-  if (__any_sync(0xffffffffu, grow)) {
-    const float alpha = grow ? ex2(m_run - mt) : 1.f;
-#pragma unroll 1
-    for (int cc = 0; cc < D; cc += 16) {
-      uint32_t ov[16];
-      tmem_ld16(tl + colO + cc, ov);
-      tmem_ld_wait();
-#pragma unroll
-      for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-      tmem_st16(tl + colO + cc, ov);
-    }
-    tmem_st_wait();  // also the first unit's P stores
-#pragma unroll 1
-    for (int cc = 0; cc < 32; cc += 16) {
-      uint32_t pv[16];
-      tmem_ld16(tl + colS + cc, pv);
-      tmem_ld_wait();
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        pv[k] = pack_bf16x2(__uint_as_float(pv[k] << 16) * alpha, __uint_as_float(pv[k] & 0xFFFF0000u) * alpha);
-      tmem_st16(tl + colS + cc, pv);
-    }
-    if (grow) {
-      l_run *= alpha;
-      m_run = mt;
-    }
-  }
-  const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
-  float ps[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) ps[k] = 0.f;
-  uint32_t sr[64], pk[32];
-  tmem_ld32(tl + colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-  tmem_ld32(tl + colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+// Re-basing helpers, out of line (rare: a row's first entries, or an entry
+// 2^64 above the reference), so the common path keeps its registers.
+// Masked maximum (log2 units) of one unit's 64 scores of the row, -inf if the
+// mask is empty.  Warp-collective.
+__device__ __noinline__ float fwd_unit_max(uint32_t taddr, uint64_t mask, float scale_log2) {
+  uint32_t sr[64];
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
   tmem_ld_wait();
+  float mx[8];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    float p0 = ex2(fmaf(__uint_as_float(sr[2 * k]), scale_log2, nref));
-    float p1 = ex2(fmaf(__uint_as_float(sr[2 * k + 1]), scale_log2, nref));
-    p0 = ((mask1 >> (2 * k)) & 1ull) ? p0 : 0.f;
-    p1 = ((mask1 >> (2 * k + 1)) & 1ull) ? p1 : 0.f;
-    ps[k & 7] += p0 + p1;
-    pk[k] = pack_bf16x2(p0, p1);
+  for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 64; ++k)
+    if ((mask >> k) & 1ull) mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k]) * scale_log2);
+  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+// O[row, c] *= alpha for the `ncols` accumulator columns at taddr.  Warp-collective.
+__device__ __noinline__ void fwd_scale_o(uint32_t taddr, int ncols, float alpha) {
+#pragma unroll 1
+  for (int cc = 0; cc < ncols; cc += 16) {
+    uint32_t ov[16];
+    tmem_ld16(taddr + cc, ov);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+    tmem_st16(taddr + cc, ov);
   }
-  tmem_st16(tl + colS + 64, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-  tmem_st16(tl + colS + 80, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-  l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-  return RowRef{m_run, l_run};
+  tmem_st_wait();
 }
 
 // The kernel body, compiled once per mask reading (BLOCK: block-cover
 // slashes) so that neither reading carries the other's code.
 template <int D, bool BLOCK>
-__device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorMap& tmQp, const CUtensorMap& tmK,
-                                         const CUtensorMap& tmV, const FwdParams& p) {
+__device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -328,19 +213,20 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     if (!arena_ok && av.hdr->status) raise_error(p.err, av.hdr->status);
     else if (!arena_ok && av.hdr->magic != kArenaMagic) raise_error(p.err, VS_ERR_ARG);
     s.abort_flag = 0;
-    mbar_init(&s.q_full, 1);
+    mbar_init(&s.q_tmem, kFwdSoftmax);
     for (int i = 0; i < kFwdSlots; ++i) {
       mbar_init(&s.slot_full[i], 1);
       mbar_init(&s.slot_empty[i], 1);
     }
     for (int i = 0; i < kRecRing; ++i) {
       mbar_init(&s.rec_full[i], 1);
-      mbar_init(&s.rec_empty[i], kFwdGroup);
+      mbar_init(&s.rec_empty[i], kFwdSoftmax);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.p_full[i], kFwdGroup);
+      mbar_init(&s.p_full[i], kFwdSoftmax);
     }
+    for (int i = 0; i < kSBufs; ++i) mbar_init(&s.pv_done[i], 1);
     mbar_init(&s.o_final, 1);
     mbar_init(&s.teardown, 1);
     fence_mbar_init();
@@ -358,7 +244,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
 
   if (warp == 0 || warp == kFwdVWarp) {
     // ------------------------------------------------------------ producers
-    // Warp 0 loads Q and the K blocks, warp kFwdVWarp the V blocks.  Each walks
+    // Warp 0 loads the K blocks, warp kFwdVWarp the V blocks.  Each walks
     // the whole block sequence (so both agree on every block's slot and
     // phase) and acts on its own kind only: one thread's TMA issue blocks
     // while the copy engine works through its boxes, so with two issuers the
@@ -369,11 +255,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     if (P > 0) {
       if (lane == 0) {
         if (my_kind == 0) {
-          prefetch_tmap(&tmQ);
           prefetch_tmap(&tmK);
-          mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
-          // packed: a box of R tokens x g heads, rows in (token, head) order
-          for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], gp ? &tmQp : &tmQ, &s.q_full, 64 * hf, h, int(r0), b);
         } else {
           prefetch_tmap(&tmV);
         }
@@ -557,19 +439,20 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Pair i belongs to softmax group g = i & 1.  Order: S0, S1, then per
-    // pair i: PV_i (once group g has written P_i), S_{i+2} into the same S_g.
-    // The whole warp runs the loop; one elected lane issues.
+    // S of pair i goes to score buffer i % 2.  Order: S0, S1, then per pair
+    // i: PV_i (once its P is in buffer i % 2), S_{i+2} into the same buffer
+    // (the tensor pipe runs them in order, so PV_i has read P_i).  The
+    // whole warp runs the loop; one elected lane issues.
     if (P > 0) {
       const uint32_t idS = idesc_bf16(128, kPairKeys, 0, 0);
       const uint32_t idO = idesc_bf16(128, D, 0, 1);
-      bool ok = mbar_wait_warp(&s.q_full, 0, ab, VS_ERR_TIMEOUT);
+      bool ok = mbar_wait_warp(&s.q_tmem, 0, ab, VS_ERR_TIMEOUT);
       int c = 0;
       for_each_block(P, [&](int kind, int i) {
         if (!ok) return;
-        const int g = i & 1;
+        const int j = i % kSBufs;
         if (kind) {
-          if (!(ok = mbar_wait_warp(&s.p_full[g], (i >> 1) & 1, ab, VS_ERR_TIMEOUT))) return;
+          if (!(ok = mbar_wait_warp(&s.p_full[j], (i / kSBufs) & 1, ab, VS_ERR_TIMEOUT))) return;
         }
         const int sl = c % kFwdSlots;
         if (!(ok = mbar_wait_warp(&s.slot_full[sl], (c / kFwdSlots) & 1, ab, VS_ERR_TIMEOUT))) return;
@@ -578,20 +461,20 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         if (!kind) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t da = sdesc_sw128(smem_u32(s.q[kk / 4]) + (kk % 4) * 32, 16, 1024);
             const uint64_t db = sdesc_sw128(smem_u32(s.slot[sl][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ss_warp(tmem + kColS + 128 * g, da, db, idS, kk > 0);
+            mma_ts_warp(tmem + kColS + 128 * j, tmem + kColQ + kk * 8, db, idS, kk > 0);  // A = Q in TMEM
           }
-          mma_commit_warp(&s.s_full[g]);
+          mma_commit_warp(&s.s_full[j]);
         } else {
           const int nk = (2 * i + 1 < U) ? kPairKeys / 16 : kKTile / 16;
 #pragma unroll
           for (int kk = 0; kk < kPairKeys / 16; ++kk) {
             if (kk >= nk) break;
             const uint64_t dv = sdesc_sw128(smem_u32(s.slot[sl][0]) + kk * 2048, kPairKeys * 128, 1024);
-            const uint32_t a_p = tmem + kColS + 128 * g + (kk >> 2) * 64 + (kk & 3) * 8;  // P of unit kk / 4
-            mma_ts_warp(tmem + kColO + 128 * g, a_p, dv, idO, (i >= 2 || kk > 0));
+            const uint32_t a_p = tmem + kColP + (kk >> 2) * 32 + (kk & 3) * 8;  // P of unit kk / 4
+            mma_ts_warp(tmem + kColO, a_p, dv, idO, (i > 0 || kk > 0));
           }
+          mma_commit_warp(&s.pv_done[j]);
         }
         mma_commit_warp(&s.slot_empty[sl]);
         mma_issued = true;
@@ -601,7 +484,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     }
   } else if (warp >= 2 && warp < 2 + 8) {
     // ------------------------------------------------------------ softmax
-    const int grp = (warp - 2) >> 2;         // softmax group: pairs i with i & 1 == grp
+    // Every pair goes through all eight warps: the warps of TMEM lane quarter
+    // q (warps 2 + q' with q' & 3 == q) hold rows 32 q .. 32 q + 31, one the
+    // pair's first unit (keys 0-63), the other its second.  The two threads
+    // of a row keep one reference maximum m_run (log2 units) and each its
+    // own partial sum; O has one accumulator.
+    const int half = (warp - 2) >> 2;        // which unit of each pair
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;       // query row within the tile
     const int ti = gp ? r / gp : r;          // its token within the tile
@@ -609,39 +497,56 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
     const uint32_t tl = tmem + (uint32_t(quarter * 32) << 16);
     const int64_t n_loc = r0 + ti;
     const bool row_ok = n_loc < p.Nq;
-    const uint32_t colO = kColO + 128 * grp, colS = kColS + 128 * grp;
+    const int qbar = 2 + quarter;            // named barrier of the quarter's two warps
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     const int64_t n_g = qpos_g(G, n_loc);
-    for (int i = grp; i < P; i += 2) {
-      const int ri = i % kRecRing;
-      // the pair's row masks first: the record is published ahead of the
-      // scores, so cutting the masks overlaps the S MMAs
+    if (P > 0) {
+      // the row's Q, columns [half d/2, (half + 1) d/2), into TMEM as bf16
+      // pairs: the A operand of every S = Q K^T chain of the tile
+      uint32_t w[D / 4];
+      const uint8_t* src = p.q + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(hrow) * p.sq[2]) * 2 + half * D;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const uint4 x = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
+        w[4 * c] = x.x;
+        w[4 * c + 1] = x.y;
+        w[4 * c + 2] = x.z;
+        w[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_st16(tl + kColQ + half * (D / 4) + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c]));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.q_tmem);
+    }
+    for (int i = 0; i < P; ++i) {
+      const int ri = i % kRecRing, j = i % kSBufs;
+      const uint32_t colS = kColS + 128 * j + 64 * half;  // this unit's scores
+      // the unit's row mask first: the record is published ahead of the
+      // scores, so cutting the mask overlaps the S MMAs
       ok = mbar_wait(&s.rec_full[ri], (i / kRecRing) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      const MaskRec& rc0 = s.rec[ri][0];
-      const MaskRec& rc1 = s.rec[ri][1];
-      const uint64_t mask0 = row_ok ? rec_row_mask<BLOCK>(rc0, rc0.kind, ti, n_g) : 0ull;
-      const uint64_t mask1 = row_ok ? rec_row_mask<BLOCK>(rc1, rc1.kind, ti, n_g) : 0ull;
+      const MaskRec& rc = s.rec[ri][half];
+      const uint64_t mask = row_ok ? rec_row_mask<BLOCK>(rc, rc.kind, ti, n_g) : 0ull;
       mbar_arrive(&s.rec_empty[ri]);
-      ok = mbar_wait(&s.s_full[grp], (i >> 1) & 1, ab, VS_ERR_TIMEOUT);
+      ok = mbar_wait(&s.s_full[j], (i / kSBufs) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // P against the row's reference maximum m_run (log2 units), one unit at
-      // a time.  The reference is lazy: it only moves when a unit's masked sum
-      // shows an entry more than 2^64 above it (or for the row's first
-      // entries); the sum bounds every single entry, so P stays <= 2^64.  S
-      // of pair i completing means the group's PV of pair i - 2 has completed
-      // too, so O may be rescaled here.
+      // P against the row's reference maximum m_run.  The reference is lazy:
+      // it only moves when a unit's masked sum shows an entry more than 2^64
+      // above it (or for the row's first entries); the sum bounds every
+      // single entry, so P stays <= 2^64.
       uint32_t pk[32];
       float unit_sum;
-      auto make_p = [&](int hh, uint64_t mask, float ref) {
+      auto make_p = [&](float ref) {
         // two keys at a time in paired fp32: t = S scale log2(e) - ref, and
         // four pairs of partial row sums
         uint64_t ps2[4];
@@ -649,8 +554,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         for (int k = 0; k < 4; ++k) ps2[k] = 0ull;
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
         uint32_t sr[64];
-        tmem_ld32(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tl + colS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tl + colS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tl + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld_wait();
         const uint32_t mlo = uint32_t(mask), mhi = uint32_t(mask >> 32);
 #pragma unroll
@@ -671,52 +576,63 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         f2_unpack(ps2[3], s6, s7);
         unit_sum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
       };
-      auto store_p = [&](int hh) {
-        tmem_st16(tl + colS + 64 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tl + colS + 64 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-      };
       // one copy of the unit body (the hot loops of all warp roles share the
-      // SM's instruction cache): unit 0, then unit 1 unless unit 0 sent the
-      // pair to re-basing
+      // SM's instruction cache): a second pass only after a re-basing
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint64_t mask = hh ? mask1 : mask0;
-        make_p(hh, mask, m_run == -INFINITY ? 0.f : m_run);
-        // (a row whose reference is still unset at unit 1 has no entry in unit 0)
+      for (int pass = 0;; ++pass) {
+        make_p(m_run == -INFINITY ? 0.f : m_run);
+        if (pass) break;
         const bool need = (mask != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
-        if (__any_sync(0xffffffffu, need)) {
-          const RowRef rr = hh ? fwd_rebase_second<D>(tl, colS, colO, mask1, m_run, l_run, p.scale_log2)
-                               : fwd_rebase_pair<D>(tl, colS, colO, mask0, mask1, m_run, l_run, p.scale_log2);
-          m_run = rr.m_run;
-          l_run = rr.l_run;
-          break;
+        // both threads of a row see the same decision
+        if (!bar_sync_or(qbar, 64, need)) break;
+        // re-base: the row's new reference is the masked maximum of the
+        // pair (both units); where it grows, O (this thread's half of the
+        // columns, once every PV issued so far has completed) and the running
+        // sum are rescaled; then P is made again against the new reference
+        s.red_m[half][r] = fwd_unit_max(tl + colS, mask, p.scale_log2);
+        bar_sync_and(qbar, 64, true);
+        const float mt = fmaxf(s.red_m[0][r], s.red_m[1][r]);
+        bar_sync_and(qbar, 64, true);  // both have read red_m before the next pair may write it
+        const bool grow = (m_run != -INFINITY) && (mt > m_run);
+        if (__any_sync(0xffffffffu, grow)) {
+          // PV_{i-1} complete implies every earlier PV is (in-order pipe).  S_i
+          // having completed implies PV_{i-kSBufs} has, so the barrier of
+          // PV_{i-1} is at most one phase behind it and its parity identifies it.
+          if (i > 0 && !mbar_wait(&s.pv_done[(i - 1) % kSBufs], ((i - 1) / kSBufs) & 1, ab, VS_ERR_TIMEOUT))
+            ok = false;
+          if (!__all_sync(0xffffffffu, ok)) break;
+          tc_fence_after();
+          const float alpha = grow ? ex2(m_run - mt) : 1.f;
+          fwd_scale_o(tl + kColO + (D / 2) * half, D / 2, alpha);
+          if (grow) l_run *= alpha;
         }
-        store_p(hh);
-        l_run += unit_sum;
+        if (m_run == -INFINITY || grow) m_run = mt;
       }
+      if (!ok) break;
+      // P's columns are free once PV_{i-1} has read them
+      if (i > 0 && !mbar_wait(&s.pv_done[(i - 1) % kSBufs], ((i - 1) / kSBufs) & 1, ab, VS_ERR_TIMEOUT)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      tmem_st16(tl + kColP + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(tl + kColP + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      l_run += unit_sum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&s.p_full[grp]);
+      mbar_arrive(&s.p_full[j]);
     }
     // -------------------------------------------------------------- epilogue
-    // Wait for every MMA, publish this group's (max, sum) per row, and merge
-    // the two groups' partial results; group g writes columns [g d/2, (g+1) d/2).
+    // Wait for every MMA, add the row's two partial sums; each half writes
+    // columns [half d/2, (half + 1) d/2) of the row.
     bool e_ok = ok && (P == 0 || mbar_wait(&s.o_final, 0, ab, VS_ERR_TIMEOUT));
     e_ok = __all_sync(0xffffffffu, e_ok);
-    s.red_m[grp][r] = m_run;
-    s.red_l[grp][r] = l_run;
-    e_ok = bar_sync_and(1, 2 * kFwdGroup, e_ok);
+    s.red_l[half][r] = l_run;
+    e_ok = bar_sync_and(1, kFwdSoftmax, e_ok);
     tc_fence_after();
     if (e_ok) {
-      const float m0 = s.red_m[0][r], m1 = s.red_m[1][r];
-      const float l0 = s.red_l[0][r], l1 = s.red_l[1][r];
-      const bool has0 = P > 0 && l0 > 0.f, has1 = P > 1 && l1 > 0.f;  // group 1 ran only if P > 1
-      const float mm = fmaxf(has0 ? m0 : -INFINITY, has1 ? m1 : -INFINITY);
-      const float f0 = has0 ? ex2(m0 - mm) : 0.f, f1 = has1 ? ex2(m1 - mm) : 0.f;
-      const float l_run2 = l0 * f0 + l1 * f1;
-      const bool empty = !(l_run2 > 0.f);
-      const float inv = empty ? 0.f : 1.f / l_run2;
-      const float lse_step = empty ? -INFINITY : (mm + __log2f(l_run2)) * kLn2;
+      const float l_tot = s.red_l[0][r] + s.red_l[1][r];
+      const bool empty = !(l_tot > 0.f);
+      const float inv = empty ? 0.f : 1.f / l_tot;
+      const float lse_step = empty ? -INFINITY : (m_run + __log2f(l_tot)) * kLn2;
       float* lse_p = p.lse + (int64_t(b) * p.Hq + hrow) * p.Nq + n_loc;
       uint8_t* orow = p.o + (int64_t(b) * p.so[0] + n_loc * p.so[1] + int64_t(hrow) * p.so[2]) * 2;
       float wa = 0.f, wb = 1.f, lse_new = lse_step;
@@ -735,25 +651,19 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
           wb = empty ? 0.f : __expf(lse_step - lse_new);
         }
       }
-      // both groups have read lse_old before group 0 overwrites it
-      bar_sync_and(1, 2 * kFwdGroup, true);
-      const float g0 = f0 * inv, g1 = f1 * inv;
+      // both halves have read lse_old before half 0 overwrites it
+      bar_sync_and(1, kFwdSoftmax, true);
 #pragma unroll 1
-      for (int cc = (D / 2) * grp; cc < (D / 2) * (grp + 1); cc += 16) {
-        uint32_t o0[16], o1[16];
+      for (int cc = (D / 2) * half; cc < (D / 2) * (half + 1); cc += 16) {
+        uint32_t o0[16];
         if (P > 0) {  // warp-collective TMEM reads
           tmem_ld16(tl + kColO + cc, o0);
-          if (P > 1) tmem_ld16(tl + kColO + 128 + cc, o1);
           tmem_ld_wait();
         }
         if (!row_ok) continue;
         float y[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = has0 ? __uint_as_float(o0[i]) * g0 : 0.f;
-          const float c = has1 ? __uint_as_float(o1[i]) * g1 : 0.f;
-          y[i] = empty ? 0.f : a + c;
-        }
+        for (int i = 0; i < 16; ++i) y[i] = (empty || P == 0) ? 0.f : __uint_as_float(o0[i]) * inv;
         if (acc) {
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
@@ -781,7 +691,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
         *reinterpret_cast<uint4*>(orow + cc * 2) = w0;
         *reinterpret_cast<uint4*>(orow + cc * 2 + 16) = w1;
       }
-      if (row_ok && grp == 0) *lse_p = lse_new;
+      if (row_ok && half == 0) *lse_p = lse_new;
     }
   }
 
@@ -804,33 +714,25 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmQ, const CUtensorM
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQp,
-                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const FwdParams p) {
-  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmQ, tmQp, tmK, tmV, p);
-  else fwd_body<D, false>(tmQ, tmQp, tmK, tmV, p);
+    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmK, tmV, p);
+  else fwd_body<D, false>(tmK, tmV, p);
 }
 
 template <int D>
 vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const void* v, const void* arena,
                        float scale, void* o, float* lse, float* o_acc, int* err, cudaStream_t st) {
-  CUtensorMap tq, tqp, tk, tv;
+  CUtensorMap tk, tv;
   vs_status rc;
-  if ((rc = make_tmap_bshd(&tq, q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile)) != VS_OK) return rc;
-  // GQA-packed tiles (when the arena asks for them): 128 / g tokens x g heads
-  const int g = sh->Hq / sh->Hkv;
-  if (g >= 2 && kQTile % g == 0) {
-    if ((rc = make_tmap_bshd(&tqp, q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile / g, g)) != VS_OK) return rc;
-  } else {
-    tqp = tq;
-  }
   if ((rc = make_tmap_bshd(&tk, k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kKTile)) != VS_OK) return rc;
   if ((rc = make_tmap_bshd(&tv, v, sh->B, sh->Nk, sh->Hkv, D, sh->sv, kKTile)) != VS_OK) return rc;
   FwdParams p;
   p.arena = arena;
+  p.q = static_cast<const uint8_t*>(q);
   p.k = static_cast<const uint8_t*>(k);
   p.v = static_cast<const uint8_t*>(v);
   for (int i = 0; i < 3; ++i) {
+    p.sq[i] = sh->sq[i];
     p.sk[i] = sh->sk[i];
     p.sv[i] = sh->sv[i];
     p.so[i] = sh->so[i];
@@ -850,7 +752,7 @@ vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const v
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   const dim3 grid(unsigned(T) * sh->B * sh->Hq);
   trace_begin("fwd", st);
-  vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tqp, tk, tv, p);
+  vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tk, tv, p);
   trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;

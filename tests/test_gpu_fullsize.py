@@ -159,6 +159,13 @@ def test_fullsize_sampled_parity(vs, name):
     _check_selection(v_gpu, s_gpu, iv_gpu, is_gpu, v_ref, s_ref, iv, is_, w.kv, w.ks)
 
     # ---- attention on the oracle's selection, same buffers and launches
+    _attention_sampled(w, x, att, iv, is_, q, k, v, do, dense)
+
+
+def _attention_sampled(w, x, att, iv, is_, q, k, v, do, dense):
+    """Forward and backward of `att` on the selection (iv, is_) against the
+    oracle on sampled rows and keys."""
+    B, N, Hq, Hkv, g = w.B, w.N, w.Hq, w.Hkv, w.Hq // w.Hkv
     att.forward(q, k, v, selection=(torch.from_numpy(iv).cuda(), torch.from_numpy(is_).cuda()))
     dq, dk, dv = att.backward(do)
     torch.cuda.synchronize()
@@ -190,6 +197,29 @@ def test_fullsize_sampled_parity(vs, name):
         assert rel_l2(got_v, dv_ref) <= TOL
         _per_head("dK", got_k, dk_ref, kb[:, 1])
         _per_head("dV", got_v, dv_ref, kb[:, 1])
+
+
+def test_fullsize_packed_group_selection_sampled_parity(vs):
+    """The per-KV-group selection with the group's heads packed into the
+    query-major tiles (VSAttention(shared=True, packed=True)) at 128K: the
+    selection replays bit-exactly from the GPU's own fp32 group sums, and the
+    attention on the oracle's fp64 group selection matches on sampled rows
+    and keys."""
+    w = synth.workloads()["qwen3b-128k"]
+    x = synth.make_batch(w)
+    B, N, Hq, Hkv, d, g = w.B, w.N, w.Hq, w.Hkv, w.d, w.Hq // w.Hkv
+    q, k, v, do = (dev_bf16(x[n]) for n in ("q", "k", "v", "dout"))
+    att = vs.VSAttention(B, N, Hq, Hkv, d, w.kv, w.ks, last_q=w.last_q, scale=w.scale, shared=True, packed=True)
+    att.forward(q, k, v)
+    torch.cuda.synchronize()
+    att.check()
+    v_gpu, s_gpu = att.v_score.cpu().numpy(), att.s_score.cpu().numpy()
+    iv_r, is_r = oracle.select_group(v_gpu, s_gpu, w.kv, w.ks, g, dtype=np.float32)
+    np.testing.assert_array_equal(att.v_idx.cpu().numpy(), iv_r)
+    np.testing.assert_array_equal(att.s_idx.cpu().numpy(), is_r)
+    v_ref, s_ref = _oracle_scores(x, w)
+    iv, is_ = oracle.select_group(v_ref, s_ref, w.kv, w.ks, g)
+    _attention_sampled(w, x, att, iv, is_, q, k, v, do, False)
 
 
 def test_fullsize_striped_ring_sampled_parity(vs):
