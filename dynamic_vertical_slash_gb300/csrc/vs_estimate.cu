@@ -15,11 +15,16 @@
 //                          in a fixed order (deterministic, no float atomics)
 //   pass 4  est_topk     : radix select of the k-th largest score, then an
 //                          index-ordered compaction; ties go to the lower index
+//                          (one thread-block cluster of 8 CTAs per list)
 // Warp roles in passes 1 and 2: warp 0 issues TMA loads, warp 1 the MMAs
 // (the whole warp runs the loop, an elected lane issues), warps 2-9 read the scores (one thread per TMEM lane, two warps
 // per lane quarter, each on half the columns).  Waits are bounded.
+#include <cooperative_groups.h>
+
 #include "vs_internal.h"
 #include "vs_kernel_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace vs {
 namespace {
@@ -442,59 +447,134 @@ __device__ __forceinline__ int block_scan(int x, int* wsum, int* total) {
   return res;
 }
 
-// Radix select of the k-th largest of N fp32 scores (the bit patterns of
-// nonnegative floats order like their values), then an index-ordered
-// compaction: out[0, k) = the k largest scores' indices, ties to the lower
-// index, ascending; out[k, cap) = -1.  Called by all threads of the block.
-__device__ void topk_block(const uint32_t* x, int N, int k, int32_t* out, int cap) {
-  __shared__ int hist[256];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_want;
-  __shared__ int wsum[32];
-  for (int i = k + threadIdx.x; i < cap; i += blockDim.x) out[i] = -1;
-  if (k <= 0) return;
-  if (threadIdx.x == 0) {
-    s_prefix = 0;
-    s_want = k;
-  }
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+// Selection on a thread-block cluster: the kSelCluster CTAs of a cluster
+// share one list, each holding a contiguous chunk of it (whole 64-token
+// blocks).  Per radix digit every CTA histograms its chunk; after a cluster
+// barrier each CTA adds the kSelCluster histograms in rank order from the
+// peers' shared memory (integer counts: the same in every CTA) and takes the
+// same decision, so no CTA waits for another's broadcast.  Histograms are
+// double-buffered across digits: the buffer of digit p is zeroed again at
+// digit p + 2, after every peer has passed the barrier of digit p + 1 and
+// hence finished reading it.  The compaction places each CTA's chunk after
+// the counts of the lower ranks.  Every CTA of a cluster takes the same
+// branches and passes the same barriers; the last one keeps a CTA's shared
+// memory alive until its peers have read it.
+constexpr int kSelCluster = 8;
+
+struct SelShared {
+  int cnt[2][256];                // digit counts of this CTA's chunk, per digit parity
+  unsigned long long sum[2][256]; // top-p: digit mass of this CTA's chunk
+  int mcnt[256];                  // the cluster's counts of the current digit
+  unsigned long long msum[256];
+  int wsum[32];
+  uint64_t red[32];
+  uint64_t part;                  // published: this chunk's saturated mass
+  int bad, skip, n_gt, n_eq;      // published: validation, skip flag, compaction counts
+  uint64_t prefix, want;
+  int above;
+};
+
+// The chunk [lo, hi) of an N-token list that cluster rank `rank` holds.
+__device__ __forceinline__ void sel_chunk(int N, int rank, int& lo, int& hi) {
+  const int nb = (N + 63) / 64, per = (nb + kSelCluster - 1) / kSelCluster;
+  lo = min(N, 64 * per * rank);
+  hi = min(N, 64 * per * (rank + 1));
+}
+
+// True in every CTA of the cluster if the status word holds a failure when
+// any of them looked (read before any CTA of this launch may raise one).
+__device__ bool sel_skip(const int* err, SelShared& S) {
+  cg::cluster_group cl = cg::this_cluster();
+  if (threadIdx.x == 0) S.skip = est_failed(err);
+  cl.sync();
+  int any = 0;
+  for (int r = 0; r < kSelCluster; ++r) any |= *cl.map_shared_rank(&S.skip, r);
+  cl.sync();
+  return any != 0;
+}
+
+// The k-th largest key (k >= 1) of the cluster's list and how many of its
+// copies belong to the k largest (ties to the lower index).
+__device__ void sel_kth(const uint32_t* x, int lo, int hi, int k, SelShared& S, uint32_t& kth, int& take) {
+  cg::cluster_group cl = cg::this_cluster();
+  uint32_t prefix = 0;
+  int want = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass, b = pass & 1;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) S.cnt[b][i] = 0;
     __syncthreads();
-    const uint32_t prefix = s_prefix;
-    const uint32_t hi_mask = (shift == 24) ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const uint32_t hi_mask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
       const uint32_t v = x[i];
-      if ((v & hi_mask) == prefix) atomicAdd(&hist[(v >> shift) & 255], 1);
+      if ((v & hi_mask) == prefix) atomicAdd(&S.cnt[b][(v >> shift) & 255], 1);
+    }
+    cl.sync();
+    if (threadIdx.x < 256) {
+      int m = 0;
+      for (int r = 0; r < kSelCluster; ++r) m += cl.map_shared_rank(&S.cnt[b][0], r)[threadIdx.x];
+      S.mcnt[threadIdx.x] = m;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      int want = s_want, cum = 0, sel = 0;
+      int cum = 0, sel = 0;
       for (int bin = 255; bin >= 0; --bin) {
-        if (cum + hist[bin] >= want) {
+        if (cum + S.mcnt[bin] >= want) {
           sel = bin;
           break;
         }
-        cum += hist[bin];
+        cum += S.mcnt[bin];
       }
-      s_want = want - cum;
-      s_prefix = prefix | (uint32_t(sel) << shift);
+      S.want = uint64_t(want - cum);
+      S.prefix = prefix | (uint32_t(sel) << shift);
     }
     __syncthreads();
+    prefix = uint32_t(S.prefix);
+    want = int(S.want);
+    __syncthreads();
   }
-  const uint32_t kth = s_prefix;
-  const int take_eq = s_want;
-  int eq_base = 0, out_base = 0;
-  for (int i0 = 0; i0 < N; i0 += blockDim.x) {
+  kth = prefix;
+  take = want;
+}
+
+// Index-ordered compaction of the k largest (keys above kth, then the first
+// `take` copies of kth): out[j * stride + i] for every copy j < rep.
+__device__ void sel_compact(const uint32_t* x, int lo, int hi, uint32_t kth, int take, int k, int32_t* out,
+                            int rep, int stride, SelShared& S) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = int(cl.block_rank());
+  if (threadIdx.x == 0) S.n_gt = S.n_eq = 0;
+  __syncthreads();
+  int gt = 0, eq = 0;
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const uint32_t v = x[i];
+    gt += v > kth;
+    eq += v == kth;
+  }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&S.n_gt, gt);
+    atomicAdd(&S.n_eq, eq);
+  }
+  cl.sync();
+  int gt_before = 0, eq_before = 0;
+  for (int r = 0; r < rank; ++r) {
+    gt_before += *cl.map_shared_rank(&S.n_gt, r);
+    eq_before += *cl.map_shared_rank(&S.n_eq, r);
+  }
+  int eq_base = eq_before, out_base = gt_before + min(eq_before, take);
+  for (int i0 = lo; i0 < hi; i0 += blockDim.x) {
     const int i = i0 + threadIdx.x;
-    const uint32_t v = (i < N) ? x[i] : 0u;
-    const int is_eq = (i < N && v == kth) ? 1 : 0;
+    const uint32_t v = (i < hi) ? x[i] : 0u;
+    const int is_eq = (i < hi && v == kth) ? 1 : 0;
     int tot;
-    const int eq_incl = block_scan(is_eq, wsum, &tot);
-    const int sel = (i < N) && (v > kth || (is_eq && eq_base + eq_incl - 1 < take_eq));
+    const int eq_incl = block_scan(is_eq, S.wsum, &tot);
+    const int sel = (i < hi) && (v > kth || (is_eq && eq_base + eq_incl - 1 < take));
     eq_base += tot;
     int tot2;
-    const int pos = block_scan(sel, wsum, &tot2);
-    if (sel && out_base + pos - 1 < k) out[out_base + pos - 1] = i;
+    const int pos = block_scan(sel, S.wsum, &tot2);
+    if (sel && out_base + pos - 1 < k)
+      for (int j = 0; j < rep; ++j) out[int64_t(j) * stride + out_base + pos - 1] = i;
     out_base += tot2;
   }
 }
@@ -509,20 +589,28 @@ struct TopkParams {
   const int* err;      // status word: a recorded failure skips the selection
 };
 
-__global__ void __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
-  __shared__ int skip;
-  if (threadIdx.x == 0) skip = est_failed(p.err);
-  __syncthreads();
-  if (skip) return;
-  const int l = blockIdx.x, which = blockIdx.y;
+// Grid (lists x kSelCluster, 2): one cluster per list; y = 0 the vertical
+// lists, y = 1 the slash lists.  Radix select of the k-th largest score (the
+// bit patterns of nonnegative floats order like their values), then the
+// index-ordered compaction: the k largest scores' indices, ties to the lower
+// index, ascending.
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kTopkThreads) est_topk(const TopkParams p) {
+  __shared__ SelShared S;
+  if (sel_skip(p.err, S)) return;
+  cg::cluster_group cl = cg::this_cluster();
+  const int l = int(blockIdx.x) / kSelCluster, which = blockIdx.y;
   const uint32_t* x = reinterpret_cast<const uint32_t*>(which == 0 ? p.score : p.score2) + int64_t(l) * p.N;
   const int k = which == 0 ? p.k : p.k2;
   int32_t* out = (which == 0 ? p.out : p.out2) + int64_t(l) * p.rep * k;
-  topk_block(x, p.N, k, out, k);
-  if (p.rep > 1) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < (p.rep - 1) * k; i += blockDim.x) out[k + i] = out[i % k];
+  int lo, hi;
+  sel_chunk(p.N, int(cl.block_rank()), lo, hi);
+  if (k > 0) {
+    uint32_t kth;
+    int take;
+    sel_kth(x, lo, hi, k, S, kth, take);
+    sel_compact(x, lo, hi, kth, take, k, out, p.rep, k, S);
   }
+  cl.sync();  // peers may still read this CTA's counts
 }
 
 // Per-KV-group sums of the heads' scores, added in head order (fp32), for
@@ -575,17 +663,8 @@ struct ToppParams {
   double pv, ps;
 };
 
-struct ToppShared {
-  int cnt[256];
-  uint64_t sum[256];
-  uint64_t red[32];
-  uint64_t prefix, want;
-  int above, bad, k;
-  int skip;
-};
-
 // Saturating block sum of one value per thread (values <= 2^62).
-__device__ uint64_t block_sum_sat(uint64_t x, ToppShared& S) {
+__device__ uint64_t block_sum_sat(uint64_t x, SelShared& S) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x = sat_add(x, __shfl_xor_sync(0xffffffffu, x, off));
@@ -597,86 +676,101 @@ __device__ uint64_t block_sum_sat(uint64_t x, ToppShared& S) {
   return t;
 }
 
-// Smallest k in [0, n] with (sum of the k largest units) >= t, for t >= 1 and
-// t <= total.  Keys order the elements like their units: POOLED keys are the
-// units (< 2^53) themselves, otherwise fp32 score bits.
+// Smallest k in [0, n] with (sum of the k largest units of the cluster's
+// list) >= t, for t >= 1 and t <= total.  This CTA holds keys [lo, hi) of
+// x (fp32 score bits) or, POOLED, pooled[0, hi - lo) (the units, < 2^53,
+// themselves); keys order the elements like their units.
 template <bool POOLED>
-__device__ int topp_count(const uint32_t* x, const uint64_t* pooled, int n, uint64_t t, ToppShared& S) {
-  if (threadIdx.x == 0) {
-    S.prefix = 0;
-    S.want = t;
-    S.above = 0;
-  }
-  for (int shift = POOLED ? 48 : 24; shift >= 0; shift -= 8) {
+__device__ int topp_count(const uint32_t* x, const uint64_t* pooled, int lo, int hi, int n, uint64_t t,
+                          SelShared& S) {
+  cg::cluster_group cl = cg::this_cluster();
+  uint64_t prefix = 0, want = t;
+  int above = 0;
+  for (int pass = 0, shift = POOLED ? 48 : 24; shift >= 0; ++pass, shift -= 8) {
+    const int b = pass & 1;
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-      S.cnt[i] = 0;
-      S.sum[i] = 0;
+      S.cnt[b][i] = 0;
+      S.sum[b][i] = 0;
     }
     __syncthreads();
-    const uint64_t hi = S.prefix >> (shift + 8);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint64_t key = POOLED ? pooled[i] : uint64_t(x[i]);
-      if ((key >> (shift + 8)) == hi) {
+    const uint64_t hi_key = prefix >> (shift + 8);
+    for (int i = threadIdx.x; i < hi - lo; i += blockDim.x) {
+      const uint64_t key = POOLED ? pooled[i] : uint64_t(x[lo + i]);
+      if ((key >> (shift + 8)) == hi_key) {
         const int dgt = int((key >> shift) & 255);
-        atomicAdd(&S.cnt[dgt], 1);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&S.sum[dgt]),
-                  static_cast<unsigned long long>(POOLED ? key : mass_unit(__uint_as_float(uint32_t(key)))));
+        atomicAdd(&S.cnt[b][dgt], 1);
+        atomicAdd(&S.sum[b][dgt], static_cast<unsigned long long>(POOLED ? key : mass_unit(__uint_as_float(uint32_t(key)))));
       }
+    }
+    cl.sync();
+    if (threadIdx.x < 256) {
+      int m = 0;
+      unsigned long long u = 0;  // below 2^53: the list's total is
+      for (int r = 0; r < kSelCluster; ++r) {
+        m += cl.map_shared_rank(&S.cnt[b][0], r)[threadIdx.x];
+        u += cl.map_shared_rank(&S.sum[b][0], r)[threadIdx.x];
+      }
+      S.mcnt[threadIdx.x] = m;
+      S.msum[threadIdx.x] = u;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      const uint64_t want = S.want;
       uint64_t cum = 0;
-      int above = 0, sel = 0;
+      int ab = 0, sel = 0;
       for (int bin = 255; bin >= 0; --bin) {
-        if (cum + S.sum[bin] >= want) {
+        if (cum + S.msum[bin] >= want) {
           sel = bin;
           break;
         }
-        cum += S.sum[bin];
-        above += S.cnt[bin];
+        cum += S.msum[bin];
+        ab += S.mcnt[bin];
       }
       S.want = want - cum;  // > 0: the bins above sum to less than want
-      S.above += above;
-      S.prefix |= uint64_t(sel) << shift;
+      S.above = above + ab;
+      S.prefix = prefix | (uint64_t(sel) << shift);
     }
     __syncthreads();
+    prefix = S.prefix;
+    want = S.want;
+    above = S.above;
+    __syncthreads();
   }
-  // the k-th largest has key S.prefix; the smallest j with j * u >= want of
+  // the k-th largest has key `prefix`; the smallest j with j * u >= want of
   // its copies completes the budget
-  const uint64_t u = POOLED ? S.prefix : mass_unit(__uint_as_float(uint32_t(S.prefix)));
-  const int k = S.above + (u ? int((S.want + u - 1) / u) : 0);
-  __syncthreads();
+  const uint64_t u = POOLED ? prefix : mass_unit(__uint_as_float(uint32_t(prefix)));
+  const int k = above + (u ? int((want + u - 1) / u) : 0);
   return k < n ? k : n;
 }
 
-// Grid (BH, 2): y = 0 the vertical list, y = 1 the slash list.  Dynamic
-// shared memory: the pooled slash units, one per 64-offset block.
-__global__ void __launch_bounds__(kTopkThreads) est_topp(const ToppParams p) {
+// Grid (BH x kSelCluster, 2): one cluster per list; y = 0 the vertical list,
+// y = 1 the slash list.  Dynamic shared memory: the pooled slash units of
+// this CTA's chunk, one per 64-offset block.
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kTopkThreads) est_topp(const ToppParams p) {
   extern __shared__ __align__(16) uint64_t pooled[];
-  __shared__ ToppShared S;
-  const int bh = blockIdx.x, which = blockIdx.y;
+  __shared__ SelShared S;
+  if (sel_skip(p.err, S)) return;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = int(cl.block_rank());
+  const int bh = int(blockIdx.x) / kSelCluster, which = blockIdx.y;
   const int N = p.N;
   const float* xf = (which == 0 ? p.v : p.s) + int64_t(bh) * N;
   const uint32_t* x = reinterpret_cast<const uint32_t*>(xf);
-  if (threadIdx.x == 0) {
-    S.bad = 0;
-    S.skip = est_failed(p.err);
-  }
+  int lo, hi;
+  sel_chunk(N, rank, lo, hi);
+  if (threadIdx.x == 0) S.bad = 0;
   __syncthreads();
-  if (S.skip) return;
   // 1. validate, total mass; the slash list is pooled per 64-offset block
   uint64_t mine = 0;
   int bad = 0;
   if (which == 0) {
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
       const float f = xf[i];
       if (!(f >= 0.f && f < 8192.f)) bad = 1;
       else mine = sat_add(mine, mass_unit(f));
     }
   } else {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int b = w; b < N / 64; b += nw) {
+    for (int b = lo / 64 + w; b < hi / 64; b += nw) {
       uint64_t u = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -686,31 +780,53 @@ __global__ void __launch_bounds__(kTopkThreads) est_topp(const ToppParams p) {
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) u = sat_add(u, __shfl_xor_sync(0xffffffffu, u, off));
-      if (lane == 0) pooled[b] = u;
+      if (lane == 0) pooled[b - lo / 64] = u;
       mine = sat_add(mine, lane == 0 ? u : 0ull);
     }
   }
   if (bad) S.bad = 1;
-  const uint64_t T = block_sum_sat(mine, S);  // its syncs also publish S.bad and pooled[]
-  const bool ok = !S.bad && T < kUnitTotalMax;
-  // 2. budget
+  const uint64_t part = block_sum_sat(mine, S);  // its syncs also publish S.bad and pooled[]
+  if (threadIdx.x == 0) S.part = part;
+  cl.sync();
+  uint64_t T = 0;
+  int any_bad = 0;
+  for (int r = 0; r < kSelCluster; ++r) {
+    T = sat_add(T, *cl.map_shared_rank(&S.part, r));
+    any_bad |= *cl.map_shared_rank(&S.bad, r);
+  }
+  const bool ok = !any_bad && T < kUnitTotalMax;
+  // 2. budget (the same in every CTA of the cluster)
   int k = 0;
   if (ok) {
     const double prod = (which == 0 ? p.pv : p.ps) * double(T);
     const uint64_t t = uint64_t(ceil(prod));
-    if (t > 0) k = which == 0 ? topp_count<false>(x, nullptr, N, t, S) : topp_count<true>(nullptr, pooled, N / 64, t, S);
-  } else if (threadIdx.x == 0) {
+    if (t > 0)
+      k = which == 0 ? topp_count<false>(x, nullptr, lo, hi, N, t, S)
+                     : topp_count<true>(nullptr, pooled, lo / 64, hi / 64, N / 64, t, S);
+  } else if (rank == 0 && threadIdx.x == 0) {
     raise_error(p.err, VS_ERR_SCORE);
   }
   const int cap = which == 0 ? p.kv_max : p.ks_max;
   if (which == 1) k = min(64 * k, N);
   k = min(k, cap);
-  if (threadIdx.x == 0) (which == 0 ? p.kv : p.ks)[bh] = k;
+  if (rank == 0 && threadIdx.x == 0) (which == 0 ? p.kv : p.ks)[bh] = k;
   // 3. the k largest at token level, padded to the list capacity
-  topk_block(x, N, k, (which == 0 ? p.v_idx : p.s_idx) + int64_t(bh) * cap, cap);
+  int32_t* out = (which == 0 ? p.v_idx : p.s_idx) + int64_t(bh) * cap;
+  for (int i = k + rank * int(blockDim.x) + threadIdx.x; i < cap; i += kSelCluster * int(blockDim.x)) out[i] = -1;
+  if (k > 0) {
+    uint32_t kth;
+    int take;
+    sel_kth(x, lo, hi, k, S, kth, take);
+    sel_compact(x, lo, hi, kth, take, k, out, 1, cap, S);
+  }
+  cl.sync();  // peers may still read this CTA's counts
 }
 
-size_t topp_smem_bytes(int N) { return size_t(N / 64) * sizeof(uint64_t); }
+// Pooled slash units of one CTA's chunk.
+size_t topp_smem_bytes(int N) {
+  const int nb = N / 64;
+  return size_t((nb + kSelCluster - 1) / kSelCluster) * sizeof(uint64_t);
+}
 
 vs_status launch_topp(const ToppParams& tp, int BH, cudaStream_t st) {
   const size_t sm = topp_smem_bytes(tp.N);
@@ -718,7 +834,7 @@ vs_status launch_topp(const ToppParams& tp, int BH, cudaStream_t st) {
   if (cudaFuncSetAttribute(est_topp, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sm)) != cudaSuccess)
     return VS_ERR_CUDA;
   trace_begin("est_topp", st);
-  est_topp<<<dim3(BH, 2), kTopkThreads, sm, st>>>(tp);
+  est_topp<<<dim3(BH * kSelCluster, 2), kTopkThreads, sm, st>>>(tp);
   trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
@@ -780,7 +896,7 @@ vs_status launch_est_kernels(const vs_shape* s, const void* q, const void* k, Es
     lists = BHK;
   }
   trace_begin("est_topk", st);
-  est_topk<<<dim3(lists, 2), kTopkThreads, 0, st>>>(tp);
+  est_topk<<<dim3(lists * kSelCluster, 2), kTopkThreads, 0, st>>>(tp);
   trace_end(st);
   note_launch(5);
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
@@ -803,7 +919,7 @@ EstParams est_params(const vs_shape* s, float scale, int* err) {
 
 vs_status launch_est(const vs_shape* s, const void* q, const void* k, EstParams& p, int kv, int ks, int32_t* v_idx,
                      int32_t* s_idx, cudaStream_t st, ToppParams* topp = nullptr) {
-  if (topp && topp_smem_bytes(s->Nk) > kToppMaxSmem) return VS_ERR_SHAPE;
+  if (topp && size_t(s->Nk) > topp_max_n()) return VS_ERR_SHAPE;
   if (s->d == 128) return launch_est_kernels<128>(s, q, k, p, kv, ks, v_idx, s_idx, topp, st);
   if (s->d == 64) return launch_est_kernels<64>(s, q, k, p, kv, ks, v_idx, s_idx, topp, st);
   return VS_ERR_SHAPE;
