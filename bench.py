@@ -202,6 +202,37 @@ def mask_entries(iv: np.ndarray, is_: np.ndarray, N: int) -> np.ndarray:
     return out
 
 
+def block_mask_entries(iv: np.ndarray, is_: np.ndarray, N: int) -> np.ndarray:
+    """|M| per head of the block-cover mask M[n, m] = (m <= n) and (m in iv or
+    block diagonal D = floor(n/64) - floor(m/64) is active), D active iff a
+    selected offset o has |o - 64 D| <= 63, for N a multiple of 64, in closed
+    form: 2080 causal entries per diagonal block and 4096 per block of an
+    active diagonal D >= 1 (N/64 - D of them), plus, per selected column m in
+    block J, its causal rows on inactive diagonals (64 - m mod 64 in block J,
+    64 in every later block).  int64 [B, H]."""
+    assert N % 64 == 0
+    nb = N // 64
+    B, H = iv.shape[:2]
+    out = np.zeros((B, H), np.int64)
+    D = np.arange(nb, dtype=np.int64)
+    for b in range(B):
+        for h in range(H):
+            offs = np.unique(is_[b, h][is_[b, h] >= 0].astype(np.int64))
+            act = np.zeros(nb, bool)
+            for dd in (0, 1):  # |o - 64 D| <= 63 holds for D = floor(o/64) and, if 64 does not divide o, the next
+                c = offs // 64 + dd
+                ok = (c < nb) & (np.abs(offs - 64 * c) <= 63)
+                act[c[ok]] = True
+            area = (2080 * nb if act[0] else 0) + int((4096 * (nb - D[1:]))[act[1:]].sum())
+            inact = (~act).astype(np.int64)
+            cum = np.cumsum(inact)  # cum[t] = inactive diagonals among 0..t
+            cols = np.unique(iv[b, h][iv[b, h] >= 0].astype(np.int64))
+            J = cols // 64
+            area += int((inact[0] * (64 - cols % 64) + 64 * (cum[nb - 1 - J] - cum[0])).sum())
+            out[b, h] = area
+    return out
+
+
 def step_flops(units_q: np.ndarray, entries: np.ndarray, B: int, N: int, Hq: int, d: int) -> dict:
     """Executed (query-major cover, 4 d + 10 d per covered entry), algorithmic
     (the same per entry of the exact mask, MagiAttention's cost = mask area)
@@ -505,7 +536,14 @@ def _accounting(attn, counts, w):
     import dynamic_vertical_slash_gb300 as vs
 
     if attn.block_cover:
-        return None
+        # the block-cover mask: its area from the host's closed form
+        iv, is_ = attn.v_idx.cpu().numpy(), attn.s_idx.cpu().numpy()
+        per_head = block_mask_entries(iv, is_, w.N)
+        gpu_u = np.asarray(counts).reshape(w.B, w.Hq, 4)[..., :2]
+        fl = step_flops(gpu_u, per_head, w.B, w.N, w.Hq, w.d)
+        return {"algorithmic_per_step": fl["algorithmic"], "mask_entries": int(per_head.sum()),
+                "mask_density": fl["mask_density"], "mask_entries_source": "host closed form of the block-cover mask",
+                "executed_over_algorithmic": fl["executed"] / fl["algorithmic"] if fl["algorithmic"] else None}
     per_head = np.zeros((w.B, w.Hq), np.int64)
     for b in range(w.B):
         for h in range(w.Hq):

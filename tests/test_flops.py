@@ -98,3 +98,22 @@ def test_mask_entries_closed_form_against_the_oracle():
     for h in range(H):
         assert got[0, h] == int(oracle.mask_dense(p, 0, h).sum())
     assert got.sum() == oracle.mask_count(p)
+
+
+def test_block_mask_entries_closed_form_against_the_oracle():
+    import oracle
+
+    rng = np.random.default_rng(10)
+    N, H = 640, 3
+    iv = np.stack([np.sort(rng.choice(N, 24, replace=False)) for _ in range(H)])[None].astype(np.int32)
+    is_ = np.stack([np.sort(rng.choice(N, 5, replace=False)) for _ in range(H)])[None].astype(np.int32)
+    is_[0, 2, :] = [0, 64, 65, 300, 639]  # offsets on and between block multiples
+    iv[0, 1, -3:] = -1  # a padded list
+    iv[0, 1, :-3] = np.sort(rng.choice(N, 21, replace=False))
+    p = oracle.Problem(np.zeros((1, N, H, 1)), np.zeros((1, N, 1, 1)), np.zeros((1, N, 1, 1)), iv, is_, 1.0, block=True)
+    got = _bench().block_mask_entries(iv, is_, N)
+    for h in range(H):
+        assert got[0, h] == int(oracle.mask_dense(p, 0, h).sum())
+    # every offset selected: the whole causal area
+    full = _bench().block_mask_entries(iv, np.arange(N, dtype=np.int32)[None, None].repeat(H, 1), N)
+    assert (full == N * (N + 1) // 2).all()
