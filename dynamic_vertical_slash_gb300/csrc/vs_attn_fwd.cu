@@ -121,13 +121,28 @@ struct FwdParams {
 };
 
 // The order in which the MMA consumes K / V blocks (and the loader fills the
-// slot ring): K0, K1, then per pair i: V_i, K_{i+2}.
+// slot ring): K0, K1, then per pair i: V_i, K_{i+2}.  One loop with one call
+// of f, so that its body is emitted once per warp role (the roles' loops
+// share the SM's instruction cache).
 template <typename F>
 __device__ __forceinline__ void for_each_block(int P, F&& f) {
-  for (int j = 0; j < kSBufs && j < P; ++j) f(0, j);
-  for (int i = 0; i < P; ++i) {
-    f(1, i);
-    if (i + kSBufs < P) f(0, i + kSBufs);
+  const int head = P < kSBufs ? P : kSBufs;  // K blocks before the first V
+  const int mid = P > kSBufs ? P - kSBufs : 0;  // pairs followed by a K block
+#pragma unroll 1
+  for (int c = 0; c < 2 * P; ++c) {
+    int kind, i;
+    if (c < head) {
+      kind = 0;
+      i = c;
+    } else if (c - head < 2 * mid) {
+      const int e = c - head;
+      kind = (e & 1) ? 0 : 1;
+      i = (e >> 1) + ((e & 1) ? kSBufs : 0);
+    } else {
+      kind = 1;
+      i = mid + (c - head - 2 * mid);
+    }
+    f(kind, i);
   }
 }
 
