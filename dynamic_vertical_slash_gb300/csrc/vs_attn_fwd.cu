@@ -461,6 +461,13 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
     if (P > 0) {
       const uint32_t idS = idesc_bf16(128, kPairKeys, 0, 0);
       const uint32_t idO = idesc_bf16(128, D, 0, 1);
+      // descriptors of slot 0 as a K block (K-major) and as a V block
+      // (MN-major); another slot's and K-chunk's are these plus the offset
+      // (shared addresses stay below 256 KB: the 14-bit start field never
+      // carries)
+      const uint64_t dk0 = sdesc_sw128(smem_u32(s.slot[0][0]), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(s.slot[0][0]), kPairKeys * 128, 1024);
+      constexpr uint32_t kSlotDesc = uint32_t(NH * kPairKeys * 128) >> 4;
       bool ok = mbar_wait_warp(&s.q_tmem, 0, ab, VS_ERR_TIMEOUT);
       int c = 0;
       for_each_block(P, [&](int kind, int i) {
@@ -474,18 +481,20 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         if (gathered(i)) fence_proxy_async_smem();
         tc_fence_after();
         if (!kind) {
+          const uint64_t dks = dk0 + uint64_t(sl) * kSlotDesc;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t db = sdesc_sw128(smem_u32(s.slot[sl][kk / 4]) + (kk % 4) * 32, 16, 1024);
-            mma_ts_warp(tmem + kColS + 128 * j, tmem + kColQ + kk * 8, db, idS, kk > 0);  // A = Q in TMEM
+            const uint32_t o = uint32_t((kk / 4) * (kPairKeys * 128) + (kk % 4) * 32) >> 4;
+            mma_ts_warp(tmem + kColS + 128 * j, tmem + kColQ + kk * 8, dks + o, idS, kk > 0);  // A = Q in TMEM
           }
           mma_commit_warp(&s.s_full[j]);
         } else {
           const int nk = (2 * i + 1 < U) ? kPairKeys / 16 : kKTile / 16;
+          const uint64_t dvs = dv0 + uint64_t(sl) * kSlotDesc;
 #pragma unroll
           for (int kk = 0; kk < kPairKeys / 16; ++kk) {
             if (kk >= nk) break;
-            const uint64_t dv = sdesc_sw128(smem_u32(s.slot[sl][0]) + kk * 2048, kPairKeys * 128, 1024);
+            const uint64_t dv = dvs + uint32_t(kk * 2048 >> 4);
             const uint32_t a_p = tmem + kColP + (kk >> 2) * 32 + (kk & 3) * 8;  // P of unit kk / 4
             mma_ts_warp(tmem + kColO, a_p, dv, idO, (i > 0 || kk > 0));
           }
