@@ -349,14 +349,18 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
         if (i >= 1 && !(ok = mbar_wait_warp(&s.s_free, (i - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         if (gathered(i)) fence_proxy_async_smem();
         tc_fence_after();
+        // a K-chunk's descriptor is the slot's plus its offset (shared
+        // addresses stay below 256 KB: the 14-bit start field never carries)
+        const uint64_t dks = sdesc_sw128(smem_u32(s.k[ks][0]), 16, 1024);
+        const uint64_t dvs = sdesc_sw128(smem_u32(s.v[vsl][0]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][kk / 4]) + (kk % 4) * 32, 16, 1024);
+          const uint64_t dk_ = dks + (uint32_t((kk / 4) * kDqPairKeys * 128 + (kk % 4) * 32) >> 4);
           mma_ts_warp(tmem + kDqColS, tmem + kDqColQ + kk * 8, dk_, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t dv_ = sdesc_sw128(smem_u32(s.v[vsl][kk / 4]) + (kk % 4) * 32, 16, 1024);
+          const uint64_t dv_ = dvs + (uint32_t((kk / 4) * kDqPairKeys * 128 + (kk % 4) * 32) >> 4);
           mma_ts_warp(tmem + kDqColDP, tmem + kDqColDO + kk * 8, dv_, idS, kk > 0);
         }
         mma_commit_warp(&s.s_full);
@@ -370,6 +374,7 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
     // keys (K stays in its slot until then).
     if (P > 0) {
       const uint32_t idQ = idesc_bf16(128, D, 0, 1);
+      const uint64_t dds = sdesc_sw128(smem_u32(s.ds[0]), 16, 1024);
       bool ok = true;
       for (int i = 0; ok && i < P; ++i) {
         if (!(ok = mbar_wait_warp(&s.ds_full, i & 1, ab, VS_ERR_TIMEOUT))) break;
@@ -377,11 +382,12 @@ __device__ __forceinline__ void dq_body(const CUtensorMap& tmK, const CUtensorMa
         tc_fence_after();
         const int ks = i % kDqKSlots;
         const int nk = (2 * i + 1 < U) ? kDqPairKeys / 16 : kKTile / 16;
+        const uint64_t dkm = sdesc_sw128(smem_u32(s.k[ks][0]), kDqPairKeys * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kDqPairKeys / 16; ++kk) {
           if (kk >= nk) break;
-          const uint64_t da = sdesc_sw128(smem_u32(s.ds[kk / 4]) + (kk % 4) * 32, 16, 1024);
-          const uint64_t dk_ = sdesc_sw128(smem_u32(s.k[ks][0]) + kk * 2048, kDqPairKeys * 128, 1024);
+          const uint64_t da = dds + (uint32_t((kk / 4) * kQTile * 128 + (kk % 4) * 32) >> 4);
+          const uint64_t dk_ = dkm + uint32_t(kk * 2048 >> 4);
           mma_ss_warp(tmem + kDqColAcc, da, dk_, idQ, (i > 0 || kk > 0));
         }
         mma_commit_warp(&s.ds_done);
@@ -853,6 +859,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     if (run) {
       const bool is_s = warp == kKvWarpS;
       const uint32_t idS = idesc_bf16(128, kRowTile, 0, 0);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(s.v[0]), 16, 1024);
       bool ok = is_s ? mbar_wait_warp(&s.k_tmem, 0, ab, VS_ERR_TIMEOUT) : mbar_wait_warp(&s.kv_full, 0, ab, VS_ERR_TIMEOUT);
       if (ok && BAR && !is_s) fence_proxy_async_smem();
       for (int j = 0; ok && j < U; ++j) {
@@ -860,18 +867,22 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
         if (!(ok = mbar_wait_warp(&s.st_full[st], (j / kBwdStages) & 1, ab, VS_ERR_TIMEOUT))) break;
         if (j >= 1 && !(ok = mbar_wait_warp(&s.s_free, (j - 1) & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
+        // a K-chunk's descriptor is the stage's plus its offset (shared
+        // addresses stay below 256 KB: the 14-bit start field never carries)
         if (is_s) {
+          const uint64_t dqs = sdesc_sw128(smem_u32(s.q[st][0]), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dq_ = dqs + (uint32_t((kk / 4) * kRowTile * 128 + (kk % 4) * 32) >> 4);
             mma_ts_warp(tmem + kKvColS, tmem + kKvColK + kk * 8, dq_, idS, kk > 0);
           }
           mma_commit_warp(&s.s_full);
         } else {
+          const uint64_t dgs = sdesc_sw128(smem_u32(s.g[st][0]), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t dva = sdesc_sw128(smem_u32(s.v[kk / 4]) + (kk % 4) * 32, 16, 1024);
-            const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][kk / 4]) + (kk % 4) * 32, 16, 1024);
+            const uint64_t dva = dv0 + (uint32_t((kk / 4) * kBarK * 128 + (kk % 4) * 32) >> 4);
+            const uint64_t dg_ = dgs + (uint32_t((kk / 4) * kRowTile * 128 + (kk % 4) * 32) >> 4);
             mma_ss_warp(tmem + kKvColDP, dva, dg_, idS, kk > 0);
           }
           mma_commit_warp(&s.sd_full);
@@ -891,10 +902,12 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
         const int st = j % kBwdStages;
         if (!(ok = mbar_wait_warp(&s.p_full, j & 1, ab, VS_ERR_TIMEOUT))) break;
         tc_fence_after();
+        const uint64_t dgm = sdesc_sw128(smem_u32(s.g[st][0]), kRowTile * 128, 1024);
+        const uint64_t dqm = sdesc_sw128(smem_u32(s.q[st][0]), kRowTile * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kRowTile / 16; ++kk) {
-          const uint64_t dg_ = sdesc_sw128(smem_u32(s.g[st][0]) + kk * 2048, kRowTile * 128, 1024);
-          const uint64_t dq_ = sdesc_sw128(smem_u32(s.q[st][0]) + kk * 2048, kRowTile * 128, 1024);
+          const uint64_t dg_ = dgm + uint32_t(kk * 2048 >> 4);
+          const uint64_t dq_ = dqm + uint32_t(kk * 2048 >> 4);
           mma_ts_warp(tmem + kKvColDV, tmem + kKvColP + kk * 8, dg_, idG, (j > 0 || kk > 0));
           mma_ts_warp(tmem + kKvColDK, tmem + kKvColDS + kk * 8, dq_, idG, (j > 0 || kk > 0));
         }
