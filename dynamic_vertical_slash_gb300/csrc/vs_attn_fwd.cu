@@ -545,19 +545,30 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
       tc_fence_before();
       mbar_arrive(&s.q_tmem);
     }
-    for (int i = 0; i < P; ++i) {
-      const int ri = i % kRecRing, j = i % kSBufs;
-      const uint32_t colS = kColS + 128 * j + 64 * half;  // this unit's scores
-      // the unit's row mask first: the record is published ahead of the
-      // scores, so cutting the mask overlaps the S MMAs
-      ok = mbar_wait(&s.rec_full[ri], (i / kRecRing) & 1, ab, VS_ERR_TIMEOUT);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
+    // A unit's row mask is cut from its record (published well ahead) one
+    // pair early: the mask of pair i + 1 while the scores of pair i are on
+    // their way from TMEM, so the record's shared-memory latency is hidden.
+    bool rec_ok = true;
+    auto cut_mask = [&](int i2) {
+      const int ri2 = i2 % kRecRing;
+      rec_ok = mbar_wait(&s.rec_full[ri2], (i2 / kRecRing) & 1, ab, VS_ERR_TIMEOUT);
+      uint64_t m = 0ull;
+      if (rec_ok && row_ok) {
+        const MaskRec& rc = s.rec[ri2][half];
+        m = rec_row_mask<BLOCK>(rc, rc.kind, ti, n_g);
       }
-      const MaskRec& rc = s.rec[ri][half];
-      const uint64_t mask = row_ok ? rec_row_mask<BLOCK>(rc, rc.kind, ti, n_g) : 0ull;
-      mbar_arrive(&s.rec_empty[ri]);
+      mbar_arrive(&s.rec_empty[ri2]);
+      return m;
+    };
+    uint64_t mask_nx = 0ull;
+    if (P > 0) {
+      mask_nx = cut_mask(0);
+      ok = __all_sync(0xffffffffu, rec_ok);
+    }
+    for (int i = 0; ok && i < P; ++i) {
+      const int j = i % kSBufs;
+      const uint32_t colS = kColS + 128 * j + 64 * half;  // this unit's scores
+      const uint64_t mask = mask_nx;
       ok = mbar_wait(&s.s_full[j], (i / kSBufs) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -570,7 +581,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
       // single entry, so P stays <= 2^64.
       uint32_t pk[32];
       float unit_sum;
-      auto make_p = [&](float ref) {
+      auto make_p = [&](float ref, bool next_mask) {
         // two keys at a time in paired fp32: t = S scale log2(e) - ref, and
         // four pairs of partial row sums
         uint64_t ps2[4];
@@ -580,7 +591,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         uint32_t sr[64];
         tmem_ld32(tl + colS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         tmem_ld32(tl + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld_wait();
+        if (next_mask) mask_nx = cut_mask(i + 1);
+        tmem_ld_wait_dep(*reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        reg_dep(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         const uint32_t mlo = uint32_t(mask), mhi = uint32_t(mask >> 32);
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
@@ -604,7 +617,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
       // SM's instruction cache): a second pass only after a re-basing
 #pragma unroll 1
       for (int pass = 0;; ++pass) {
-        make_p(m_run == -INFINITY ? 0.f : m_run);
+        make_p(m_run == -INFINITY ? 0.f : m_run, pass == 0 && i + 1 < P);
         if (pass) break;
         const bool need = (mask != 0ull) && (m_run == -INFINITY || !(unit_sum <= kRefSlack));
         // both threads of a row see the same decision
@@ -632,7 +645,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         }
         if (m_run == -INFINITY || grow) m_run = mt;
       }
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, ok && rec_ok)) {
+        ok = false;
+        break;
+      }
       // P's columns are free once PV_{i-1} has read them
       if (i > 0 && !mbar_wait(&s.pv_done[(i - 1) % kSBufs], ((i - 1) / kSBufs) & 1, ab, VS_ERR_TIMEOUT)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) break;
