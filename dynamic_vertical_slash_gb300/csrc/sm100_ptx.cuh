@@ -220,6 +220,22 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four MMAs of one chain (D += A_k B_k, k = 0..3, A in TMEM) issued by one
+// elected lane of a convergent warp from a single elect: the first
+// accumulates into D iff acc is nonzero, the other three always.
+__device__ __forceinline__ void mma_ts_chain4_warp(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                   uint32_t a3, uint64_t b0, uint64_t b1, uint64_t b2, uint64_t b3,
+                                                   uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t, e;\n setp.ne.b32 p, %10, 0;\n setp.eq.b32 t, %10, %10;\n"
+      " elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, t;\n}" ::"r"(d_tmem),
+      "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc), "r"(acc)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"

@@ -482,21 +482,25 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         tc_fence_after();
         if (!kind) {
           const uint64_t dks = dk0 + uint64_t(sl) * kSlotDesc;
+          // four K-chunks of 16 per elect; A = Q in TMEM
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = uint32_t((kk / 4) * (kPairKeys * 128) + (kk % 4) * 32) >> 4;
-            mma_ts_warp(tmem + kColS + 128 * j, tmem + kColQ + kk * 8, dks + o, idS, kk > 0);  // A = Q in TMEM
+          for (int k4 = 0; k4 < D / 64; ++k4) {
+            const uint64_t b = dks + (uint32_t(k4 * kPairKeys * 128) >> 4);
+            const uint32_t a = tmem + kColQ + k4 * 32;
+            mma_ts_chain4_warp(tmem + kColS + 128 * j, a, a + 8, a + 16, a + 24, b, b + 2, b + 4, b + 6, idS, k4 > 0);
           }
           mma_commit_warp(&s.s_full[j]);
         } else {
-          const int nk = (2 * i + 1 < U) ? kPairKeys / 16 : kKTile / 16;
           const uint64_t dvs = dv0 + uint64_t(sl) * kSlotDesc;
+          // per unit of the pair four K-chunks of 16 keys, one elect; A = P
+          // of the unit in TMEM (an odd last unit's second half is left out)
+          const int nu = (2 * i + 1 < U) ? 2 : 1;
 #pragma unroll
-          for (int kk = 0; kk < kPairKeys / 16; ++kk) {
-            if (kk >= nk) break;
-            const uint64_t dv = dvs + uint32_t(kk * 2048 >> 4);
-            const uint32_t a_p = tmem + kColP + (kk >> 2) * 32 + (kk & 3) * 8;  // P of unit kk / 4
-            mma_ts_warp(tmem + kColO, a_p, dv, idO, (i > 0 || kk > 0));
+          for (int u = 0; u < 2; ++u) {
+            if (u >= nu) break;
+            const uint64_t b = dvs + uint32_t(u * 4 * 2048 >> 4);
+            const uint32_t a = tmem + kColP + u * 32;
+            mma_ts_chain4_warp(tmem + kColO, a, a + 8, a + 16, a + 24, b, b + 128, b + 256, b + 384, idO, i > 0 || u > 0);
           }
           mma_commit_warp(&s.pv_done[j]);
         }
