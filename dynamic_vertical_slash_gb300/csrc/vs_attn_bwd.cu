@@ -985,21 +985,10 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
         }
       }
       const uint32_t hm = uint32_t(mask >> (32 * half));
-      float l2v[32], ddv[32];
-      const float4* l4 = reinterpret_cast<const float4*>(&s.l2[st][32 * half]);
-      const float4* d4 = reinterpret_cast<const float4*>(&s.dd[st][32 * half]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 a = l4[i], c = d4[i];
-        l2v[4 * i] = a.x;
-        l2v[4 * i + 1] = a.y;
-        l2v[4 * i + 2] = a.z;
-        l2v[4 * i + 3] = a.w;
-        ddv[4 * i] = c.x;
-        ddv[4 * i + 1] = c.y;
-        ddv[4 * i + 2] = c.z;
-        ddv[4 * i + 3] = c.w;
-      }
+      // the rows' -LSE log2(e) and D, read pair by pair inside the loop
+      // (broadcast shared-memory reads; fewer registers live at once)
+      const float2* l2p = reinterpret_cast<const float2*>(&s.l2[st][32 * half]);
+      const float2* ddp = reinterpret_cast<const float2*>(&s.dd[st][32 * half]);
       // two rows at a time in paired fp32: t = S^T scale log2(e) - LSE log2(e)
       // (the workspace holds -LSE log2(e)), P = 2^t on the mask, dS = P (dP - D)
       uint32_t pk[16], dk[16];
@@ -1008,14 +997,14 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
       for (int i = 0; i < 16; ++i) {
         const int c = 2 * i;
         float t0, t1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2,
-                         f2_pack(l2v[c], l2v[c + 1])),
-                  t0, t1);
+        const float2 lv = l2p[i], dv2 = ddp[i];
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, f2_pack(lv.x, lv.y)), t0,
+                  t1);
         const float x0 = ((hm >> c) & 1u) ? ex2(t0) : 0.f;  // one select: dS inherits the zero
         const float x1 = ((hm >> (c + 1)) & 1u) ? ex2(t1) : 0.f;
         float d0, d1;
         f2_unpack(f2_mul(f2_pack(x0, x1), f2_sub(f2_pack(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])),
-                                                  f2_pack(ddv[c], ddv[c + 1]))),
+                                                  f2_pack(dv2.x, dv2.y))),
                   d0, d1);
         pk[i] = pack_bf16x2(x0, x1);
         dk[i] = pack_bf16x2(d0, d1);
