@@ -929,6 +929,14 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
     const bool key_ok = run && kl >= 0 && kl < p.Nk;
     const int64_t m_g = key_ok ? kpos_g(G, kl) : 0;
     constexpr bool block_cover = BLOCK;
+    // slash: bit hh set iff head hk g + hh selected the key as a column (its
+    // rows are the bar kernel's); read once, the key is fixed per thread
+    uint64_t vsel = 0;
+    if (!BAR && key_ok)
+      for (int hh = 0; hh < G.g; ++hh) {
+        const int64_t bh = int64_t(b) * p.Hq + hk * G.g + hh;
+        vsel |= ((__ldg(av.vlocbits + bh * G.WL + (kl >> 6)) >> (kl & 63)) & 1ull) << hh;
+      }
     if (run) {
       // K row of key r, d columns [half D/2, (half + 1) D/2), into TMEM
       uint32_t w[D / 4];
@@ -978,8 +986,7 @@ __device__ __forceinline__ void kv_body(const CUtensorMap& tmK, const CUtensorMa
           else if (lim > 0) valid &= (~0ull) << lim;
           mask = valid;
         } else {
-          const uint64_t vw = __ldg(av.vlocbits + bh * G.WL + (kl >> 6));
-          if (!((vw >> (kl & 63)) & 1ull))
+          if (!((vsel >> (h - hk * G.g)) & 1ull))
             mask = block_cover ? block_col_mask(G, av.bdbits + bh * G.WG, kl, r0)
                                : slash_col_mask(G, av.offbits + bh * G.WG, kl, r0);
         }
