@@ -15,19 +15,21 @@
 // issues), warps 2-9 run the softmax: every pair goes through all eight, the
 // two warps of a TMEM lane quarter holding the same 32 rows, one the pair's
 // first unit and one its second.  fp32 online softmax on the exact token mask
-// in registers, P (bf16) into TMEM columns of its own.
+// in registers, P (bf16) over the first half of the unit's own score columns.
 //
-// TMEM columns: O [0, d), score buffers S_j [128 + 128 j, +128) for j < 2,
-// Q [384, 384 + d / 2) and P [448, 512) as bf16 pairs.  The softmax threads
+// TMEM columns: O [0, d), score buffers S_j [128 + 128 j, +128) for j < 2
+// (unit u's scores in [64 u, +64), then its P as bf16 pairs in [64 u, +32)),
+// Q [384, 384 + d / 2) as bf16 pairs; [448, 512) unused.  The softmax threads
 // write their row of Q there once per tile, so every S = Q K^T chain reads
 // its A operand from TMEM and only K from shared memory.  S of pair i goes to
 // buffer i % 2.  The MMA order is S0 S1, then per pair i: PV_i (once P_i is
-// stored), S_{i+2} into buffer i % 2, whose scores the softmax has read by
-// then: the scores of pair i + 1 are computed while pair i is in softmax.
-// P_i is stored once PV_{i-1} has read P_{i-1}.  The row's reference maximum
-// is lazy (it moves only for the row's first entries or an entry 2^64 above
-// it); the two threads of a row agree on it through a named barrier of their
-// two warps, and before O is rescaled every PV issued so far has completed.
+// stored), S_{i+2} into buffer i % 2 (the pipe runs them in order, so PV_i
+// has read P_i by then): the scores of pair i + 1 are computed while pair i
+// is in softmax.  P_i overwrites scores the softmax already holds, so it is
+// stored without waiting for any PV.  The row's reference maximum is lazy
+// (it moves only for the row's first entries or an entry 2^64 above it); the
+// two threads of a row agree on it through a named barrier of their two
+// warps, and before O is rescaled every PV issued so far has completed.
 //
 // Shared memory: a ring of slots that each hold K or V of one pair (128 rows),
 // filled and released in the MMA's order K0 K1 V0 K2 V1 K3 ..., and a ring of
@@ -46,7 +48,7 @@ constexpr int kPairKeys = 2 * kKTile;
 constexpr int kFwdSlots = 6;
 constexpr int kRecRing = 8;
 constexpr int kSBufs = 2;  // score buffers: S of pair i + 1 is computed while pair i is in softmax
-constexpr uint32_t kColO = 0, kColS = 128, kColQ = 128 + 128 * kSBufs, kColP = 448, kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 128, kColQ = 128 + 128 * kSBufs, kTmemCols = 512;
 constexpr float kRefSlack = 18446744073709551616.0f;  // 2^64: largest masked pair sum accepted against the reference
 
 // What a unit's 128 row masks are cut from (written by the loader).
@@ -499,7 +501,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
           for (int u = 0; u < 2; ++u) {
             if (u >= nu) break;
             const uint64_t b = dvs + uint32_t(u * 4 * 2048 >> 4);
-            const uint32_t a = tmem + kColP + u * 32;
+            const uint32_t a = tmem + kColS + 128 * j + u * 64;
             mma_ts_chain4_warp(tmem + kColO, a, a + 8, a + 16, a + 24, b, b + 128, b + 256, b + 384, idO, i > 0 || u > 0);
           }
           mma_commit_warp(&s.pv_done[j]);
@@ -653,12 +655,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         ok = false;
         break;
       }
-      // P's columns are free once PV_{i-1} has read them
-      if (i > 0 && !mbar_wait(&s.pv_done[(i - 1) % kSBufs], ((i - 1) / kSBufs) & 1, ab, VS_ERR_TIMEOUT)) ok = false;
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      tmem_st16(tl + kColP + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(tl + kColP + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      // P over the first 32 of the unit's own score columns (its scores are
+      // in registers; S_{i+2} overwrites the buffer only after PV_i has read
+      // P_i, in the pipe's order)
+      tmem_st16(tl + colS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(tl + colS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
       l_run += unit_sum;
       tmem_st_wait();
       tc_fence_before();
