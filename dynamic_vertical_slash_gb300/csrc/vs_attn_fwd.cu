@@ -575,6 +575,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
       const int j = i % kSBufs;
       const uint32_t colS = kColS + 128 * j + 64 * half;  // this unit's scores
       const uint64_t mask = mask_nx;
+      // the 16-key chunks holding a mask entry of any of the warp's rows
+      // (warp-uniform): the others' numerators are zero without arithmetic
+      const uint32_t occ = chunk_occupancy16(mask);
       ok = mbar_wait(&s.s_full[j], (i / kSBufs) & 1, ab, VS_ERR_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -602,15 +605,23 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         reg_dep(*reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         const uint32_t mlo = uint32_t(mask), mhi = uint32_t(mask >> 32);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          // bits 2k, 2k + 1 of the mask select the numerator or zero
-          const uint32_t w = k < 16 ? mlo : mhi;
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])), sc2, nref2), t0, t1);
-          const float p0 = ((w >> ((2 * k) & 31)) & 1u) ? ex2(t0) : 0.f;
-          const float p1 = ((w >> ((2 * k + 1) & 31)) & 1u) ? ex2(t1) : 0.f;
-          ps2[k & 3] = f2_add(ps2[k & 3], f2_pack(p0, p1));
-          pk[k] = pack_bf16x2(p0, p1);
+        for (int cq = 0; cq < 4; ++cq) {
+          if (!((occ >> cq) & 1u)) {
+#pragma unroll
+            for (int k = 8 * cq; k < 8 * cq + 8; ++k) pk[k] = 0u;
+            continue;
+          }
+#pragma unroll
+          for (int k = 8 * cq; k < 8 * cq + 8; ++k) {
+            // bits 2k, 2k + 1 of the mask select the numerator or zero
+            const uint32_t w = k < 16 ? mlo : mhi;
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1])), sc2, nref2), t0, t1);
+            const float p0 = ((w >> ((2 * k) & 31)) & 1u) ? ex2(t0) : 0.f;
+            const float p1 = ((w >> ((2 * k + 1) & 31)) & 1u) ? ex2(t1) : 0.f;
+            ps2[k & 3] = f2_add(ps2[k & 3], f2_pack(p0, p1));
+            pk[k] = pack_bf16x2(p0, p1);
+          }
         }
         float s0, s1, s2, s3, s4, s5, s6, s7;
         f2_unpack(ps2[0], s0, s1);
