@@ -620,8 +620,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ------------------------------------------------------ key-major dK / dV
-// TMEM: dK [0, 128), dV [128, 256), S^T [256, 320), dP^T [320, 384),
-//       P^T x2 [384, 448), dS^T x2 [448, 512)
 // TMEM: dK [0, 128), dV [128, 256), S^T [256, 320), dP^T [320, 384), P^T (bf16)
 // [384, 416), dS^T (bf16) [416, 448), K (bf16, the A operand of S^T = K Q^T,
 // loaded once per tile) [448, 512).
