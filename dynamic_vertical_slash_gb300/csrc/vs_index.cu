@@ -43,7 +43,27 @@ struct IndexParams {
   uint8_t* arena;
   const int32_t* v_idx;
   const int32_t* s_idx;
+  int staged;  // the lists walked by thread 0 live in dynamic shared memory
+  int sbits;   // the bitmaps are built in dynamic shared memory
 };
+
+// Dynamic shared memory of the staged cover: the f- and e-lists (EMAX
+// each), the slash list (ks), then either the parallel cover's scratch (4
+// (ks + 1) ints) or one flag byte per local block diagonal (striped); 0 when
+// that exceeds kIdxStageMax.
+constexpr size_t kIdxStageMax = 200 * 1024;
+size_t index_stage_bytes(const ArenaHeader& h) {
+  const size_t b = size_t(4) * (2 * size_t(h.EMAX) + size_t(h.ks)) +
+                   std::max(size_t(16) * (size_t(h.ks) + 1), size_t(h.EMAX) + 16);
+  return b <= kIdxStageMax ? b : 0;
+}
+// The offset, column and local-column bitmaps, or 0 when they exceed
+// kIdxStageMax.  The same dynamic shared memory serves both, one after the
+// other.
+size_t index_bits_bytes(const ArenaHeader& h) {
+  const size_t b = size_t(8) * (2 * size_t(h.WG) + size_t(h.WL));
+  return b <= kIdxStageMax ? b : 0;
+}
 
 __device__ __forceinline__ bool block_diag_active(const uint64_t* off, int WG, int64_t x) {
   // some selected offset in [64x - 63, 64x + 63]
@@ -51,6 +71,96 @@ __device__ __forceinline__ bool block_diag_active(const uint64_t* off, int WG, i
   const uint64_t a = bits64(off, 64 * x - 63, WG);
   const uint64_t b = bits64(off, 64 * x + 1, WG) & 0x7FFFFFFFFFFFFFFFull;
   return (a | b) != 0;
+}
+
+// Exclusive prefix sum of a[0, n) in shared memory by the whole block;
+// returns the total.  part holds kIdxThreads + 1 ints.
+__device__ int block_scan_excl(int* a, int n, int* part, int tid) {
+  const int per = (n + kIdxThreads - 1) / kIdxThreads;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += a[i];
+  part[tid] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int i = 0; i < kIdxThreads; ++i) {
+      const int c = part[i];
+      part[i] = run;
+      run += c;
+    }
+    part[kIdxThreads] = run;
+  }
+  __syncthreads();
+  int run = part[tid];
+  for (int i = lo; i < hi; ++i) {
+    const int v = a[i];
+    a[i] = run;
+    run += v;
+  }
+  const int total = part[kIdxThreads];
+  __syncthreads();
+  return total;
+}
+
+// The greedy cover of E = union of [o_j, o_j + dil] over the n ascending
+// offsets o (shared memory) by disjoint 64-wide intervals, the starts u <=
+// ulim, at most cap of them, written to out; by the whole block, returns
+// their number.  Same result as walking the offsets one by one: E falls into
+// segments (runs of intervals that overlap or touch; [A_s, B_s]); inside one
+// the walk places starts u_s, u_s + 64, ... while <= B_s, with u_s = max(cur,
+// A_s) for the walk's position cur on entry, and leaves at u_s + 64 K_s.
+// The position on entry is at most B_{s-1} + 64, so a segment starting that
+// far past its predecessor is entered at A_s whatever came before: the walk
+// is split at those segments and the pieces run in parallel.  sc holds 4 (n
+// + 1) ints.
+__device__ int cover_parallel(const int32_t* o, int n, int dil, int64_t ulim, int cap, int32_t* out, int* sc,
+                              int* part, int tid) {
+  int* first = sc;               // per offset: 1 if it starts a segment, then the segment index
+  int* segJ = sc + (n + 1);      // first offset of segment s; segJ[S] = n
+  int* segU = segJ + (n + 1);    // the segment's first start
+  int* segK = segU + (n + 1);    // its number of starts, then their exclusive prefix
+  for (int j = tid; j < n; j += kIdxThreads) first[j] = (j == 0 || o[j] > o[j - 1] + dil + 1) ? 1 : 0;
+  __syncthreads();
+  const int S = block_scan_excl(first, n, part, tid);
+  for (int j = tid; j < n; j += kIdxThreads)
+    if (j == 0 || o[j] > o[j - 1] + dil + 1) segJ[first[j]] = j;
+  if (tid == 0) segJ[S] = n;
+  __syncthreads();
+  for (int s = tid; s < S; s += kIdxThreads) {
+    const int64_t A = o[segJ[s]];
+    if (s > 0 && A < int64_t(o[segJ[s] - 1]) + dil + 64) continue;  // not the head of a piece
+    int64_t cur = A;
+    for (int t = s; t < S; ++t) {
+      const int64_t At = o[segJ[t]], Bt = int64_t(o[segJ[t + 1] - 1]) + dil;
+      if (t > s && At >= int64_t(o[segJ[t] - 1]) + dil + 64) break;  // the next piece's head
+      const int64_t u = max(cur, At);
+      const int K = u <= Bt ? int((Bt - u) / 64) + 1 : 0;
+      segU[t] = int(u);
+      segK[t] = K;
+      cur = u + 64 * int64_t(K);
+    }
+  }
+  __syncthreads();
+  const int T = block_scan_excl(segK, S, part, tid);
+  if (tid == 0) segK[S] = T;
+  __shared__ int s_cnt;
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  // the starts increase along the walk: those <= ulim are a prefix of it
+  int mine = 0;
+  for (int s = tid; s < S; s += kIdxThreads) {
+    const int p0 = segK[s], K = segK[s + 1] - p0;
+    const int64_t u0 = segU[s];
+    const int keep = u0 > ulim ? 0 : int(min(int64_t(K), (ulim - u0) / 64 + 1));
+    mine += keep;
+    for (int k = 0; k < keep && p0 + k < cap; ++k) out[p0 + k] = int32_t(u0 + 64 * k);
+  }
+  if (mine) atomicAdd(&s_cnt, mine);
+  __syncthreads();
+  const int cnt = min(s_cnt, cap);
+  __syncthreads();
+  return cnt;
 }
 
 __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams P) {
@@ -126,17 +236,39 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     for (int w = tid; w < H.WL; w += kIdxThreads) vpre[w] = 0;
     return;
   }
-  // 3. bitmaps
+  // 3. bitmaps.  Neighbouring entries of a sorted list set bits of the same
+  // word; built in shared memory when they fit (cheap same-word atomics),
+  // then written out.
+  extern __shared__ __align__(16) int32_t stage[];
+  uint64_t* ob = offbits;
+  uint64_t* cb = colbits;
+  uint64_t* vb = vloc;
+  if (P.sbits) {
+    uint64_t* s64 = reinterpret_cast<uint64_t*>(stage);
+    ob = s64;
+    cb = s64 + H.WG;
+    vb = s64 + 2 * H.WG;
+    for (int w = tid; w < 2 * H.WG + H.WL; w += kIdxThreads) s64[w] = 0ull;
+    __syncthreads();
+  }
   for (int i = tid; i < H.ks; i += kIdxThreads) {
     const int x = is[i];
-    if (x >= 0) atomicOr(reinterpret_cast<unsigned long long*>(offbits + (x >> 6)), 1ull << (x & 63));
+    if (x >= 0) atomicOr(reinterpret_cast<unsigned long long*>(ob + (x >> 6)), 1ull << (x & 63));
   }
   for (int i = tid; i < H.kv; i += kIdxThreads) {
     const int x = iv[i];
     if (x < 0) continue;
-    atomicOr(reinterpret_cast<unsigned long long*>(colbits + (x >> 6)), 1ull << (x & 63));
+    atomicOr(reinterpret_cast<unsigned long long*>(cb + (x >> 6)), 1ull << (x & 63));
     const int64_t l = local_key_of(W, H.kv_rank, H.Nk, x);
-    if (l >= 0) atomicOr(reinterpret_cast<unsigned long long*>(vloc + (l >> 6)), 1ull << (l & 63));
+    if (l >= 0) atomicOr(reinterpret_cast<unsigned long long*>(vb + (l >> 6)), 1ull << (l & 63));
+  }
+  __syncthreads();
+  if (P.sbits) {
+    for (int w = tid; w < H.WG; w += kIdxThreads) {
+      offbits[w] = ob[w];
+      colbits[w] = cb[w];
+    }
+    for (int w = tid; w < H.WL; w += kIdxThreads) vloc[w] = vb[w];
   }
   __threadfence_block();
   __syncthreads();
@@ -184,7 +316,49 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   for (int i = nv + tid; i < H.KVP; i += kIdxThreads) vlist[i] = -1;
   __threadfence_block();
   __syncthreads();
-  // 5. slash cover and 6. work counts (sequential; lists are short)
+  // 5. slash cover and 6. work counts, walked by thread 0 (the greedy cover
+  // is a chain of dependent reads).  Staged, the walk reads and writes
+  // shared memory: the slash list is copied in, the striped block diagonals'
+  // activity is evaluated by all threads, and the cover lists are copied out
+  // afterwards.
+  __shared__ int s_ne, s_nf;
+  const bool staged = P.staged != 0;
+  int32_t* fl = staged ? stage : flist;
+  int32_t* el = staged ? stage + H.EMAX : elist;
+  const int32_t* isr = is;
+  uint8_t* dflag = staged ? reinterpret_cast<uint8_t*>(stage + 2 * H.EMAX + H.ks) : nullptr;
+  const int64_t rel = int64_t(H.q_rank) - H.kv_rank;
+  const int nb = H.Nq / kBlk, nbk = H.Nk / kBlk;
+  if (staged) {
+    int32_t* s_is = stage + 2 * H.EMAX;
+    for (int i = tid; i < H.ks; i += kIdxThreads) s_is[i] = is[i];
+    isr = s_is;
+    if (!H.sheared) {
+      // bit 0: D is active for a (2 row blocks x 1 key block) tile, bit 1:
+      // for a (1 row block x 2 key blocks) tile
+      for (int D = -nbk + tid; D <= nb; D += kIdxThreads) {
+        const bool a = block_diag_active(offbits, H.WG, int64_t(W) * D + rel);
+        const bool e = a || block_diag_active(offbits, H.WG, int64_t(W) * D + W + rel);
+        const bool f = a || block_diag_active(offbits, H.WG, int64_t(W) * D - W + rel);
+        dflag[D + nbk] = uint8_t((e ? 1 : 0) | (f ? 2 : 0));
+      }
+    }
+  }
+  __syncthreads();
+  // the sheared cover of the exact offsets, by the whole block
+  const bool par_cover = staged && H.sheared && !H.block_cover;
+  int pnf = 0, pne = 0;
+  if (par_cover) {
+    int* sc = stage + 2 * H.EMAX + H.ks;
+    pnf = cover_parallel(isr, nks, kQTile - 1, int64_t(H.Nq) + kQTile - 2, H.EMAX, fl, sc, part, tid);
+    if (gp) {
+      pne = cover_parallel(isr, nks, kQTile / gp - 1, int64_t(H.Nq) + kQTile / gp - 2, H.EMAX, el, sc, part, tid);
+    } else {
+      for (int i = tid; i < pnf; i += kIdxThreads) el[i] = fl[i];
+      pne = pnf;
+    }
+    __syncthreads();
+  }
   if (tid == 0) {
     int ne = 0, nf = 0;
     // block cover: the smallest offset >= x inside an active block diagonal's
@@ -201,7 +375,10 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
       }
       return -1;
     };
-    if (H.sheared) {
+    if (par_cover) {
+      nf = pnf;
+      ne = pne;
+    } else if (H.sheared) {
       // greedy cover by disjoint 64-wide intervals of the selected offsets
       // dilated by `dil` (tile height - 1)
       auto cover = [&](int32_t* list, int64_t dil) {
@@ -213,9 +390,9 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
             o = next_eff(cur - dil);
             if (o < 0) break;
           } else {
-            while (j < nks && is[j] < cur - dil) ++j;
+            while (j < nks && isr[j] < cur - dil) ++j;
             if (j == nks) break;
-            o = is[j];
+            o = isr[j];
           }
           const int64_t u = max(cur, o);
           if (u > int64_t(H.Nq) + dil - 1 || n >= H.EMAX) break;
@@ -224,34 +401,42 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
         }
         return n;
       };
-      nf = cover(flist, kQTile - 1);
+      nf = cover(fl, kQTile - 1);
       if (gp) {
-        ne = cover(elist, kQTile / gp - 1);
+        ne = cover(el, kQTile / gp - 1);
       } else {
-        for (int i = 0; i < nf; ++i) elist[i] = flist[i];
+        for (int i = 0; i < nf; ++i) el[i] = fl[i];
         ne = nf;
       }
     } else {
       // local block diagonals from the key window's end to the query
       // window's end (negative D: keys after the rows locally, which the
       // window offsets may still make causal)
-      const int64_t rel = int64_t(H.q_rank) - H.kv_rank;
-      const int nb = H.Nq / kBlk, nbk = H.Nk / kBlk;
       for (int D = -nbk; D <= nb && ne < H.EMAX; ++D)
-        if (block_diag_active(offbits, H.WG, int64_t(W) * D + rel) ||
-            block_diag_active(offbits, H.WG, int64_t(W) * D + W + rel))
-          elist[ne++] = 64 * D + 64;
+        if (staged ? (dflag[D + nbk] & 1)
+                   : (block_diag_active(offbits, H.WG, int64_t(W) * D + rel) ||
+                      block_diag_active(offbits, H.WG, int64_t(W) * D + W + rel)))
+          el[ne++] = 64 * D + 64;
       for (int D = -nbk; D <= nb && nf < H.EMAX; ++D)
-        if (block_diag_active(offbits, H.WG, int64_t(W) * D + rel) ||
-            block_diag_active(offbits, H.WG, int64_t(W) * D - W + rel))
-          flist[nf++] = 64 * D;
+        if (staged ? (dflag[D + nbk] & 2)
+                   : (block_diag_active(offbits, H.WG, int64_t(W) * D + rel) ||
+                      block_diag_active(offbits, H.WG, int64_t(W) * D - W + rel)))
+          fl[nf++] = 64 * D;
     }
     *ecount = ne;
     *fcount = nf;
     *vcount = nv;
+    s_ne = ne;
+    s_nf = nf;
+  }
+  __syncthreads();
+  // 6. work counts of the four passes (every thread a share of the entries;
+  // integer sums, so the order does not matter)
+  {
+    const int ne = s_ne, nf = s_nf;
     const int64_t T = (H.Nq + kQTile - 1) / kQTile;
     const int64_t TK = (H.Nk + kBarK - 1) / kBarK;
-    int64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    int64_t c[4] = {0, 0, 0, 0};
     // the same unit ranges as the kernels: query tile t takes the entries
     // e in [128 t + 64 - Nk + 1, 128 t + 127] (its 64 keys start before Nk)
     // and the bar chunks whose first column precedes its last row; key tile
@@ -261,48 +446,60 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     auto ceil_div = [](int64_t a, int64_t b) { return a >= 0 ? (a + b - 1) / b : -((-a) / b); };
     auto floor_div = [](int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
     if (!gp) {
-      for (int i = 0; i < ne; ++i) {
-        const int64_t e = elist[i];
+      for (int i = tid; i < ne; i += kIdxThreads) {
+        const int64_t e = el[i];
         const int64_t tmin = max(int64_t(0), ceil_div(e - 127, kQTile));
         const int64_t tmax = min(T - 1, floor_div(e - 65 + H.Nk, kQTile));
-        c0 += max(int64_t(0), tmax - tmin + 1);
+        c[0] += max(int64_t(0), tmax - tmin + 1);
       }
-      for (int c = 0; c * kKTile < nv; ++c) {
-        const int64_t m_g = (int64_t(W) * (vlist[c * kKTile] >> 6) + H.kv_rank) * kBlk + (vlist[c * kKTile] & 63);
+      for (int ch = tid; ch * kKTile < nv; ch += kIdxThreads) {
+        const int64_t m_g = (int64_t(W) * (vlist[ch * kKTile] >> 6) + H.kv_rank) * kBlk + (vlist[ch * kKTile] & 63);
         const int64_t tmin = first_causal_row_block(W, H.q_rank, m_g) / 2;
-        c1 += max(int64_t(0), T - tmin);
+        c[1] += max(int64_t(0), T - tmin);
       }
     } else if ((bh % H.Hq) % gp == 0) {
       // packed strips of R tokens (unstriped): strip s takes the entries e
       // in [R s + R - 63 - Nk, R s + R - 1] and the bar chunks whose first
       // column is at most its last token
       const int64_t R = kQTile / gp, TS = (H.Nq + R - 1) / R;
-      for (int i = 0; i < ne; ++i) {
-        const int64_t e = elist[i];
+      for (int i = tid; i < ne; i += kIdxThreads) {
+        const int64_t e = el[i];
         const int64_t smin = max(int64_t(0), ceil_div(e - R + 1, R));
         const int64_t smax = min(TS - 1, floor_div(e - R + 63 + H.Nk, R));
-        c0 += max(int64_t(0), smax - smin + 1);
+        c[0] += max(int64_t(0), smax - smin + 1);
       }
-      for (int c = 0; c * kKTile < nv; ++c) {
-        const int64_t f = vlist[c * kKTile];
-        c1 += max(int64_t(0), TS - max(int64_t(0), ceil_div(f - R + 1, R)));
+      for (int ch = tid; ch * kKTile < nv; ch += kIdxThreads) {
+        const int64_t f = vlist[ch * kKTile];
+        c[1] += max(int64_t(0), TS - max(int64_t(0), ceil_div(f - R + 1, R)));
       }
     }
-    for (int i = 0; i < nf; ++i) {
-      const int64_t f = flist[i];
+    for (int i = tid; i < nf; i += kIdxThreads) {
+      const int64_t f = fl[i];
       const int64_t tmin = max(int64_t(0), ceil_div(-f - 63, kBarK));
       const int64_t tmax = min(TK - 1, floor_div(H.Nq - 1 - f, kBarK));
-      c2 += max(int64_t(0), tmax - tmin + 1);
+      c[2] += max(int64_t(0), tmax - tmin + 1);
     }
-    for (int c = 0; c * kBarK < nv; ++c) {
-      const int64_t m_g = (int64_t(W) * (vlist[c * kBarK] >> 6) + H.kv_rank) * kBlk + (vlist[c * kBarK] & 63);
+    for (int ch = tid; ch * kBarK < nv; ch += kIdxThreads) {
+      const int64_t m_g = (int64_t(W) * (vlist[ch * kBarK] >> 6) + H.kv_rank) * kBlk + (vlist[ch * kBarK] & 63);
       const int64_t rs = first_causal_row_block(W, H.q_rank, m_g) * kBlk;
-      c3 += max(int64_t(0), (H.Nq - rs + kRowTile - 1) / kRowTile);
+      c[3] += max(int64_t(0), (H.Nq - rs + kRowTile - 1) / kRowTile);
     }
-    counts[0] = c0;
-    counts[1] = c1;
-    counts[2] = c2;
-    counts[3] = c3;
+    __shared__ unsigned long long s_cnt[4];
+    if (tid < 4) s_cnt[tid] = 0ull;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      unsigned long long v = static_cast<unsigned long long>(c[k]);
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if ((tid & 31) == 0 && v) atomicAdd(&s_cnt[k], v);
+    }
+    __syncthreads();
+    if (tid < 4) counts[tid] = static_cast<int64_t>(s_cnt[tid]);
+  }
+  if (staged) {
+    __syncthreads();
+    for (int i = tid; i < s_nf; i += kIdxThreads) flist[i] = fl[i];
+    for (int i = tid; i < s_ne; i += kIdxThreads) elist[i] = el[i];
   }
 }
 
@@ -361,9 +558,16 @@ vs_status launch_index(const vs_shape* s, const int32_t* v_idx, const int32_t* s
   P.arena = static_cast<uint8_t*>(arena);
   P.v_idx = v_idx;
   P.s_idx = s_idx;
+  const size_t lists = index_stage_bytes(P.hdr), bits = index_bits_bytes(P.hdr);
+  const size_t stage = std::max(lists, bits);
+  P.staged = lists > 0;
+  P.sbits = bits > 0;
+  if (stage > 48 * 1024 &&
+      cudaFuncSetAttribute(vs_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(stage)) != cudaSuccess)
+    return VS_ERR_CUDA;
   if (cudaMemsetAsync(arena, 0, sizeof(int32_t), st) != cudaSuccess) return VS_ERR_CUDA;
   trace_begin("index", st);
-  vs_index_kernel<<<s->B * s->Hq, kIdxThreads, 0, st>>>(P);
+  vs_index_kernel<<<s->B * s->Hq, kIdxThreads, stage, st>>>(P);
   trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
