@@ -123,24 +123,38 @@ __global__ void __launch_bounds__(256) bwd_prep(const BwdParams p, int d) {
   const BwdLayout L = bwd_layout_dev(av.hdr, d);
   float* l2 = reinterpret_cast<float*>(p.ws + L.off_l2);
   float* dd = reinterpret_cast<float*>(p.ws + L.off_d);
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t n = i % p.Nq, bh = i / p.Nq;
-    const int64_t b = bh / p.Hq, h = bh % p.Hq;
-    const int64_t off = (b * p.so[0] + n * p.so[1] + h * p.so[2]) * 2;
-    const uint4* orow = reinterpret_cast<const uint4*>(p.o + off);
-    const uint4* grow = reinterpret_cast<const uint4*>(p.dO + off);
+  // eight lanes per row, 16-byte pieces (a row's 128 or 256 bytes in one or
+  // two coalesced sweeps); a warp takes four consecutive rows and every lane
+  // runs the same trip count, so the lane reductions see the whole warp
+  const int lane = threadIdx.x & 31, sub = lane & 7;
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x / 32);
+  for (int64_t base = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32 * 4; base < total; base += warps * 4) {
+    const int64_t i = base + (lane >> 3);
+    const bool ok = i < total;
     float acc = 0.f;
-    for (int c = 0; c < d / 8; ++c) {
-      const uint4 a = orow[c], g = grow[c];
-      const uint32_t av4[4] = {a.x, a.y, a.z, a.w}, gv4[4] = {g.x, g.y, g.z, g.w};
+    if (ok) {
+      const int64_t n = i % p.Nq, bh = i / p.Nq;
+      const int64_t b = bh / p.Hq, h = bh % p.Hq;
+      const int64_t off = (b * p.so[0] + n * p.so[1] + h * p.so[2]) * 2;
+      const uint4* orow = reinterpret_cast<const uint4*>(p.o + off);
+      const uint4* grow = reinterpret_cast<const uint4*>(p.dO + off);
+      for (int c = sub; c < d / 8; c += 8) {
+        const uint4 a = orow[c], g = grow[c];
+        const uint32_t av4[4] = {a.x, a.y, a.z, a.w}, gv4[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(av4[e] << 16), __uint_as_float(gv4[e] << 16), acc);
-        acc = fmaf(__uint_as_float(av4[e] & 0xFFFF0000u), __uint_as_float(gv4[e] & 0xFFFF0000u), acc);
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(__uint_as_float(av4[e] << 16), __uint_as_float(gv4[e] << 16), acc);
+          acc = fmaf(__uint_as_float(av4[e] & 0xFFFF0000u), __uint_as_float(gv4[e] & 0xFFFF0000u), acc);
+        }
       }
     }
-    dd[i] = acc;
-    l2[i] = -p.lse[i] * kLog2e;  // stored negated: the kernels add it to the scaled scores
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (ok && sub == 0) {
+      dd[i] = acc;
+      l2[i] = -p.lse[i] * kLog2e;  // stored negated: the kernels add it to the scaled scores
+    }
   }
 }
 
