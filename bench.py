@@ -465,6 +465,12 @@ def ours(args, w, x, rank, world):
             att[kname]["issued_tflops"] = issued_per_step[kname] / (att[kname]["ms_avg"] * 1e-3) / 1e12
     attn_ms = sum(per_kernel[kname]["ms_avg"] for kname in att)
 
+    # ---------------- end to end through the public API, host buffers (run
+    # right after the timed region, before the optional dense comparison)
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, w, attn, q, k, v, do, dev, world, executed)
+
     extra = {}
     # ---------------- same kernels on the dense causal mask (every offset selected)
     if rank == 0 and not args.no_dense:
@@ -500,11 +506,6 @@ def ours(args, w, x, rank, world):
         extra["x_vs_dense"] = dense_ms / ms
         extra["x_vs_dense_attention_only"] = dense_ms / attn_ms if attn_ms else None
         del arena_d, o_d, dq_d, dk_d, dv_d, ws_b
-
-    # ---------------- end to end through the public API, host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = _e2e(args, w, attn, q, k, v, do, dev, world, executed)
 
     dense_f = dense_causal_flops(w.B, w.N, w.Hq, w.d)
     cfg = _config(w)
@@ -576,7 +577,9 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     host->device copy runs on its own stream while step i-1 computes, and its
     results go back on a third stream while step i+1 computes -- the usual
     prefetching of the next batch.  Device time from CUDA events spanning
-    the first copy to the last one."""
+    the first copy to the last one; SM clocks are sampled during both timed
+    loops and reported beside each (a long run under load can be power
+    capped below the clocks of the short kernel-timed region).
     import torch
 
     import dynamic_vertical_slash_gb300 as vs
@@ -608,11 +611,12 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     if world > 1:
         torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        serial_step()
-    b.record()
-    torch.cuda.synchronize()
+    with ClockSampler(_gpu_id(dev.index)) as clk_s:
+        a.record()
+        for _ in range(args.steps):
+            serial_step()
+        b.record()
+        torch.cuda.synchronize()
     serial_ms = reduce_max(a.elapsed_time(b) / args.steps)
     attn.check()
 
@@ -659,14 +663,17 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    start, end = run(args.steps)
-    torch.cuda.synchronize()
+    with ClockSampler(_gpu_id(dev.index)) as clk_p:
+        start, end = run(args.steps)
+        torch.cuda.synchronize()
     pipe_ms = reduce_max(start.elapsed_time(end) / args.steps)
     for a_ in att:
         a_.check()
     return {"value": job_tflops(world, executed, pipe_ms), "unit": UNIT, "ms_per_step": pipe_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "serial": {"value": job_tflops(world, executed, serial_ms), "ms_per_step": serial_ms},
+            "clocks": clk_p.summary(),
+            "serial": {"value": job_tflops(world, executed, serial_ms), "ms_per_step": serial_ms,
+                       "clocks": clk_s.summary()},
             "path": "VSAttention.forward/backward (C ABI) with pinned host inputs and outputs; pipelined: next "
                     "step's inputs copied in and previous step's results copied out on separate streams while a "
                     "step computes (two instances, two input sets)"}
