@@ -579,7 +579,7 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     prefetching of the next batch.  Device time from CUDA events spanning
     the first copy to the last one; SM clocks are sampled during both timed
     loops and reported beside each (a long run under load can be power
-    capped below the clocks of the short kernel-timed region).
+    capped below the clocks of the short kernel-timed region)."""
     import torch
 
     import dynamic_vertical_slash_gb300 as vs
