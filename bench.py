@@ -574,9 +574,10 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
     Two schedules: `serial` (copy in, compute, copy out, one after the other
     on one stream) and `pipelined` (the line's value): two VSAttention
     instances and two input buffer sets alternate between steps, step i's
-    host->device copy runs on its own stream while step i-1 computes, and its
-    results go back on a third stream while step i+1 computes -- the usual
-    prefetching of the next batch.  Device time from CUDA events spanning
+    host->device copy runs on its own stream while step i-1 computes (dO may
+    still be arriving while step i's forward runs), and its results go back
+    on a third stream (O while step i's backward runs, the gradients while
+    step i+1 computes) -- the usual prefetching of the next batch.  Device time from CUDA events spanning
     the first copy to the last one; SM clocks are sampled during both timed
     loops and reported beside each (a long run under load can be power
     capped below the clocks of the short kernel-timed region)."""
@@ -636,21 +637,29 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
             with torch.cuda.stream(s_in):
                 if comp_done[sl] is not None:  # step i - 2 has finished reading this input set
                     s_in.wait_event(comp_done[sl])
-                for dst, src in zip(din[sl], hin):
+                for dst, src in zip(din[sl][:3], hin[:3]):
                     dst.copy_(src, non_blocking=True)
-                in_done = torch.cuda.Event()
-                in_done.record(s_in)
-            s_comp.wait_event(in_done)
+                qkv_in = torch.cuda.Event()
+                qkv_in.record(s_in)
+                din[sl][3].copy_(hin[3], non_blocking=True)  # dO: needed by the backward only
+                do_in = torch.cuda.Event()
+                do_in.record(s_in)
+            s_comp.wait_event(qkv_in)
             if out_done[sl] is not None:  # step i - 2's results have left this instance's buffers
                 s_comp.wait_event(out_done[sl])
             o, _ = att[sl].forward(din[sl][0], din[sl][1], din[sl][2], stream=s_comp)
+            fwd_done = torch.cuda.Event()
+            fwd_done.record(s_comp)
+            s_comp.wait_event(do_in)
             gq, gk, gv = att[sl].backward(din[sl][3], stream=s_comp)
             cd = torch.cuda.Event()
             cd.record(s_comp)
             comp_done[sl] = cd
             with torch.cuda.stream(s_out):
+                s_out.wait_event(fwd_done)  # O leaves while the backward runs
+                hout[0].copy_(o, non_blocking=True)
                 s_out.wait_event(cd)
-                for dst, src in zip(hout, (o, gq, gk, gv)):
+                for dst, src in zip(hout[1:], (gq, gk, gv)):
                     dst.copy_(src, non_blocking=True)
                 od = torch.cuda.Event()
                 od.record(s_out)
@@ -676,7 +685,8 @@ def _e2e(args, w, attn, q, k, v, do, dev, world, executed):
                        "clocks": clk_s.summary()},
             "path": "VSAttention.forward/backward (C ABI) with pinned host inputs and outputs; pipelined: next "
                     "step's inputs copied in and previous step's results copied out on separate streams while a "
-                    "step computes (two instances, two input sets)"}
+                    "step computes (two instances, two input sets; dO copied in during the forward, O copied out "
+                    "during the backward)"}
 
 
 def striped(args, w, x, rank, world):
