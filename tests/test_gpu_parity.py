@@ -128,6 +128,38 @@ def test_index_covers_mask_exactly_once(vs, N, kv, ks, seed):
         np.testing.assert_array_equal(A.coverage_key_major(h), M)
 
 
+# slash offsets whose gaps sit at the boundaries of the cover's segments: the
+# dilated intervals [o, o + 127] touch (gap 128), just separate (129, 130),
+# leave the previous cover interval overhanging the next segment (gap 190:
+# 63 past the segment's end) or not (191: exactly 64; 192)
+@pytest.mark.parametrize("gaps", [(65,), (128,), (129,), (130,), (190,), (191,), (192,), (1, 190, 63, 191, 300),
+                                  (127, 128, 129, 190, 191, 192, 64, 65, 2)])
+def test_index_cover_segment_gaps(vs, gaps):
+    N, Hq, Hkv, d, kv = 1536, 2, 1, 64, 8
+    offs, o, i = [], 3, 0
+    while o < N:
+        offs.append(o)
+        o += gaps[i % len(gaps)]
+        i += 1
+    ks = len(offs)
+    is_ = np.full((1, Hq, ks), -1, np.int32)
+    is_[0, 0] = offs
+    is_[0, 1, :ks // 2] = offs[::2][:ks // 2]  # the other head: every second offset
+    rng = np.random.default_rng(len(gaps))
+    iv = np.sort(rng.choice(N, size=(1, Hq, kv), replace=False), axis=-1).astype(np.int32)
+    q = torch.zeros(1, N, Hq, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, N, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    arena = vs.vs_build_block_index(q, k, torch.from_numpy(iv).cuda(), torch.from_numpy(is_).cuda())
+    torch.cuda.synchronize()
+    assert vs.vs_check_status(arena) == 0
+    A = Arena(arena)
+    p = oracle.Problem(np.zeros((1, N, Hq, d)), np.zeros((1, N, Hkv, d)), np.zeros((1, N, Hkv, d)), iv, is_, 0.1)
+    for h in range(Hq):
+        M = oracle.mask_dense(p, 0, h).astype(np.int32)
+        np.testing.assert_array_equal(A.coverage_query_major(h), M)
+        np.testing.assert_array_equal(A.coverage_key_major(h), M)
+
+
 def test_index_rejects_bad_lists(vs):
     N = 256
     q = torch.zeros(1, N, 1, 64, dtype=torch.bfloat16, device="cuda")
