@@ -316,11 +316,12 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
   for (int i = nv + tid; i < H.KVP; i += kIdxThreads) vlist[i] = -1;
   __threadfence_block();
   __syncthreads();
-  // 5. slash cover and 6. work counts, walked by thread 0 (the greedy cover
-  // is a chain of dependent reads).  Staged, the walk reads and writes
-  // shared memory: the slash list is copied in, the striped block diagonals'
-  // activity is evaluated by all threads, and the cover lists are copied out
-  // afterwards.
+  // 5. slash cover.  Staged (the lists fit the dynamic shared memory), the
+  // slash list is copied in and the cover lists are built there and copied
+  // out afterwards: the exact sheared cover by the whole block
+  // (cover_parallel), the striped cover from block-diagonal flags evaluated
+  // by all threads, the block-cover walk by thread 0.  Otherwise thread 0
+  // walks the lists in global memory.
   __shared__ int s_ne, s_nf;
   const bool staged = P.staged != 0;
   int32_t* fl = staged ? stage : flist;
