@@ -53,8 +53,11 @@ struct IndexParams {
 // that exceeds kIdxStageMax.
 constexpr size_t kIdxStageMax = 200 * 1024;
 size_t index_stage_bytes(const ArenaHeader& h) {
-  const size_t b = size_t(4) * (2 * size_t(h.EMAX) + size_t(h.ks)) +
-                   std::max(size_t(16) * (size_t(h.ks) + 1), size_t(h.EMAX) + 16);
+  size_t b = size_t(4) * (2 * size_t(h.EMAX) + size_t(h.ks)) +
+             std::max(size_t(16) * (size_t(h.ks) + 1), size_t(h.EMAX) + 16);
+  // block cover: the active block diagonals (at most WG), their words'
+  // counts (at most WG) and the cover's scratch instead of the slash list
+  if (h.block_cover) b = std::max(b, size_t(4) * (2 * size_t(h.EMAX) + 2 * size_t(h.WG) + 4 * (size_t(h.WG) + 1)));
   return b <= kIdxStageMax ? b : 0;
 }
 // The offset, column and local-column bitmaps, or 0 when they exceed
@@ -103,37 +106,50 @@ __device__ int block_scan_excl(int* a, int n, int* part, int tid) {
   return total;
 }
 
-// The greedy cover of E = union of [o_j, o_j + dil] over the n ascending
-// offsets o (shared memory) by disjoint 64-wide intervals, the starts u <=
-// ulim, at most cap of them, written to out; by the whole block, returns
-// their number.  Same result as walking the offsets one by one: E falls into
-// segments (runs of intervals that overlap or touch; [A_s, B_s]); inside one
-// the walk places starts u_s, u_s + 64, ... while <= B_s, with u_s = max(cur,
-// A_s) for the walk's position cur on entry, and leaves at u_s + 64 K_s.
-// The position on entry is at most B_{s-1} + 64, so a segment starting that
-// far past its predecessor is entered at A_s whatever came before: the walk
-// is split at those segments and the pieces run in parallel.  sc holds 4 (n
-// + 1) ints.
+// The greedy cover of E = union of the intervals [a_j, b_j] (ascending in
+// both ends) by disjoint 64-wide intervals, the starts u <= ulim, at most cap
+// of them, written to out; by the whole block, returns their number.  Exact
+// offsets (BLK = false): o holds the n ascending selected offsets, [a_j, b_j]
+// = [o_j, o_j + dil].  Block cover (BLK = true): o holds the n ascending
+// active block diagonals D, whose effective offsets [max(0, 64 D - 63), 64 D
+// + 63] are dilated the same way.  Same result as walking the list one by
+// one: E falls into segments (runs of intervals that overlap or touch; [A_s,
+// B_s]); inside one the walk places starts u_s, u_s + 64, ... while <= B_s,
+// with u_s = max(cur, A_s) for the walk's position cur on entry, and leaves
+// at u_s + 64 K_s.  The position on entry is at most B_{s-1} + 64, so a
+// segment starting that far past its predecessor is entered at A_s whatever
+// came before: the walk is split at those segments and the pieces run in
+// parallel.  sc holds 4 (n + 1) ints.
+template <bool BLK>
+__device__ __forceinline__ int64_t cov_a(const int32_t* o, int j) {
+  return BLK ? max(int64_t(0), 64 * int64_t(o[j]) - 63) : int64_t(o[j]);
+}
+template <bool BLK>
+__device__ __forceinline__ int64_t cov_b(const int32_t* o, int j, int dil) {
+  return BLK ? 64 * int64_t(o[j]) + 63 + dil : int64_t(o[j]) + dil;
+}
+template <bool BLK>
 __device__ int cover_parallel(const int32_t* o, int n, int dil, int64_t ulim, int cap, int32_t* out, int* sc,
                               int* part, int tid) {
-  int* first = sc;               // per offset: 1 if it starts a segment, then the segment index
-  int* segJ = sc + (n + 1);      // first offset of segment s; segJ[S] = n
+  int* first = sc;               // per interval: 1 if it starts a segment, then the segment index
+  int* segJ = sc + (n + 1);      // first interval of segment s; segJ[S] = n
   int* segU = segJ + (n + 1);    // the segment's first start
   int* segK = segU + (n + 1);    // its number of starts, then their exclusive prefix
-  for (int j = tid; j < n; j += kIdxThreads) first[j] = (j == 0 || o[j] > o[j - 1] + dil + 1) ? 1 : 0;
+  auto starts_segment = [&](int j) { return j == 0 || cov_a<BLK>(o, j) > cov_b<BLK>(o, j - 1, dil) + 1; };
+  for (int j = tid; j < n; j += kIdxThreads) first[j] = starts_segment(j) ? 1 : 0;
   __syncthreads();
   const int S = block_scan_excl(first, n, part, tid);
   for (int j = tid; j < n; j += kIdxThreads)
-    if (j == 0 || o[j] > o[j - 1] + dil + 1) segJ[first[j]] = j;
+    if (starts_segment(j)) segJ[first[j]] = j;
   if (tid == 0) segJ[S] = n;
   __syncthreads();
   for (int s = tid; s < S; s += kIdxThreads) {
-    const int64_t A = o[segJ[s]];
-    if (s > 0 && A < int64_t(o[segJ[s] - 1]) + dil + 64) continue;  // not the head of a piece
+    const int64_t A = cov_a<BLK>(o, segJ[s]);
+    if (s > 0 && A < cov_b<BLK>(o, segJ[s] - 1, dil) + 64) continue;  // not the head of a piece
     int64_t cur = A;
     for (int t = s; t < S; ++t) {
-      const int64_t At = o[segJ[t]], Bt = int64_t(o[segJ[t + 1] - 1]) + dil;
-      if (t > s && At >= int64_t(o[segJ[t] - 1]) + dil + 64) break;  // the next piece's head
+      const int64_t At = cov_a<BLK>(o, segJ[t]), Bt = cov_b<BLK>(o, segJ[t + 1] - 1, dil);
+      if (t > s && At >= cov_b<BLK>(o, segJ[t] - 1, dil) + 64) break;  // the next piece's head
       const int64_t u = max(cur, At);
       const int K = u <= Bt ? int((Bt - u) / 64) + 1 : 0;
       segU[t] = int(u);
@@ -346,15 +362,39 @@ __global__ void __launch_bounds__(kIdxThreads) vs_index_kernel(const IndexParams
     }
   }
   __syncthreads();
-  // the sheared cover of the exact offsets, by the whole block
-  const bool par_cover = staged && H.sheared && !H.block_cover;
+  // the sheared cover by the whole block: of the exact offsets, or of the
+  // active block diagonals (listed first from their bitmap)
+  const bool par_cover = staged && H.sheared;
   int pnf = 0, pne = 0;
   if (par_cover) {
-    int* sc = stage + 2 * H.EMAX + H.ks;
-    pnf = cover_parallel(isr, nks, kQTile - 1, int64_t(H.Nq) + kQTile - 2, H.EMAX, fl, sc, part, tid);
-    if (gp) {
-      pne = cover_parallel(isr, nks, kQTile / gp - 1, int64_t(H.Nq) + kQTile / gp - 2, H.EMAX, el, sc, part, tid);
+    if (H.block_cover) {
+      int32_t* dl = stage + 2 * H.EMAX;
+      int* wc = dl + H.WG;
+      int* sc = wc + H.WG;
+      const int nw = int((ndiag + 63) / 64);
+      for (int w = tid; w < nw; w += kIdxThreads) wc[w] = __popcll(bdbits[w]);
+      __syncthreads();
+      const int nd = block_scan_excl(wc, nw, part, tid);
+      for (int w = tid; w < nw; w += kIdxThreads) {
+        uint64_t x = bdbits[w];
+        int at = wc[w];
+        while (x) {
+          dl[at++] = w * 64 + __ffsll(x) - 1;
+          x &= x - 1;
+        }
+      }
+      __syncthreads();
+      pnf = cover_parallel<true>(dl, nd, kQTile - 1, int64_t(H.Nq) + kQTile - 2, H.EMAX, fl, sc, part, tid);
+      if (gp)
+        pne = cover_parallel<true>(dl, nd, kQTile / gp - 1, int64_t(H.Nq) + kQTile / gp - 2, H.EMAX, el, sc, part, tid);
     } else {
+      int* sc = stage + 2 * H.EMAX + H.ks;
+      pnf = cover_parallel<false>(isr, nks, kQTile - 1, int64_t(H.Nq) + kQTile - 2, H.EMAX, fl, sc, part, tid);
+      if (gp)
+        pne = cover_parallel<false>(isr, nks, kQTile / gp - 1, int64_t(H.Nq) + kQTile / gp - 2, H.EMAX, el, sc, part,
+                                    tid);
+    }
+    if (!gp) {
       for (int i = tid; i < pnf; i += kIdxThreads) el[i] = fl[i];
       pne = pnf;
     }
