@@ -39,6 +39,40 @@ def _compare(got, ref):
     assert np.max(np.abs(lse[fin] - ref["lse"][fin]), initial=0.0) <= 1e-3
 
 
+# active block diagonals D at given spacings: an offset 64 D activates only
+# diagonal D, and the dilated offset intervals of diagonals k apart overlap
+# (k <= 3), are just separated (k = 4: the previous cover interval overhangs
+# the next one) or are entered at their own start (k >= 5)
+@pytest.mark.parametrize("steps", [(1,), (3,), (4,), (5,), (6,), (1, 4, 2, 5, 3, 6)])
+def test_block_index_cover_diagonal_spacings(vs, steps):
+    N, Hq, Hkv, d, kv = 2560, 2, 1, 64, 4
+    diags, D, i = [], 1, 0
+    while 64 * D < N:
+        diags.append(D)
+        D += steps[i % len(steps)]
+        i += 1
+    offs = [64 * D for D in diags]
+    ks = len(offs)
+    is_ = np.full((1, Hq, ks), -1, np.int32)
+    is_[0, 0] = offs
+    is_[0, 1, :ks - 1] = offs[1:]  # the other head: without the first diagonal
+    rng = np.random.default_rng(len(steps))
+    iv = np.sort(rng.choice(N, size=(1, Hq, kv), replace=False), axis=-1).astype(np.int32)
+    q = torch.zeros(1, N, Hq, d, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, N, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    arena = vs.vs_build_block_index(q, k, torch.from_numpy(iv).cuda(), torch.from_numpy(is_).cuda(),
+                                    block_cover=True)
+    torch.cuda.synchronize()
+    assert vs.vs_check_status(arena) == 0
+    A = Arena(arena)
+    p = oracle.Problem(np.zeros((1, N, Hq, d)), np.zeros((1, N, Hkv, d)), np.zeros((1, N, Hkv, d)), iv, is_, 0.1,
+                       block=True)
+    for h in range(Hq):
+        M = oracle.mask_dense(p, 0, h).astype(np.int32)
+        np.testing.assert_array_equal(A.coverage_query_major(h), M)
+        np.testing.assert_array_equal(A.coverage_key_major(h), M)
+
+
 @pytest.mark.parametrize("N,kv,ks,seed", [(1024, 32, 32, 1), (1088, 40, 50, 2), (640, 3, 200, 3), (256, 4, 1, 4)])
 def test_block_index_covers_block_mask_exactly_once(vs, N, kv, ks, seed):
     Hq, Hkv, d = 2, 1, 64
