@@ -95,7 +95,7 @@ struct EstSmem {
 // A failure recorded earlier in this call (or left in the status word by an
 // earlier call) makes the estimator's later kernels skip their work, so that
 // no kernel reads scratch a failed kernel left unwritten.  VS_ERR_SCORE is a
-// per-list verdict of the top-p step, not a failure of the scores.
+// per-list outcome of the top-p step, not a failure of the scores.
 __device__ __forceinline__ bool est_failed(const int* err) {
   const int w = *reinterpret_cast<const volatile int*>(err);
   return w != 0 && w != VS_ERR_SCORE;
