@@ -17,23 +17,22 @@
 // first unit and one its second.  fp32 online softmax on the exact token mask
 // in registers, P (bf16) over the first half of the unit's own score columns.
 //
-// TMEM columns: O [0, d), score buffers S_j [128 + 128 j, +128) for j < 2
-// (unit u's scores in [64 u, +64), then its P as bf16 pairs in [64 u, +32)),
-// Q [384, 384 + d / 2) as bf16 pairs; [448, 512) unused.  The softmax threads
-// write their row of Q there once per tile, so every S = Q K^T chain reads
-// its A operand from TMEM and only K from shared memory.  S of pair i goes to
-// buffer i % 2.  The MMA order is S0 S1, then per pair i: PV_i (once P_i is
-// stored), S_{i+2} into buffer i % 2 (the pipe runs them in order, so PV_i
-// has read P_i by then): the scores of pair i + 1 are computed while pair i
+// TMEM columns: O [0, d), score buffers S_j [128 + 128 j, +128) for j < 3
+// (unit u's scores in [64 u, +64), then its P as bf16 pairs in [64 u,
+// +32)).  Q sits in shared memory (one TMA load per tile), so every S = Q K^T
+// chain reads both operands from there.  S of pair i goes to buffer i % 3.
+// The MMA order is S0 S1 S2, then per pair i: PV_i (once P_i is stored),
+// S_{i+3} into buffer i % 3 (the pipe runs them in order, so PV_i has read
+// P_i by then): the scores of the next two pairs are computed while pair i
 // is in softmax.  P_i overwrites scores the softmax already holds, so it is
 // stored without waiting for any PV.  The row's reference maximum is lazy
 // (it moves only for the row's first entries or an entry 2^64 above it); the
 // two threads of a row agree on it through a named barrier of their two
 // warps, and before O is rescaled every PV issued so far has completed.
 //
-// Shared memory: a ring of slots that each hold K or V of one pair (128 rows),
-// filled and released in the MMA's order K0 K1 V0 K2 V1 K3 ..., and a ring of
-// per-pair mask records.
+// Shared memory: the tile's Q, a ring of five slots that each hold K or V
+// of one pair (128 rows), filled and released in the MMA's order K0 K1 K2
+// V0 K3 V1 K4 ..., and a ring of per-pair mask records.
 #include "vs_internal.h"
 #include "vs_kernel_common.cuh"
 
@@ -45,10 +44,10 @@ constexpr int kFwdRecWarp = 10;
 constexpr int kFwdVWarp = 11;
 constexpr int kFwdSoftmax = 256;  // softmax threads (warps 2-9): two per row, one per unit of a pair
 constexpr int kPairKeys = 2 * kKTile;
-constexpr int kFwdSlots = 6;
+constexpr int kFwdSlots = 5;
 constexpr int kRecRing = 8;
-constexpr int kSBufs = 2;  // score buffers: S of pair i + 1 is computed while pair i is in softmax
-constexpr uint32_t kColO = 0, kColS = 128, kColQ = 128 + 128 * kSBufs, kTmemCols = 512;
+constexpr int kSBufs = 3;  // score buffers: S of pair i + 3 is issued right after pair i's PV
+constexpr uint32_t kColO = 0, kColS = 128, kTmemCols = 512;
 constexpr float kRefSlack = 18446744073709551616.0f;  // 2^64: largest masked pair sum accepted against the reference
 
 // What a unit's 128 row masks are cut from (written by the loader).
@@ -95,8 +94,9 @@ template <int D>
 struct FwdSmem {
   static constexpr int NH = D / 64;
   uint8_t slot[kFwdSlots][NH][kPairKeys * 128];  // K or V of one pair, 128B-swizzled, per d-half
+  uint8_t q[NH][kQTile * 128];                    // the tile's Q: A operand of every S = Q K^T
   MaskRec rec[kRecRing][2];                      // mask records of a pair's two units
-  uint64_t q_tmem;  // Q rows written to TMEM by the softmax threads
+  uint64_t q_full;  // the tile's Q (TMA)
   uint64_t slot_full[kFwdSlots], slot_empty[kFwdSlots];
   uint64_t rec_full[kRecRing], rec_empty[kRecRing];
   uint64_t s_full[kSBufs], p_full[kSBufs];  // per score buffer
@@ -182,7 +182,8 @@ __device__ __noinline__ void fwd_scale_o(uint32_t taddr, int ncols, float alpha)
 // The kernel body, compiled once per mask reading (BLOCK: block-cover
 // slashes) so that neither reading carries the other's code.
 template <int D, bool BLOCK>
-__device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorMap& tmV, const FwdParams& p) {
+__device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
+                                         const CUtensorMap& tmQp, const FwdParams& p) {
   constexpr int NH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& s = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -230,7 +231,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
     if (!arena_ok && av.hdr->status) raise_error(p.err, av.hdr->status);
     else if (!arena_ok && av.hdr->magic != kArenaMagic) raise_error(p.err, VS_ERR_ARG);
     s.abort_flag = 0;
-    mbar_init(&s.q_tmem, kFwdSoftmax);
+    mbar_init(&s.q_full, 1);
     for (int i = 0; i < kFwdSlots; ++i) {
       mbar_init(&s.slot_full[i], 1);
       mbar_init(&s.slot_empty[i], 1);
@@ -273,6 +274,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
       if (lane == 0) {
         if (my_kind == 0) {
           prefetch_tmap(&tmK);
+          // the tile's Q: R tokens of one head, or of the gp heads of a group
+          mbar_arrive_expect_tx(&s.q_full, NH * kQTile * 128);
+          for (int hf = 0; hf < NH; ++hf) tma_load_4d(s.q[hf], gp ? &tmQp : &tmQ, &s.q_full, 64 * hf, h, int(r0), b);
         } else {
           prefetch_tmap(&tmV);
         }
@@ -337,6 +341,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         issued[sl] = cb;
         __syncwarp();
       });
+    }
+    if (lane == 0 && s.abort_flag && my_kind == 0 && P > 0) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(&s.q_full, 0) && global_ns() - t0 < kWaitBudgetNs) {
+      }
     }
     if (lane == 0 && s.abort_flag) {
       // drain loads still in flight before the CTA's shared memory is released
@@ -456,9 +465,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // S of pair i goes to score buffer i % 2.  Order: S0, S1, then per pair
-    // i: PV_i (once its P is in buffer i % 2), S_{i+2} into the same buffer
-    // (the tensor pipe runs them in order, so PV_i has read P_i).  The
+    // S of pair i goes to score buffer i % 3.  Order: S0, S1, S2, then per
+    // pair i: PV_i (once its P is in buffer i % 3), S_{i+3} into the same
+    // buffer (the tensor pipe runs them in order, so PV_i has read P_i).  The
     // whole warp runs the loop; one elected lane issues.
     if (P > 0) {
       const uint32_t idS = idesc_bf16(128, kPairKeys, 0, 0);
@@ -470,7 +479,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
       const uint64_t dk0 = sdesc_sw128(smem_u32(s.slot[0][0]), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_u32(s.slot[0][0]), kPairKeys * 128, 1024);
       constexpr uint32_t kSlotDesc = uint32_t(NH * kPairKeys * 128) >> 4;
-      bool ok = mbar_wait_warp(&s.q_tmem, 0, ab, VS_ERR_TIMEOUT);
+      const uint64_t dq0 = sdesc_sw128(smem_u32(s.q[0]), 16, 1024);
+      bool ok = mbar_wait_warp(&s.q_full, 0, ab, VS_ERR_TIMEOUT);
       int c = 0;
       for_each_block(P, [&](int kind, int i) {
         if (!ok) return;
@@ -484,12 +494,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
         tc_fence_after();
         if (!kind) {
           const uint64_t dks = dk0 + uint64_t(sl) * kSlotDesc;
-          // four K-chunks of 16 per elect; A = Q in TMEM
+          // A = Q, B = K, both in shared memory; one K-chunk of 16 per MMA
 #pragma unroll
-          for (int k4 = 0; k4 < D / 64; ++k4) {
-            const uint64_t b = dks + (uint32_t(k4 * kPairKeys * 128) >> 4);
-            const uint32_t a = tmem + kColQ + k4 * 32;
-            mma_ts_chain4_warp(tmem + kColS + 128 * j, a, a + 8, a + 16, a + 24, b, b + 2, b + 4, b + 6, idS, k4 > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = dq0 + (uint32_t((kk / 4) * kQTile * 128 + (kk % 4) * 32) >> 4);
+            const uint64_t bk = dks + (uint32_t((kk / 4) * kPairKeys * 128 + (kk % 4) * 32) >> 4);
+            mma_ss_warp(tmem + kColS + 128 * j, a, bk, idS, kk > 0);
           }
           mma_commit_warp(&s.s_full[j]);
         } else {
@@ -531,26 +541,6 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     const int64_t n_g = qpos_g(G, n_loc);
-    if (P > 0) {
-      // the row's Q, columns [half d/2, (half + 1) d/2), into TMEM as bf16
-      // pairs: the A operand of every S = Q K^T chain of the tile
-      uint32_t w[D / 4];
-      const uint8_t* src = p.q + (int64_t(b) * p.sq[0] + n_loc * p.sq[1] + int64_t(hrow) * p.sq[2]) * 2 + half * D;
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        const uint4 x = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
-        w[4 * c] = x.x;
-        w[4 * c + 1] = x.y;
-        w[4 * c + 2] = x.z;
-        w[4 * c + 3] = x.w;
-      }
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tmem_st16(tl + kColQ + half * (D / 4) + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&w[16 * c]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&s.q_tmem);
-    }
     // A unit's row mask is cut from its record (published well ahead) one
     // pair early: the mask of pair i + 1 while the scores of pair i are on
     // their way from TMEM, so the record's shared-memory latency is hidden.
@@ -770,18 +760,24 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tmK, const CUtensorM
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmK, tmV, p);
-  else fwd_body<D, false>(tmK, tmV, p);
+    vs_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQp, const FwdParams p) {
+  if (arena_view(p.arena).hdr->block_cover) fwd_body<D, true>(tmK, tmV, tmQ, tmQp, p);
+  else fwd_body<D, false>(tmK, tmV, tmQ, tmQp, p);
 }
 
 template <int D>
 vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const void* v, const void* arena,
                        float scale, void* o, float* lse, float* o_acc, int* err, cudaStream_t st) {
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq, tqp;
   vs_status rc;
   if ((rc = make_tmap_bshd(&tk, k, sh->B, sh->Nk, sh->Hkv, D, sh->sk, kKTile)) != VS_OK) return rc;
   if ((rc = make_tmap_bshd(&tv, v, sh->B, sh->Nk, sh->Hkv, D, sh->sv, kKTile)) != VS_OK) return rc;
+  // Q tiles: 128 rows of one head, or (GQA packing) 128 / g tokens of the g
+  // heads of a KV group, token-major with the heads inside
+  const int g = sh->Hq / sh->Hkv, gq = (kQTile % g == 0) ? g : 1;
+  if ((rc = make_tmap_bshd(&tq, q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile)) != VS_OK) return rc;
+  if ((rc = make_tmap_bshd(&tqp, q, sh->B, sh->Nq, sh->Hq, D, sh->sq, kQTile / gq, gq)) != VS_OK) return rc;
   FwdParams p;
   p.arena = arena;
   p.q = static_cast<const uint8_t*>(q);
@@ -808,7 +804,7 @@ vs_status launch_fwd_d(const vs_shape* sh, const void* q, const void* k, const v
   const int T = (sh->Nq + kQTile - 1) / kQTile;
   const dim3 grid(unsigned(T) * sh->B * sh->Hq);
   trace_begin("fwd", st);
-  vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tk, tv, p);
+  vs_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tk, tv, tq, tqp, p);
   trace_end(st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? VS_OK : VS_ERR_CUDA;
